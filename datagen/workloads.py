@@ -1,0 +1,83 @@
+"""The five synthetic workloads of the MaxSim operator, as seeded host arrays.
+
+Shapes and distributions follow the workloads the pages measure (ColBERT
+reranking, ColPali cross products, contrastive training, INT8 visual rerank);
+no dataset item is reproduced: every value is drawn from the seeded
+generators in this package.
+
+ tiny_rerank      Q [1,32,128] f16, D [1000,180,128] f16, no masks, seed 0
+ colbert_varlen   Q [32,32,128] f16, D packed with cu_seqlens, Ld ~ U{32..300},
+                  Nd = 100,000, seed 2
+ colpali_cross    Q [128,128,128] bf16, D [128,1024,128] bf16, q_mask drops the
+                  last k ~ U{0..40} query tokens, d_mask hides a random subset of
+                  k ~ U{0..200} doc patches, seed 3
+ contrastive_bwd  Q [64,128,128] bf16, D [64,1024,128] bf16, grad [64,64] f32
+                  N(0,1), seed 4
+ int8_rerank      Q int8 [1,1024,128] + scales, D int8 [10000,1024,128] + scales,
+                  seed 5
+Every row is an l2-normalised Gaussian vector rounded once to its storage type.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import (TID_D, TID_DMASK, TID_GRAD, TID_LEN_D, TID_Q, TID_QMASK, gaussian_rows, int8_rows,
+               mask_drop_tail, mask_random_subset, normal_f32, uniform_int)
+
+SPECS = {
+    "tiny_rerank": dict(Nq=1, Lq=32, Nd=1000, Ld=180, dim=128, dtype="f16", seed=0),
+    "colbert_varlen": dict(Nq=32, Lq=32, Nd=100_000, ld_min=32, ld_max=300, dim=128, dtype="f16", seed=2),
+    "colpali_cross": dict(Nq=128, Lq=128, Nd=128, Ld=1024, dim=128, dtype="bf16", seed=3,
+                          q_drop_max=40, d_hide_max=200),
+    "contrastive_bwd": dict(Nq=64, Lq=128, Nd=64, Ld=1024, dim=128, dtype="bf16", seed=4),
+    "int8_rerank": dict(Nq=1, Lq=1024, Nd=10_000, Ld=1024, dim=128, seed=5),
+}
+
+
+def dense(Nq, Lq, Nd, Ld, dim, dtype, seed, q_drop_max=None, d_hide_max=None, grad=False):
+    """Dense Q [Nq,Lq,dim] and D [Nd,Ld,dim] (+ optional masks / gradient)."""
+    w = dict(Nq=Nq, Lq=Lq, Nd=Nd, Ld=Ld, dim=dim, dtype=dtype, seed=seed)
+    w["Q"] = gaussian_rows(seed, TID_Q, Nq * Lq, dim, dtype).reshape(Nq, Lq, dim)
+    w["D"] = gaussian_rows(seed, TID_D, Nd * Ld, dim, dtype).reshape(Nd, Ld, dim)
+    w["q_mask"] = mask_drop_tail(seed, TID_QMASK, Nq, Lq, q_drop_max) if q_drop_max is not None else None
+    w["d_mask"] = mask_random_subset(seed, TID_DMASK, Nd, Ld, d_hide_max) if d_hide_max is not None else None
+    w["grad"] = normal_f32(seed, TID_GRAD, Nq * Nd).reshape(Nq, Nd) if grad else None
+    return w
+
+
+def varlen(Nq, Lq, Nd, ld_min, ld_max, dim, dtype, seed):
+    """Dense Q [Nq,Lq,dim]; D packed [sum Ld, dim] with int32 cu_seqlens [Nd+1]."""
+    w = dict(Nq=Nq, Lq=Lq, Nd=Nd, dim=dim, dtype=dtype, seed=seed)
+    lens = uniform_int(seed, TID_LEN_D, Nd, ld_min, ld_max)
+    cu = np.zeros(Nd + 1, dtype=np.int64)
+    np.cumsum(lens, out=cu[1:])
+    assert cu[-1] < 2**31
+    w["lens"] = lens
+    w["cu_seqlens_d"] = cu.astype(np.int32)
+    w["total_d"] = int(cu[-1])
+    w["max_ld"] = int(lens.max()) if Nd else 0
+    w["Q"] = gaussian_rows(seed, TID_Q, Nq * Lq, dim, dtype).reshape(Nq, Lq, dim)
+    w["D"] = gaussian_rows(seed, TID_D, int(cu[-1]), dim, dtype)
+    return w
+
+
+def int8(Nq, Lq, Nd, Ld, dim, seed):
+    """INT8 Q/D with one float32 scale per token (per-token symmetric)."""
+    w = dict(Nq=Nq, Lq=Lq, Nd=Nd, Ld=Ld, dim=dim, seed=seed)
+    q, qs = int8_rows(seed, TID_Q, Nq * Lq, dim)
+    d, ds = int8_rows(seed, TID_D, Nd * Ld, dim)
+    w["Q"], w["q_scale"] = q.reshape(Nq, Lq, dim), qs.reshape(Nq, Lq)
+    w["D"], w["d_scale"] = d.reshape(Nd, Ld, dim), ds.reshape(Nd, Ld)
+    return w
+
+
+def make(name: str, **overrides):
+    """Build a named workload; keyword overrides shrink it for quick tests."""
+    spec = dict(SPECS[name])
+    spec.update(overrides)
+    if name == "colbert_varlen":
+        return varlen(**spec)
+    if name == "int8_rerank":
+        return int8(**spec)
+    grad = name == "contrastive_bwd"
+    return dense(**spec, grad=grad)

@@ -1,0 +1,180 @@
+"""CPU oracle for the MaxSim operator -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, double-precision restatement of the operator (``maxsim_oracle.c``)
+with a numpy-facing ctypes wrapper. Only the tests, the smoke check and the
+benchmark's CPU-baseline leg may import this package; the CUDA library never
+calls it and shares no code with it.
+
+Functions
+  fwd_packed / fwd_dense : scores, argmax (lowest index, -1 if no valid token)
+                           and the top-2 gap of every query row
+  fwd_int8               : INT8 x INT8 scores with per-token scales, argmax,
+                           and the int32 dot product at the argmax
+  csr                    : inverse-argmax CSR (row_ptr, col)
+  bwd                    : dQ, dD through the saved argmax (+ the CSR)
+See the C source for the page sections each one follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "maxsim_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPES = {"f16": 0, "bf16": 1, "f64": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc -O2 -fopenmp) next to its source."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+            lib.oracle_fwd.argtypes = [vp, vp, ci, i64, vp, i64, vp, i64, vp, vp, vp, i64, vp, vp, vp, i64, ci]
+            lib.oracle_fwd_int8.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, i64, vp, vp, vp,
+                                            vp, ci]
+            lib.oracle_csr.argtypes = [vp, i64, i64, i64, i64, vp, vp]
+            lib.oracle_bwd.argtypes = [vp, vp, ci, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, ci]
+            for f in (lib.oracle_fwd, lib.oracle_fwd_int8, lib.oracle_csr, lib.oracle_bwd, lib.oracle_max_threads):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+def _check_dtype(x, dtype):
+    want = np.float64 if dtype == "f64" else np.uint16
+    assert x.dtype == want, f"{dtype} inputs are passed as {want.__name__}"
+
+
+def fwd_packed(Q, q_off, D, d_off, dtype, q_mask=None, d_mask=None, docs=None, lq_stride=None, threads=0):
+    """MaxSim over packed rows.
+
+    Q [total_q, dim], D [total_d, dim] (uint16 bits for f16/bf16, float64 for f64);
+    q_off [Nq+1], d_off [Nd+1] row offsets; masks one byte per packed row.
+    docs: optional subset of document indices to score.
+    Returns (scores [Nq, n_sel] f64, argmax [Nq*n_sel, lq_stride] i32, gap f64).
+    """
+    _check_dtype(Q, dtype)
+    _check_dtype(D, dtype)
+    dim = Q.shape[-1]
+    assert D.shape[-1] == dim
+    q_off = np.ascontiguousarray(q_off, dtype=np.int64)
+    d_off = np.ascontiguousarray(d_off, dtype=np.int64)
+    Nq, Nd = len(q_off) - 1, len(d_off) - 1
+    docs_arr = None if docs is None else np.ascontiguousarray(docs, dtype=np.int64)
+    n_sel = Nd if docs_arr is None else len(docs_arr)
+    if lq_stride is None:
+        lq_stride = int(np.max(np.diff(q_off))) if Nq else 0
+    scores = np.zeros((Nq, n_sel), dtype=np.float64)
+    argmax = np.zeros((Nq * n_sel, lq_stride), dtype=np.int32)
+    gap = np.zeros((Nq * n_sel, lq_stride), dtype=np.float64)
+    qm = None if q_mask is None else np.ascontiguousarray(q_mask, dtype=np.uint8).reshape(-1)
+    dm = None if d_mask is None else np.ascontiguousarray(d_mask, dtype=np.uint8).reshape(-1)
+    Qc, Dc = np.ascontiguousarray(Q), np.ascontiguousarray(D)
+    rc = _load().oracle_fwd(_p(Qc), _p(Dc), DTYPES[dtype], Nq, _p(q_off), Nd, _p(d_off), dim, _p(qm), _p(dm),
+                            _p(docs_arr), n_sel, _p(scores), _p(argmax), _p(gap), lq_stride, threads)
+    if rc:
+        raise ValueError(f"oracle_fwd failed ({rc})")
+    return scores, argmax, gap
+
+
+def fwd_dense(Q, D, dtype, q_mask=None, d_mask=None, docs=None, threads=0):
+    """MaxSim for dense Q [Nq,Lq,dim], D [Nd,Ld,dim]; masks [Nq,Lq] / [Nd,Ld]."""
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, _ = D.shape
+    q_off = np.arange(Nq + 1, dtype=np.int64) * Lq
+    d_off = np.arange(Nd + 1, dtype=np.int64) * Ld
+    return fwd_packed(Q.reshape(Nq * Lq, dim), q_off, D.reshape(Nd * Ld, dim), d_off, dtype, q_mask, d_mask,
+                      docs, lq_stride=Lq, threads=threads)
+
+
+def fwd_int8(Q, q_scale, D, d_scale, q_mask=None, d_mask=None, docs=None, threads=0):
+    """INT8 x INT8 MaxSim. Q int8 [Nq,Lq,dim], D int8 [Nd,Ld,dim], scales f32 per token.
+
+    Returns (scores f64 [Nq, n_sel], argmax, win_dot int32, gap).
+    """
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, _ = D.shape
+    docs_arr = None if docs is None else np.ascontiguousarray(docs, dtype=np.int64)
+    n_sel = Nd if docs_arr is None else len(docs_arr)
+    scores = np.zeros((Nq, n_sel), dtype=np.float64)
+    argmax = np.zeros((Nq * n_sel, Lq), dtype=np.int32)
+    win = np.zeros((Nq * n_sel, Lq), dtype=np.int32)
+    gap = np.zeros((Nq * n_sel, Lq), dtype=np.float64)
+    qm = None if q_mask is None else np.ascontiguousarray(q_mask, dtype=np.uint8)
+    dm = None if d_mask is None else np.ascontiguousarray(d_mask, dtype=np.uint8)
+    args = [np.ascontiguousarray(a) for a in (Q, q_scale.astype(np.float32), D, d_scale.astype(np.float32))]
+    rc = _load().oracle_fwd_int8(_p(args[0]), _p(args[1]), _p(args[2]), _p(args[3]), Nq, Lq, Nd, Ld, dim, _p(qm),
+                                 _p(dm), _p(docs_arr), n_sel, _p(scores), _p(argmax), _p(win), _p(gap), threads)
+    if rc == 2:
+        raise OverflowError("an INT8 dot product does not fit int32")
+    if rc:
+        raise ValueError(f"oracle_fwd_int8 failed ({rc})")
+    return scores, argmax, win, gap
+
+
+def csr(argmax, Nq, Lq, Nd, Ld):
+    """Inverse-argmax CSR: (row_ptr [Nd*Ld+1], col [#non-sentinel sources])."""
+    a = np.ascontiguousarray(argmax, dtype=np.int32).reshape(-1)
+    assert a.size == Nq * Nd * Lq
+    row_ptr = np.zeros(Nd * Ld + 1, dtype=np.int32)
+    col = np.zeros(max(1, a.size), dtype=np.int32)
+    rc = _load().oracle_csr(_p(a), Nq, Lq, Nd, Ld, _p(row_ptr), _p(col))
+    if rc == 3:
+        raise ValueError("argmax outside [-1, Ld)")
+    if rc:
+        raise ValueError(f"oracle_csr failed ({rc})")
+    return row_ptr, col[: row_ptr[-1]].copy()
+
+
+def bwd(Q, D, dtype, argmax, grad, q_mask=None, threads=0):
+    """dQ [Nq,Lq,dim], dD [Nd,Ld,dim] (float64) and the CSR, for dense Q / D."""
+    _check_dtype(Q, dtype)
+    _check_dtype(D, dtype)
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, _ = D.shape
+    a = np.ascontiguousarray(argmax, dtype=np.int32).reshape(-1)
+    g = np.ascontiguousarray(grad, dtype=np.float32).reshape(-1)
+    assert g.size == Nq * Nd
+    dQ = np.zeros((Nq, Lq, dim), dtype=np.float64)
+    dD = np.zeros((Nd, Ld, dim), dtype=np.float64)
+    row_ptr = np.zeros(Nd * Ld + 1, dtype=np.int32)
+    col = np.zeros(max(1, a.size), dtype=np.int32)
+    qm = None if q_mask is None else np.ascontiguousarray(q_mask, dtype=np.uint8)
+    Qc, Dc = np.ascontiguousarray(Q), np.ascontiguousarray(D)
+    rc = _load().oracle_bwd(_p(Qc), _p(Dc), DTYPES[dtype], Nq, Lq, Nd, Ld, dim, _p(qm), _p(a), _p(g), _p(dQ),
+                            _p(dD), _p(row_ptr), _p(col), threads)
+    if rc == 3:
+        raise ValueError("argmax outside [-1, Ld)")
+    if rc:
+        raise ValueError(f"oracle_bwd failed ({rc})")
+    return dQ, dD, row_ptr, col[: row_ptr[-1]].copy()

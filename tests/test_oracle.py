@@ -1,0 +1,325 @@
+"""Pins for the CPU oracle: hand-worked values, an independent brute force,
+closed forms, invariants and finite differences (no GPU)."""
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+# ---------------------------------------------------------------- hand-worked values
+
+def test_hand_two_by_three(golden):
+    ex = golden["two_by_three"]
+    Q, D = f64(ex["Q"]), f64(ex["D"])
+    for case in ex["cases"]:
+        qm = None if case["q_mask"] is None else np.array(case["q_mask"], dtype=np.uint8)
+        dm = None if case["d_mask"] is None else np.array(case["d_mask"], dtype=np.uint8)
+        for dtype in ("f64", "f16", "bf16"):
+            Qx = Q if dtype == "f64" else datagen.float_to_bits(Q, dtype)
+            Dx = D if dtype == "f64" else datagen.float_to_bits(D, dtype)
+            s, a, _ = oracle.fwd_dense(Qx, Dx, dtype, q_mask=qm, d_mask=dm)
+            assert s[0, 0] == case["score"], (case["name"], dtype)
+            assert a[0].tolist() == case["argmax"], (case["name"], dtype)
+
+
+def test_hand_backward(golden):
+    ex = golden["two_by_three"]
+    Q, D = f64(ex["Q"]), f64(ex["D"])
+    _, a, _ = oracle.fwd_dense(Q, D, "f64")
+    dQ, dD, rp, col = oracle.bwd(Q, D, "f64", a, np.ones((1, 1), np.float32))
+    bw = ex["backward_g1"]
+    assert np.array_equal(dQ, f64(bw["dQ"]))
+    assert np.array_equal(dD, f64(bw["dD"]))
+    assert rp.tolist() == bw["row_ptr"]
+    assert col.tolist() == bw["col"]
+
+
+def test_negative_scores_masked_before_max(golden):
+    ex = golden["negative_scores"]
+    Q, D = f64(ex["Q"]), f64(ex["D"])
+    for case in ex["cases"]:
+        dm = None if case["d_mask"] is None else np.array(case["d_mask"], dtype=np.uint8)
+        s, a, _ = oracle.fwd_dense(Q, D, "f64", d_mask=dm)
+        assert s[0, 0] == case["score"]
+        assert a[0].tolist() == case["argmax"]
+
+
+def test_tie_lowest_index(golden):
+    ex = golden["tie"]
+    s, a, g = oracle.fwd_dense(f64(ex["Q"]), f64(ex["D"]), "f64")
+    assert s[0, 0] == ex["score"] and a[0].tolist() == ex["argmax"] and g[0].tolist() == ex["gap"]
+
+
+def test_all_masked_doc_sentinel(golden):
+    ex = golden["all_masked_doc"]
+    s, a, g = oracle.fwd_dense(f64(ex["Q"]), f64(ex["D"]), "f64", d_mask=np.array(ex["d_mask"], np.uint8))
+    assert s[0, 0] == ex["score"] and a[0].tolist() == ex["argmax"]
+    assert np.all(np.isinf(g))
+    # the backward routes nothing through a sentinel
+    dQ, dD, rp, col = oracle.bwd(f64(ex["Q"]), f64(ex["D"]), "f64", a, np.ones((1, 1), np.float32))
+    assert not dQ.any() and not dD.any() and rp[-1] == 0 and col.size == 0
+
+
+def test_int8_scale_flip(golden):
+    ex = golden["int8_scale_flip"]
+    Q = np.array(ex["Q"], np.int8)
+    D = np.array(ex["D"], np.int8)
+    s, a, w, _ = oracle.fwd_int8(Q, np.array(ex["q_scale"], np.float32), D, np.array(ex["d_scale"], np.float32))
+    assert abs(s[0, 0] - ex["score"]) < 1e-12  # 0.1 is not exact in binary
+    assert a[0].tolist() == ex["argmax"] and w[0].tolist() == ex["win_dot"]
+
+
+# ---------------------------------------------------------------- decoders
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_decoder_matches_numpy_on_all_finite_patterns(dtype):
+    # Every finite bit pattern, decoded by the oracle (via a 1x1 product with 1.0)
+    # must equal numpy's own conversion of the same bits.
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = datagen.bits_to_float(bits, dtype)
+    keep = np.isfinite(vals)
+    bits, vals = bits[keep], vals[keep]
+    n = bits.size
+    Q = bits.reshape(n, 1, 1).copy()
+    one = datagen.float_to_bits(np.ones((1, 1, 1)), dtype)
+    s, _, _ = oracle.fwd_dense(Q, one, dtype)
+    assert np.array_equal(s[:, 0], vals)
+
+
+# ---------------------------------------------------------------- brute force
+
+def brute_force(Qf, Df, q_mask=None, d_mask=None):
+    """Independent einsum-then-reduce restatement: materialise S, mask, max, sum."""
+    S = np.einsum("isk,jtk->ijst", Qf, Df)  # [Nq, Nd, Lq, Ld]
+    if d_mask is not None:
+        S = np.where(d_mask[None, :, None, :].astype(bool), S, -np.inf)
+    m = S.max(axis=3) if S.shape[3] else np.full(S.shape[:3], -np.inf)
+    arg = np.where(np.isfinite(m), S.argmax(axis=3) if S.shape[3] else 0, -1)
+    active = np.ones(Qf.shape[:2], bool) if q_mask is None else q_mask.astype(bool)
+    contrib = np.where(np.isfinite(m) & active[:, None, :], m, 0.0)
+    return contrib.sum(axis=2), arg.reshape(-1, Qf.shape[1])
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_brute_force_tiny(seed, dtype):
+    rng = np.random.default_rng(seed)
+    Nq, Nd = rng.integers(1, 4, size=2)
+    Lq, Ld = rng.integers(1, 8, size=2)
+    dim = int(rng.integers(1, 9))
+    Q = datagen.gaussian_rows(100 + seed, 1, Nq * Lq, dim, dtype).reshape(Nq, Lq, dim)
+    D = datagen.gaussian_rows(100 + seed, 2, Nd * Ld, dim, dtype).reshape(Nd, Ld, dim)
+    qm = (rng.random((Nq, Lq)) > 0.3).astype(np.uint8)
+    dm = (rng.random((Nd, Ld)) > 0.3).astype(np.uint8)
+    Qf, Df = datagen.bits_to_float(Q, dtype), datagen.bits_to_float(D, dtype)
+    for q_mask, d_mask in ((None, None), (qm, None), (None, dm), (qm, dm)):
+        s, a, g = oracle.fwd_dense(Q, D, dtype, q_mask=q_mask, d_mask=d_mask)
+        bs, ba = brute_force(Qf, Df, q_mask, d_mask)
+        np.testing.assert_allclose(s, bs, rtol=1e-12, atol=1e-12)
+        clear = g > 1e-9
+        assert np.array_equal(a[clear], ba[clear])
+        assert np.array_equal(a == -1, ba == -1)
+
+
+def test_top2_gap_is_max_minus_second():
+    rng = np.random.default_rng(7)
+    Q = f64(rng.standard_normal((2, 3, 4)))
+    D = f64(rng.standard_normal((3, 5, 4)))
+    _, _, g = oracle.fwd_dense(Q, D, "f64")
+    S = np.einsum("isk,jtk->ijst", Q, D)
+    top = np.sort(S, axis=3)
+    np.testing.assert_allclose(g.reshape(2, 3, 3), top[..., -1] - top[..., -2], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_single_doc_token_closed_form():
+    rng = np.random.default_rng(1)
+    Q = f64(rng.standard_normal((3, 6, 8)))
+    D = f64(rng.standard_normal((4, 1, 8)))
+    s, a, _ = oracle.fwd_dense(Q, D, "f64")
+    np.testing.assert_allclose(s, Q.sum(axis=1) @ D[:, 0, :].T, rtol=1e-12, atol=1e-12)
+    assert (a == 0).all()
+
+
+def test_single_query_token_closed_form():
+    rng = np.random.default_rng(2)
+    Q = f64(rng.standard_normal((1, 1, 16)))
+    D = f64(rng.standard_normal((5, 9, 16)))
+    s, a, _ = oracle.fwd_dense(Q, D, "f64")
+    mv = D @ Q[0, 0]  # [Nd, Ld] textbook mat-vec
+    np.testing.assert_allclose(s[0], mv.max(axis=1), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(a[:, 0], mv.argmax(axis=1))
+
+
+def test_positive_homogeneity():
+    rng = np.random.default_rng(3)
+    Q = f64(rng.standard_normal((2, 4, 8)))
+    D = f64(rng.standard_normal((3, 7, 8)))
+    s1, a1, _ = oracle.fwd_dense(Q, D, "f64")
+    s2, a2, _ = oracle.fwd_dense(f64(2.0 * Q), D, "f64")
+    assert np.array_equal(s2, 2.0 * s1) and np.array_equal(a1, a2)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_chunking_identity():
+    # Splitting Q into 128-token chunks and summing the chunk scores equals the
+    # full score (design notes, "Long-query chunking").
+    Nq, Lq, Nd, Ld, dim = 2, 1024, 3, 40, 16
+    Q = datagen.gaussian_rows(5, 1, Nq * Lq, dim, "bf16").reshape(Nq, Lq, dim)
+    D = datagen.gaussian_rows(5, 2, Nd * Ld, dim, "bf16").reshape(Nd, Ld, dim)
+    qm = datagen.mask_drop_tail(5, 4, Nq, Lq, 300)
+    full, a_full, _ = oracle.fwd_dense(Q, D, "bf16", q_mask=qm)
+    nc = Lq // 128
+    sc, a_c, _ = oracle.fwd_dense(Q.reshape(Nq * nc, 128, dim), D, "bf16", q_mask=qm.reshape(Nq * nc, 128))
+    np.testing.assert_allclose(sc.reshape(Nq, nc, Nd).sum(axis=1), full, rtol=0, atol=1e-12)
+    # argmax in original token layout
+    a_c = a_c.reshape(Nq, nc, Nd, 128).transpose(0, 2, 1, 3).reshape(Nq * Nd, Lq)
+    assert np.array_equal(a_c, a_full)
+
+
+def test_mask_invariants():
+    Nq, Lq, Nd, Ld, dim = 3, 9, 4, 13, 8
+    Q = datagen.gaussian_rows(9, 1, Nq * Lq, dim, "f16").reshape(Nq, Lq, dim)
+    D = datagen.gaussian_rows(9, 2, Nd * Ld, dim, "f16").reshape(Nd, Ld, dim)
+    base, a0, _ = oracle.fwd_dense(Q, D, "f16")
+    ones_s, ones_a, _ = oracle.fwd_dense(Q, D, "f16", q_mask=np.ones((Nq, Lq), np.uint8),
+                                         d_mask=np.ones((Nd, Ld), np.uint8))
+    assert np.array_equal(base, ones_s) and np.array_equal(a0, ones_a)
+    # trailing d_mask of k tokens == varlen documents of length Ld - k
+    k = np.array([0, 3, Ld, 5])
+    dm = np.ones((Nd, Ld), np.uint8)
+    for j in range(Nd):
+        dm[j, Ld - k[j]:] = 0
+    ms, ma, _ = oracle.fwd_dense(Q, D, "f16", d_mask=dm)
+    lens = Ld - k
+    rows = np.concatenate([D[j, :lens[j]] for j in range(Nd)]).reshape(-1, dim)
+    d_off = np.concatenate([[0], np.cumsum(lens)])
+    q_off = np.arange(Nq + 1) * Lq
+    vs, va, _ = oracle.fwd_packed(Q.reshape(-1, dim), q_off, rows, d_off, "f16")
+    assert np.array_equal(ms, vs) and np.array_equal(ma, va)
+    assert (vs[:, 2] == 0).all() and (va.reshape(Nq, Nd, Lq)[:, 2] == -1).all()  # empty doc
+    # q_mask = 0 on a row == deleting the row
+    qm = np.ones((Nq, Lq), np.uint8)
+    qm[:, 4] = 0
+    s_masked, _, _ = oracle.fwd_dense(Q, D, "f16", q_mask=qm)
+    s_del, _, _ = oracle.fwd_dense(np.ascontiguousarray(np.delete(Q, 4, axis=1)), D, "f16")
+    assert np.array_equal(s_masked, s_del)
+    # permuting document tokens permutes the argmax and keeps the score
+    perm = np.random.default_rng(0).permutation(Ld)
+    ps, pa, pg = oracle.fwd_dense(Q, np.ascontiguousarray(D[:, perm]), "f16")
+    np.testing.assert_allclose(ps, base, rtol=0, atol=1e-12)
+    clear = pg > 0
+    assert np.array_equal(perm[pa[clear]], a0[clear])
+
+
+# ---------------------------------------------------------------- INT8
+
+def test_int8_brute_force():
+    Nq, Lq, Nd, Ld, dim = 2, 5, 3, 11, 32
+    q, qs = datagen.int8_rows(11, 1, Nq * Lq, dim)
+    d, ds = datagen.int8_rows(11, 2, Nd * Ld, dim)
+    dm = (np.random.default_rng(3).random((Nd, Ld)) > 0.2).astype(np.uint8)
+    Q, D = q.reshape(Nq, Lq, dim), d.reshape(Nd, Ld, dim)
+    s, a, w, _ = oracle.fwd_int8(Q, qs.reshape(Nq, Lq), D, ds.reshape(Nd, Ld), d_mask=dm)
+    dots = np.einsum("isk,jtk->ijst", Q.astype(np.int64), D.astype(np.int64))
+    v = dots * ds.reshape(Nd, Ld).astype(np.float64)[None, :, None, :]
+    v = np.where(dm[None, :, None, :].astype(bool), v, -np.inf)
+    am = v.argmax(axis=3)
+    want = (v.max(axis=3) * qs.reshape(Nq, Lq).astype(np.float64)[:, None, :]).sum(axis=2)
+    np.testing.assert_allclose(s, want, rtol=1e-12)
+    assert np.array_equal(a.reshape(Nq, Nd, Lq), am)
+    assert np.array_equal(w.reshape(Nq, Nd, Lq), np.take_along_axis(dots, am[..., None], axis=3)[..., 0])
+
+
+def test_int8_quantisation_recipe():
+    q, s = datagen.int8_rows(1, 2, 64, 128)
+    x = datagen.gaussian_rows(1, 2, 64, 128, "f64")
+    assert (np.abs(q).max(axis=1) == 127).all()  # the largest entry maps to +-127
+    np.testing.assert_allclose(s, (np.abs(x).max(axis=1) / 127).astype(np.float32), rtol=0)
+    assert (np.abs(q.astype(np.float64) * s[:, None] - x) <= s[:, None] * 0.5 + 1e-12).all()
+
+
+# ---------------------------------------------------------------- backward
+
+def small_problem(seed=21, Nq=3, Lq=6, Nd=4, Ld=9, dim=8):
+    rng = np.random.default_rng(seed)
+    Q = f64(rng.standard_normal((Nq, Lq, dim)))
+    D = f64(rng.standard_normal((Nd, Ld, dim)))
+    g = rng.standard_normal((Nq, Nd)).astype(np.float32)
+    qm = (rng.random((Nq, Lq)) > 0.25).astype(np.uint8)
+    return Q, D, g, qm
+
+
+def test_backward_euler_identity():
+    # score is positively 1-homogeneous in Q and in D, so
+    # sum <dQ, Q> = sum g * score = sum <dD, D>.
+    Q, D, g, qm = small_problem()
+    s, a, _ = oracle.fwd_dense(Q, D, "f64", q_mask=qm)
+    dQ, dD, _, _ = oracle.bwd(Q, D, "f64", a, g, q_mask=qm)
+    target = float((g.astype(np.float64) * s).sum())
+    assert abs((dQ * Q).sum() - target) < 1e-10
+    assert abs((dD * D).sum() - target) < 1e-10
+
+
+def test_backward_finite_differences():
+    Q, D, g, qm = small_problem(seed=5, Nq=2, Lq=4, Nd=3, Ld=5, dim=4)
+    s, a, gap = oracle.fwd_dense(Q, D, "f64", q_mask=qm)
+    assert gap.min() > 1e-3  # differentiable point for this seed
+    dQ, dD, _, _ = oracle.bwd(Q, D, "f64", a, g, q_mask=qm)
+    gd = g.astype(np.float64)
+
+    def loss(Qx, Dx):
+        return float((gd * oracle.fwd_dense(f64(Qx), f64(Dx), "f64", q_mask=qm)[0]).sum())
+
+    h = 1e-6
+    for idx in np.ndindex(Q.shape):
+        Qp, Qn = Q.copy(), Q.copy()
+        Qp[idx] += h
+        Qn[idx] -= h
+        assert abs((loss(Qp, D) - loss(Qn, D)) / (2 * h) - dQ[idx]) < 1e-6
+    for idx in np.ndindex(D.shape):
+        Dp, Dn = D.copy(), D.copy()
+        Dp[idx] += h
+        Dn[idx] -= h
+        assert abs((loss(Q, Dp) - loss(Q, Dn)) / (2 * h) - dD[idx]) < 1e-6
+
+
+def test_backward_column_sums_and_csr():
+    Q, D, g, qm = small_problem(seed=8, Nq=4, Lq=5, Nd=3, Ld=6)
+    dm = np.ones((3, 6), np.uint8)
+    dm[1] = 0  # a fully masked document produces sentinels
+    s, a, _ = oracle.fwd_dense(Q, D, "f64", q_mask=qm, d_mask=dm)
+    dQ, dD, rp, col = oracle.bwd(Q, D, "f64", a, g, q_mask=qm)
+    Nq, Lq, Nd, Ld = 4, 5, 3, 6
+    # sum_t dD[j,t] = sum_i g_ij sum_s q_mask * Q[i,s]  (for documents with a winner)
+    qsum = (Q * qm[..., None]).sum(axis=1)
+    want = g.astype(np.float64).T @ qsum
+    want[1] = 0
+    np.testing.assert_allclose(dD.sum(axis=1), want, rtol=1e-12, atol=1e-12)
+    # CSR: row_ptr is the exclusive scan of a direct histogram; sources ascend
+    src = np.arange(Nq * Nd * Lq)
+    av = a.reshape(-1)
+    keep = av >= 0
+    dest = ((src // Lq) % Nd) * Ld + av
+    hist = np.bincount(dest[keep], minlength=Nd * Ld)
+    assert np.array_equal(np.diff(rp), hist) and rp[0] == 0 and rp[-1] == keep.sum()
+    assert np.array_equal(col, np.argsort(np.where(keep, dest, Nd * Ld), kind="stable")[: keep.sum()])
+    # dQ gathers exactly one D row per document
+    i, s_ = 2, 3
+    w = qm[i, s_]
+    want_q = sum(g[i, j] * D[j, a[i * Nd + j, s_]] for j in range(Nd) if a[i * Nd + j, s_] >= 0) * w
+    np.testing.assert_allclose(dQ[i, s_], want_q, rtol=1e-12, atol=1e-12)
+
+
+def test_csr_rejects_out_of_range():
+    with pytest.raises(ValueError):
+        oracle.csr(np.array([[0, 7]], np.int32), 1, 2, 1, 3)
