@@ -1,0 +1,180 @@
+/*
+ * maxsim.h -- C ABI of the fused MaxSim library for GB300 (sm_103a).
+ *
+ * The operator (late interaction, ColBERT / ColPali):
+ *
+ *     score[i, j] = sum_s  max_t  < Q[i, s], D[j, t] >
+ *
+ * ("Flash-MaxSim" paper, Sec. 1, Eq. (1); "late-interaction-kernels" design
+ * notes, section "Problem"). The [Lq, Ld] similarity tile of a pair lives only
+ * in tensor memory and registers; it is never written to device memory.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller. Tensors are
+ *    contiguous and row-major with the embedding dimension innermost. Q, D,
+ *    and scale pointers must be 16-byte aligned; row strides are dim elements.
+ *  - Masks are one byte per token, nonzero = active. A masked document token
+ *    is set to -inf before the max; a masked query token contributes 0 to the
+ *    sum (design notes, "Problem" and "Mask handling").
+ *  - argmax uses the lowest index among equal maxima (design notes,
+ *    "Backward"). A query row with no valid document token (an empty or fully
+ *    masked document) contributes 0 and reports argmax -1.
+ *  - Outputs are fully overwritten; callers need not clear them.
+ *  - `workspace` is caller-owned device scratch of at least the size reported
+ *    by maxsim_workspace_size() for the same shape (NULL is allowed when that
+ *    size is 0). The library itself never allocates device memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *    asynchronous; arguments are validated on the host before any launch and
+ *    an invalid call returns an error without launching anything.
+ *  - Device-side checks (a bounded wait that gave up, an out-of-range argmax
+ *    handed to the backward, inconsistent cu_seqlens) never trap: the kernel
+ *    records a code that maxsim_device_status() returns.
+ *  - Sizes are int64; supported: dim a multiple of 16 in [16, 256] for
+ *    f16 / bf16 (a multiple of 32 in [32, 256] for int8); every token count
+ *    below 2^31.
+ */
+#ifndef MAXSIM_H
+#define MAXSIM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MAXSIM_OK = 0,
+    MAXSIM_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, negative size, bad dtype */
+    MAXSIM_ERR_UNSUPPORTED = 2,  /* valid but outside the supported envelope (e.g. dim) */
+    MAXSIM_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed */
+    MAXSIM_ERR_TIMEOUT = 4,      /* device: a bounded wait expired; results are invalid */
+    MAXSIM_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
+    MAXSIM_ERR_DEVICE_INPUT = 6  /* device: an input failed a device-side check */
+} maxsim_status;
+
+typedef enum { MAXSIM_F16 = 0, MAXSIM_BF16 = 1 } maxsim_dtype;
+
+/* Operation codes for maxsim_workspace_size(). */
+enum { MAXSIM_OP_FWD = 0, MAXSIM_OP_FWD_VARLEN = 1, MAXSIM_OP_BWD = 2, MAXSIM_OP_FWD_INT8 = 3 };
+
+/*
+ * Dense forward.
+ *   Q       [Nq, Lq, dim]  f16 / bf16
+ *   D       [Nd, Ld, dim]  same dtype
+ *   q_mask  [Nq, Lq] u8 or NULL      d_mask [Nd, Ld] u8 or NULL
+ *   scores  [Nq, Nd] f32 (out)
+ *   argmax  [Nq * Nd, Lq] i32 (out, optional): row i*Nd + j, column s holds
+ *           the winning document token t of query token s (0 <= t < Ld), or -1.
+ * Computed with fp32 accumulation on the tensor cores ("late-interaction-
+ * kernels" design notes, "Forward" and "Numerical accuracy"). Queries longer
+ * than 512 tokens are split into chunks whose partial scores are summed
+ * (notes, "Long-query chunking"); dim > 128 accumulates the partial dot
+ * products of successive 128-wide slices before the max.
+ */
+maxsim_status maxsim_fwd(const void *Q, const void *D, maxsim_dtype dtype,
+                         int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim,
+                         const uint8_t *q_mask, const uint8_t *d_mask,
+                         float *scores, int32_t *argmax,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Padding-free forward over packed documents ("Flash-MaxSim" Sec. 4.3.2;
+ * design notes, "Varlen / packed path").
+ *   Q             dense [Nq, max_lq, dim] when cu_seqlens_q is NULL, else
+ *                 packed [cu_seqlens_q[Nq], dim]
+ *   cu_seqlens_q  [Nq + 1] i32 or NULL (FlashAttention convention: query i
+ *                 owns rows cu[i] .. cu[i+1]-1, cu[0] = 0, non-decreasing)
+ *   D             packed [total_d, dim]; document j owns rows
+ *                 cu_seqlens_d[j] .. cu_seqlens_d[j+1]-1
+ *   cu_seqlens_d  [Nd + 1] i32, cu[0] = 0, cu[Nd] = total_d
+ *   max_lq        the longest query (upper bound on every query length)
+ *   q_mask        one byte per query row of Q's layout, or NULL
+ *   d_mask        [total_d] u8 or NULL
+ *   scores        [Nq, Nd] f32 (out); an empty document scores 0
+ *   argmax        [Nq * Nd, max_lq] i32 (out, optional); t is relative to the
+ *                 document's first row; -1 beyond the query's length.
+ * Work is proportional to the real tokens (sum of lengths), not Nd * max_ld.
+ * cu_seqlens are checked on the device (MAXSIM_ERR_DEVICE_INPUT).
+ */
+maxsim_status maxsim_fwd_varlen(const void *Q, const int32_t *cu_seqlens_q, int64_t max_lq,
+                                const void *D, const int32_t *cu_seqlens_d, int64_t total_d,
+                                maxsim_dtype dtype, int64_t Nq, int64_t Nd, int64_t dim,
+                                const uint8_t *q_mask, const uint8_t *d_mask,
+                                float *scores, int32_t *argmax,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward through the saved argmax ("Flash-MaxSim" Sec. 4.2, Eqs. (2)-(3);
+ * design notes, "Backward"), for dense Q / D:
+ *   dQ[i,s] = q_mask[i,s] * sum_j g[i,j] * D[j, argmax[i*Nd+j, s]]
+ *   dD[j,t] = sum over (i,s) with argmax[i*Nd+j, s] == t of q_mask[i,s]*g[i,j]*Q[i,s]
+ *   argmax       [Nq * Nd, Lq] i32 from maxsim_fwd (values in [-1, Ld))
+ *   grad_scores  [Nq, Nd] f32
+ *   dQ           [Nq, Lq, dim] f32 (out, optional)
+ *   dD           [Nd, Ld, dim] f32 (out, optional)
+ *   csr_row_ptr  [Nd * Ld + 1] i32 (out, optional): exclusive prefix sum of the
+ *                number of sources that selected each document token
+ *   csr_col      [Nq * Nd * Lq] i32 (out, optional): for each destination, its
+ *                sources p = (i*Nd + j)*Lq + s in ascending order (first
+ *                csr_row_ptr[Nd*Ld] entries written)
+ * dD is reduced destination by destination from the inverse-argmax CSR with
+ * no atomics (Sec. 4.2.2-4.2.3); dQ is reduced row by row in ascending j.
+ * Both are bitwise reproducible. Sources with argmax -1 contribute nothing;
+ * an argmax outside [-1, Ld) is skipped and reported as
+ * MAXSIM_ERR_DEVICE_INPUT by maxsim_device_status().
+ */
+maxsim_status maxsim_bwd(const void *Q, const void *D, maxsim_dtype dtype,
+                         int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim,
+                         const uint8_t *q_mask, const int32_t *argmax, const float *grad_scores,
+                         float *dQ, float *dD, int32_t *csr_row_ptr, int32_t *csr_col,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * INT8 x INT8 forward with per-token symmetric scales ("Flash-MaxSim"
+ * Sec. 4.3.1: dequantisation fused into the kernel):
+ *   dot[s,t] = sum_k Q8[i,s,k] * D8[j,t,k]   (exact integer)
+ *   m_s      = max_t dot[s,t] * d_scale[j,t] (valid t only)
+ *   score    = sum_s q_mask * q_scale[i,s] * m_s
+ *   Q [Nq, Lq, dim] i8, q_scale [Nq, Lq] f32 (> 0)
+ *   D [Nd, Ld, dim] i8, d_scale [Nd, Ld] f32 (> 0)
+ *   win_dot [Nq * Nd, Lq] i32 (out, optional): the exact dot at the argmax
+ *   (0 where argmax is -1).
+ * The integer products are exact (|dot| < 2^24 for dim <= 256 with values in
+ * [-127, 127]).
+ */
+maxsim_status maxsim_fwd_int8(const int8_t *Q, const float *q_scale,
+                              const int8_t *D, const float *d_scale,
+                              int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim,
+                              const uint8_t *q_mask, const uint8_t *d_mask,
+                              float *scores, int32_t *argmax, int32_t *win_dot,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of device workspace an operation needs for a shape (0 if none).
+ *   MAXSIM_OP_FWD / MAXSIM_OP_FWD_INT8: (Nq, Lq, Nd, Ld, dim)
+ *   MAXSIM_OP_FWD_VARLEN:              (Nq, max_lq, Nd, total_d, dim); assumes
+ *                                      packed Q (an upper bound for dense Q)
+ *   MAXSIM_OP_BWD:                     (Nq, Lq, Nd, Ld, dim); assumes the CSR
+ *                                      outputs are NULL (an upper bound)
+ * Returns (size_t)-1 for an invalid shape.
+ */
+size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim);
+
+/* Static English description of a status code. */
+const char *maxsim_status_string(maxsim_status status);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side status word
+ * of the current device (MAXSIM_OK if no kernel recorded a problem).
+ */
+maxsim_status maxsim_device_status(void *stream);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int maxsim_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAXSIM_H */

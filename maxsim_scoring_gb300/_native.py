@@ -1,0 +1,77 @@
+"""ctypes loader for libmaxsim.so (the C ABI in include/maxsim.h).
+
+The library is built in-tree by ``maxsim_scoring_gb300.build``. There is no
+fallback: if the shared library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmaxsim.so")
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {
+    0: "MAXSIM_OK",
+    1: "MAXSIM_ERR_INVALID_ARG",
+    2: "MAXSIM_ERR_UNSUPPORTED",
+    3: "MAXSIM_ERR_CUDA",
+    4: "MAXSIM_ERR_TIMEOUT",
+    5: "MAXSIM_ERR_WORKSPACE",
+    6: "MAXSIM_ERR_DEVICE_INPUT",
+}
+
+OP_FWD, OP_FWD_VARLEN, OP_BWD, OP_FWD_INT8 = 0, 1, 2, 3
+F16, BF16 = 0, 1
+
+# Every symbol the header declares, with its ctypes signature.
+_I64, _VP, _SZ, _I = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+SIGNATURES = {
+    "maxsim_fwd": (_I, [_VP, _VP, _I, _I64, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "maxsim_fwd_varlen": (_I, [_VP, _VP, _I64, _VP, _VP, _I64, _I, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _SZ,
+                               _VP]),
+    "maxsim_bwd": (_I, [_VP, _VP, _I, _I64, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
+                        _VP]),
+    "maxsim_fwd_int8": (_I, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
+                             _VP]),
+    "maxsim_workspace_size": (_SZ, [_I, _I64, _I64, _I64, _I64, _I64]),
+    "maxsim_status_string": (ctypes.c_char_p, [_I]),
+    "maxsim_device_status": (_I, [_VP]),
+    "maxsim_version": (_I, []),
+}
+
+
+class MaxSimError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({status_string(code)})")
+
+
+def lib():
+    """The loaded library; raises if it was not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with maxsim_scoring_gb300.build.build()")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def status_string(code: int) -> str:
+    s = lib().maxsim_status_string(code)
+    return s.decode() if s else "?"
+
+
+def check(code: int, where: str) -> None:
+    if code != 0:
+        raise MaxSimError(code, where)

@@ -1,0 +1,32 @@
+"""torch.autograd integration: the forward saves the argmax, the backward runs
+the inverse-argmax CSR kernels ("Flash-MaxSim" Sec. 4.2: built at runtime from
+the saved argmax, inside autograd)."""
+from __future__ import annotations
+
+import torch
+
+from . import ops
+
+
+class _MaxSim(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, Q, D, q_mask, d_mask):
+        scores, argmax = ops.maxsim_fwd(Q, D, q_mask, d_mask, want_argmax=True)
+        ctx.save_for_backward(Q, D, argmax, q_mask if q_mask is not None else torch.empty(0))
+        ctx.has_qmask = q_mask is not None
+        return scores
+
+    @staticmethod
+    def backward(ctx, grad_scores):
+        Q, D, argmax, q_mask = ctx.saved_tensors
+        need_q, need_d = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        dQ, dD, _, _ = ops.maxsim_bwd(Q, D, argmax, grad_scores.float().contiguous(),
+                                      q_mask if ctx.has_qmask else None, want_dq=need_q, want_dd=need_d)
+        dQ = dQ.to(Q.dtype) if dQ is not None else None
+        dD = dD.to(D.dtype) if dD is not None else None
+        return dQ, dD, None, None
+
+
+def maxsim(Q: torch.Tensor, D: torch.Tensor, q_mask=None, d_mask=None) -> torch.Tensor:
+    """Differentiable MaxSim scores [Nq, Nd] for Q [Nq,Lq,d], D [Nd,Ld,d]."""
+    return _MaxSim.apply(Q, D, q_mask, d_mask)

@@ -1,0 +1,247 @@
+// Backward of MaxSim through the saved argmax ("Flash-MaxSim" Sec. 4.2):
+//  * inverse-argmax CSR, built per document: sources p = (i*Nd + j)*Lq + s of
+//    document j only point at rows of document j, so each document's slice of
+//    the CSR is a counting sort of its own Nq*Lq sources (bincount -> prefix
+//    sum -> stable placement in ascending p, Sec. 4.2.2);
+//  * dD, destination-owned: one warp per document token walks its CSR sources
+//    and writes its row once, no atomics (Sec. 4.2.3, Eq. (3));
+//  * dQ, row-owned: one warp per query token gathers D at the winners of every
+//    document in ascending j (Eq. (2)).
+// Everything is deterministic: integer counts, fixed summation orders.
+#pragma once
+
+#include <cstdint>
+
+namespace maxsim {
+
+struct BwdArgs {
+    const uint16_t* Q;     // [Nq, Lq, dim] f16 / bf16 bits
+    const uint16_t* D;     // [Nd, Ld, dim]
+    int32_t is_bf16;
+    int32_t nq, lq, nd, ld, dim;
+    const uint8_t* q_mask; // [Nq, Lq] or NULL
+    const int32_t* argmax; // [Nq*Nd, Lq]
+    const float* g;        // [Nq, Nd]
+    float* dQ;             // [Nq, Lq, dim] or NULL
+    float* dD;             // [Nd, Ld, dim] or NULL
+    int32_t* row_ptr;      // [Nd*Ld + 1]
+    int32_t* col;          // [Nq*Nd*Lq]
+    int32_t* doc_cnt;      // [Nd]
+    int32_t* doc_base;     // [Nd + 1]
+    int* status;
+};
+
+__device__ __forceinline__ float bits_to_f32(uint16_t h, int32_t is_bf16) {
+    return is_bf16 ? __uint_as_float(static_cast<uint32_t>(h) << 16) : __half2float(__ushort_as_half(h));
+}
+
+__device__ __forceinline__ bool argmax_ok(int32_t a, int32_t ld) { return a >= -1 && a < ld; }
+
+// Sources of document j, in ascending p: (i, s) for i < Nq, s < Lq.
+__device__ __forceinline__ int64_t src_index(const BwdArgs& b, int32_t j, int32_t n) {
+    int32_t i = n / b.lq, s = n - (n / b.lq) * b.lq;
+    return (static_cast<int64_t>(i) * b.nd + j) * b.lq + s;
+}
+
+// Per-document count of sources with a valid winner.
+__global__ void __launch_bounds__(256) csr_count_kernel(const BwdArgs b) {
+    const int32_t j = blockIdx.x;
+    const int32_t nsrc = b.nq * b.lq;
+    int32_t cnt = 0;
+    bool bad = false;
+    for (int32_t n = threadIdx.x; n < nsrc; n += blockDim.x) {
+        int32_t a = b.argmax[src_index(b, j, n)];
+        if (a >= 0 && a < b.ld) ++cnt;
+        else if (!argmax_ok(a, b.ld)) bad = true;
+    }
+    if (bad && b.status) atomicCAS(b.status, 0, 6);
+    __shared__ int32_t red[8];
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cnt;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int32_t tot = 0;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += red[w];
+        b.doc_cnt[j] = tot;
+    }
+}
+
+// Exclusive prefix sum of the per-document counts (one block, fixed order).
+__global__ void __launch_bounds__(1024) csr_doc_scan_kernel(const BwdArgs b) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int32_t base = 0; base < b.nd; base += blockDim.x) {
+        int32_t j = base + threadIdx.x;
+        int32_t v = j < b.nd ? b.doc_cnt[j] : 0;
+        int32_t x = v;
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t ws = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
+            for (int o = 1; o < 32; o <<= 1) {
+                int32_t y = __shfl_up_sync(0xFFFFFFFFu, ws, o);
+                if (lane >= o) ws += y;
+            }
+            warp_sums[lane] = ws;  // inclusive
+        }
+        __syncthreads();
+        int32_t excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+        if (j < b.nd) b.doc_base[j] = excl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = excl + v;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        b.doc_base[b.nd] = carry;
+        b.row_ptr[static_cast<int64_t>(b.nd) * b.ld] = carry;
+    }
+}
+
+// Counting sort of one document's sources into its CSR rows. Each of the
+// block's `nw` warps owns a contiguous run of the sources; per-warp histograms
+// give every warp its starting offset inside each row, and inside a warp the
+// lanes holding the same destination are ranked by lane order, so sources land
+// in ascending p (a stable sort, as Sec. 4.2.2 requires).
+__global__ void __launch_bounds__(256) csr_build_kernel(const BwdArgs b, int32_t nw) {
+    extern __shared__ int32_t hist[];  // [nw][ld]
+    const int32_t j = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t nsrc = b.nq * b.lq;
+    const int32_t per = (nsrc + nw - 1) / nw;
+    for (int32_t x = threadIdx.x; x < nw * b.ld; x += blockDim.x) hist[x] = 0;
+    __syncthreads();
+    if (warp < nw) {
+        const int32_t n0 = warp * per, n1 = min(n0 + per, nsrc);
+        for (int32_t n = n0 + lane; n < n1; n += 32) {
+            int32_t a = b.argmax[src_index(b, j, n)];
+            if (a >= 0 && a < b.ld) atomicAdd(&hist[warp * b.ld + a], 1);
+        }
+    }
+    __syncthreads();
+    // exclusive scan over destinations t of the per-row totals; each thread
+    // owns a contiguous range of t
+    __shared__ int32_t part[256];
+    const int32_t tper = (b.ld + blockDim.x - 1) / blockDim.x;
+    const int32_t t0 = threadIdx.x * tper, t1 = min(t0 + tper, b.ld);
+    int32_t local = 0;
+    for (int32_t t = t0; t < t1; ++t)
+        for (int32_t w = 0; w < nw; ++w) local += hist[w * b.ld + t];
+    part[threadIdx.x] = local;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int32_t run = 0;
+        for (int x = 0; x < static_cast<int>(blockDim.x); ++x) {
+            int32_t v = part[x];
+            part[x] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    int32_t run = b.doc_base[j] + part[threadIdx.x];
+    for (int32_t t = t0; t < t1; ++t) {
+        b.row_ptr[static_cast<int64_t>(j) * b.ld + t] = run;
+        for (int32_t w = 0; w < nw; ++w) {
+            int32_t c = hist[w * b.ld + t];
+            hist[w * b.ld + t] = run;  // becomes warp w's next free slot in row t
+            run += c;
+        }
+    }
+    __syncthreads();
+    if (warp < nw) {
+        const int32_t n0 = warp * per, n1 = min(n0 + per, nsrc);
+        for (int32_t nb = n0; nb < n1; nb += 32) {
+            const int32_t n = nb + lane;
+            int32_t a = -1;
+            int64_t p = 0;
+            if (n < n1) {
+                p = src_index(b, j, n);
+                a = b.argmax[p];
+                if (!(a >= 0 && a < b.ld)) a = -1;
+            }
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, a);
+            if (a >= 0) {
+                const uint32_t lower = peers & ((1u << lane) - 1u);
+                const int32_t rank = __popc(lower);
+                const int32_t slot = hist[warp * b.ld + a] + rank;
+                b.col[slot] = static_cast<int32_t>(p);
+                __syncwarp(peers);
+                if ((peers >> lane) == 1u) hist[warp * b.ld + a] += __popc(peers);  // highest peer lane
+            }
+            __syncwarp();
+        }
+    }
+}
+
+// dD: one warp per destination row (j, t); lanes split the embedding.
+template <int kVec>  // floats per lane (dim / 32)
+__global__ void __launch_bounds__(256) dd_kernel(const BwdArgs b) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t nrows = static_cast<int64_t>(b.nd) * b.ld;
+    if (r >= nrows) return;
+    const int32_t j = static_cast<int32_t>(r / b.ld);
+    float acc[kVec];
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
+    const int32_t e0 = b.row_ptr[r], e1 = b.row_ptr[r + 1];
+    for (int32_t e = e0; e < e1; ++e) {
+        const int32_t p = b.col[e];
+        const int32_t s = p % b.lq;
+        const int32_t i = (p / b.lq) / b.nd;
+        float w = b.g[static_cast<int64_t>(i) * b.nd + j];
+        if (b.q_mask && !b.q_mask[static_cast<int64_t>(i) * b.lq + s]) w = 0.f;
+        const uint16_t* qrow = b.Q + (static_cast<int64_t>(i) * b.lq + s) * b.dim;
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+            const int k = lane * kVec + v;
+            if (k < b.dim) acc[v] = fmaf(w, bits_to_f32(qrow[k], b.is_bf16), acc[v]);
+        }
+    }
+    float* out = b.dD + r * b.dim;
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+        const int k = lane * kVec + v;
+        if (k < b.dim) out[k] = acc[v];
+    }
+}
+
+// dQ: one warp per query row (i, s), ascending j.
+template <int kVec>
+__global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t nrows = static_cast<int64_t>(b.nq) * b.lq;
+    if (r >= nrows) return;
+    const int32_t i = static_cast<int32_t>(r / b.lq);
+    const int32_t s = static_cast<int32_t>(r - static_cast<int64_t>(i) * b.lq);
+    float acc[kVec];
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
+    for (int32_t j = 0; j < b.nd; ++j) {
+        const int32_t a = b.argmax[(static_cast<int64_t>(i) * b.nd + j) * b.lq + s];
+        if (a < 0 || a >= b.ld) continue;
+        const float w = b.g[static_cast<int64_t>(i) * b.nd + j];
+        const uint16_t* drow = b.D + (static_cast<int64_t>(j) * b.ld + a) * b.dim;
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+            const int k = lane * kVec + v;
+            if (k < b.dim) acc[v] = fmaf(w, bits_to_f32(drow[k], b.is_bf16), acc[v]);
+        }
+    }
+    const bool active = b.q_mask == nullptr || b.q_mask[r] != 0;
+    float* out = b.dQ + r * b.dim;
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+        const int k = lane * kVec + v;
+        if (k < b.dim) out[k] = active ? acc[v] : 0.f;
+    }
+}
+
+}  // namespace maxsim

@@ -1,0 +1,182 @@
+"""PyTorch-facing binding of the MaxSim C ABI: argument marshalling only.
+
+Every function here checks shapes / dtypes, allocates outputs and workspace
+with torch on the tensors' device, and calls the entry point of the same name
+in libmaxsim.so on the current CUDA stream. All arithmetic happens in the
+CUDA kernels behind that call.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _native
+
+_DT = {torch.float16: _native.F16, torch.bfloat16: _native.BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _contig(t: Optional[torch.Tensor], name: str, dtype=None, device=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t.contiguous()
+
+
+def _mask(m: Optional[torch.Tensor], name: str, device):
+    if m is None:
+        return None
+    if m.dtype == torch.bool:
+        m = m.to(torch.uint8)
+    return _contig(m, name, torch.uint8, device)
+
+
+def workspace_size(op: int, Nq: int, Lq: int, Nd: int, Ld: int, dim: int) -> int:
+    n = _native.lib().maxsim_workspace_size(op, Nq, Lq, Nd, Ld, dim)
+    if n == ctypes_size_max():
+        raise ValueError("invalid shape for maxsim_workspace_size")
+    return int(n)
+
+
+def ctypes_size_max() -> int:
+    import ctypes
+    return ctypes.c_size_t(-1).value
+
+
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
+    if nbytes == 0:
+        return None, 0
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError(f"workspace needs {nbytes} bytes")
+        return ws, ws.numel() * ws.element_size()
+    t = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return t, nbytes
+
+
+def maxsim_fwd(Q: torch.Tensor, D: torch.Tensor, q_mask=None, d_mask=None, *, want_argmax: bool = False,
+               scores: Optional[torch.Tensor] = None, argmax: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None):
+    """scores [Nq, Nd] (and argmax [Nq*Nd, Lq] int32) for Q [Nq,Lq,d], D [Nd,Ld,d]."""
+    if Q.dtype not in _DT or D.dtype != Q.dtype:
+        raise TypeError("Q and D must both be float16 or both bfloat16")
+    dev = Q.device
+    Q, D = _contig(Q, "Q"), _contig(D, "D", device=dev)
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, dim2 = D.shape
+    if dim2 != dim:
+        raise ValueError("Q and D embedding dimensions differ")
+    qm, dm = _mask(q_mask, "q_mask", dev), _mask(d_mask, "d_mask", dev)
+    if scores is None:
+        scores = torch.empty((Nq, Nd), dtype=torch.float32, device=dev)
+    if want_argmax and argmax is None:
+        argmax = torch.empty((Nq * Nd, Lq), dtype=torch.int32, device=dev)
+    ws, nbytes = _workspace(workspace_size(_native.OP_FWD, Nq, Lq, Nd, Ld, dim), dev, workspace)
+    rc = _native.lib().maxsim_fwd(_ptr(Q), _ptr(D), _DT[Q.dtype], Nq, Lq, Nd, Ld, dim, _ptr(qm), _ptr(dm),
+                                  _ptr(scores), _ptr(argmax), _ptr(ws), nbytes, _stream(dev))
+    _native.check(rc, "maxsim_fwd")
+    return scores, argmax
+
+
+def maxsim_fwd_varlen(Q: torch.Tensor, cu_seqlens_q: Optional[torch.Tensor], max_lq: int, D: torch.Tensor,
+                      cu_seqlens_d: torch.Tensor, q_mask=None, d_mask=None, *, want_argmax: bool = False,
+                      scores: Optional[torch.Tensor] = None, argmax: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None):
+    """Packed documents D [total_d, d] with cu_seqlens_d [Nd+1] (int32).
+
+    Q is dense [Nq, max_lq, d] when cu_seqlens_q is None, else packed
+    [total_q, d]. Returns scores [Nq, Nd] (and argmax [Nq*Nd, max_lq]).
+    """
+    if Q.dtype not in _DT or D.dtype != Q.dtype:
+        raise TypeError("Q and D must both be float16 or both bfloat16")
+    dev = Q.device
+    Q, D = _contig(Q, "Q"), _contig(D, "D", device=dev)
+    cu_d = _contig(cu_seqlens_d, "cu_seqlens_d", torch.int32, dev)
+    cu_q = _contig(cu_seqlens_q, "cu_seqlens_q", torch.int32, dev)
+    dim = Q.shape[-1]
+    if D.dim() != 2 or D.shape[1] != dim:
+        raise ValueError("D must be packed [total_d, dim]")
+    Nd = cu_d.numel() - 1
+    Nq = (cu_q.numel() - 1) if cu_q is not None else Q.shape[0]
+    if cu_q is None and (Q.dim() != 3 or Q.shape[1] != max_lq):
+        raise ValueError("dense Q must be [Nq, max_lq, dim]")
+    total_d = D.shape[0]
+    qm, dm = _mask(q_mask, "q_mask", dev), _mask(d_mask, "d_mask", dev)
+    if scores is None:
+        scores = torch.empty((Nq, Nd), dtype=torch.float32, device=dev)
+    if want_argmax and argmax is None:
+        argmax = torch.empty((Nq * Nd, max_lq), dtype=torch.int32, device=dev)
+    ws, nbytes = _workspace(workspace_size(_native.OP_FWD_VARLEN, Nq, max_lq, Nd, total_d, dim), dev, workspace)
+    rc = _native.lib().maxsim_fwd_varlen(_ptr(Q), _ptr(cu_q), max_lq, _ptr(D), _ptr(cu_d), total_d, _DT[Q.dtype], Nq,
+                                         Nd, dim, _ptr(qm), _ptr(dm), _ptr(scores), _ptr(argmax), _ptr(ws), nbytes,
+                                         _stream(dev))
+    _native.check(rc, "maxsim_fwd_varlen")
+    return scores, argmax
+
+
+def maxsim_bwd(Q: torch.Tensor, D: torch.Tensor, argmax: torch.Tensor, grad_scores: torch.Tensor, q_mask=None, *,
+               want_dq: bool = True, want_dd: bool = True, want_csr: bool = False,
+               workspace: Optional[torch.Tensor] = None):
+    """dQ [Nq,Lq,d] f32, dD [Nd,Ld,d] f32 (and the CSR row_ptr / col)."""
+    if Q.dtype not in _DT or D.dtype != Q.dtype:
+        raise TypeError("Q and D must both be float16 or both bfloat16")
+    dev = Q.device
+    Q, D = _contig(Q, "Q"), _contig(D, "D", device=dev)
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, _ = D.shape
+    am = _contig(argmax, "argmax", torch.int32, dev)
+    g = _contig(grad_scores, "grad_scores", torch.float32, dev)
+    if am.numel() != Nq * Nd * Lq or g.numel() != Nq * Nd:
+        raise ValueError("argmax must be [Nq*Nd, Lq] and grad_scores [Nq, Nd]")
+    qm = _mask(q_mask, "q_mask", dev)
+    dQ = torch.empty((Nq, Lq, dim), dtype=torch.float32, device=dev) if want_dq else None
+    dD = torch.empty((Nd, Ld, dim), dtype=torch.float32, device=dev) if want_dd else None
+    row_ptr = torch.empty(Nd * Ld + 1, dtype=torch.int32, device=dev) if want_csr else None
+    col = torch.empty(max(1, Nq * Nd * Lq), dtype=torch.int32, device=dev) if want_csr else None
+    ws, nbytes = _workspace(workspace_size(_native.OP_BWD, Nq, Lq, Nd, Ld, dim), dev, workspace)
+    rc = _native.lib().maxsim_bwd(_ptr(Q), _ptr(D), _DT[Q.dtype], Nq, Lq, Nd, Ld, dim, _ptr(qm), _ptr(am), _ptr(g),
+                                  _ptr(dQ), _ptr(dD), _ptr(row_ptr), _ptr(col), _ptr(ws), nbytes, _stream(dev))
+    _native.check(rc, "maxsim_bwd")
+    return dQ, dD, row_ptr, col
+
+
+def maxsim_fwd_int8(Q: torch.Tensor, q_scale: torch.Tensor, D: torch.Tensor, d_scale: torch.Tensor, q_mask=None,
+                    d_mask=None, *, want_argmax: bool = False, want_win_dot: bool = False,
+                    scores: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """INT8 x INT8 scores [Nq, Nd] with per-token float32 scales."""
+    dev = Q.device
+    Q = _contig(Q, "Q", torch.int8)
+    D = _contig(D, "D", torch.int8, dev)
+    qs = _contig(q_scale, "q_scale", torch.float32, dev)
+    ds = _contig(d_scale, "d_scale", torch.float32, dev)
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, _ = D.shape
+    qm, dm = _mask(q_mask, "q_mask", dev), _mask(d_mask, "d_mask", dev)
+    if scores is None:
+        scores = torch.empty((Nq, Nd), dtype=torch.float32, device=dev)
+    argmax = torch.empty((Nq * Nd, Lq), dtype=torch.int32, device=dev) if (want_argmax or want_win_dot) else None
+    win = torch.empty((Nq * Nd, Lq), dtype=torch.int32, device=dev) if want_win_dot else None
+    ws, nbytes = _workspace(workspace_size(_native.OP_FWD_INT8, Nq, Lq, Nd, Ld, dim), dev, workspace)
+    rc = _native.lib().maxsim_fwd_int8(_ptr(Q), _ptr(qs), _ptr(D), _ptr(ds), Nq, Lq, Nd, Ld, dim, _ptr(qm), _ptr(dm),
+                                       _ptr(scores), _ptr(argmax), _ptr(win), _ptr(ws), nbytes, _stream(dev))
+    _native.check(rc, "maxsim_fwd_int8")
+    return scores, argmax, win
+
+
+def device_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device status word."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    return int(_native.lib().maxsim_device_status(_stream(dev)))

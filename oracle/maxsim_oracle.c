@@ -125,23 +125,30 @@ int oracle_fwd(const void *Q, const void *D, int dtype, int64_t Nq, const int64_
     if (Nq < 0 || Nd < 0 || dim <= 0 || n_sel < 0) return 1;
     set_threads(nthreads);
     int64_t npairs = Nq * n_sel;
-#pragma omp parallel for schedule(dynamic, 1)
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
     for (int64_t pair = 0; pair < npairs; ++pair) {
         int64_t i = pair / n_sel;
         int64_t c = pair % n_sel;
         int64_t j = docs ? docs[c] : c;
-        double score = 0.0;
         int64_t lq = q_off[i + 1] - q_off[i];
+        int64_t ld = d_off[j + 1] - d_off[j];
+        /* decode this pair's rows once into doubles */
+        double *qv = (double *)malloc((size_t)(lq > 0 ? lq : 1) * (size_t)dim * sizeof(double));
+        double *dv = (double *)malloc((size_t)(ld > 0 ? ld : 1) * (size_t)dim * sizeof(double));
+        if (!qv || !dv) { free(qv); free(dv); failed = 1; continue; }
+        for (int64_t s = 0; s < lq; ++s)
+            for (int64_t k = 0; k < dim; ++k) qv[s * dim + k] = load_elem(Q, dtype, (q_off[i] + s) * dim + k);
+        for (int64_t t = 0; t < ld; ++t)
+            for (int64_t k = 0; k < dim; ++k) dv[t * dim + k] = load_elem(D, dtype, (d_off[j] + t) * dim + k);
+        double score = 0.0;
         for (int64_t s = 0; s < lq; ++s) {
-            int64_t qrow = q_off[i] + s;
             double best = -INFINITY, second = -INFINITY;
             int32_t best_t = -1;
-            for (int64_t t = 0; t < d_off[j + 1] - d_off[j]; ++t) {
-                int64_t drow = d_off[j] + t;
-                if (d_mask && !d_mask[drow]) continue;
+            for (int64_t t = 0; t < ld; ++t) {
+                if (d_mask && !d_mask[d_off[j] + t]) continue;
                 double v = 0.0;
-                for (int64_t k = 0; k < dim; ++k)
-                    v += load_elem(Q, dtype, qrow * dim + k) * load_elem(D, dtype, drow * dim + k);
+                for (int64_t k = 0; k < dim; ++k) v += qv[s * dim + k] * dv[t * dim + k];
                 if (best_t < 0 || v > best) {
                     second = best;
                     best = v;
@@ -150,7 +157,7 @@ int oracle_fwd(const void *Q, const void *D, int dtype, int64_t Nq, const int64_
                     second = v;
                 }
             }
-            int active = q_mask ? (q_mask[qrow] != 0) : 1;
+            int active = q_mask ? (q_mask[q_off[i] + s] != 0) : 1;
             if (active && best_t >= 0) score += best;
             if (argmax) argmax[pair * lq_stride + s] = best_t;
             if (gap) gap[pair * lq_stride + s] = (best_t >= 0 && second > -INFINITY) ? best - second : INFINITY;
@@ -160,8 +167,10 @@ int oracle_fwd(const void *Q, const void *D, int dtype, int64_t Nq, const int64_
             if (gap) gap[pair * lq_stride + s] = INFINITY;
         }
         scores[pair] = score;
+        free(qv);
+        free(dv);
     }
-    return 0;
+    return failed ? 4 : 0;
 }
 
 /*

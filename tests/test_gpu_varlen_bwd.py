@@ -1,0 +1,154 @@
+"""Parity of the packed forward (maxsim_fwd_varlen) and of the backward
+(maxsim_bwd) with the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+from maxsim_scoring_gb300 import ops
+from tests.gpu_util import assert_argmax, assert_grad, assert_scores, dev, dev_bits, integer_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def packed_docs(seed, lens, dim, dtype):
+    cu = np.zeros(len(lens) + 1, np.int64)
+    np.cumsum(lens, out=cu[1:])
+    D = datagen.gaussian_rows(seed, 2, int(cu[-1]), dim, dtype)
+    return D, cu
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_varlen_ragged_with_empty_docs(dtype):
+    lens = np.array([0, 33, 1, 300, 0, 0, 128, 129, 5, 0, 260, 31, 32, 0])
+    Nq, Lq, dim = 3, 32, 128
+    D, cu = packed_docs(11, lens, dim, dtype)
+    Q = datagen.gaussian_rows(11, 1, Nq * Lq, dim, dtype).reshape(Nq, Lq, dim)
+    dm = (np.random.default_rng(2).random(int(cu[-1])) > 0.1).astype(np.uint8)
+    for d_mask in (None, dm):
+        s, a = ops.maxsim_fwd_varlen(dev_bits(Q, dtype), None, Lq, dev_bits(D, dtype), dev(cu.astype(np.int32)),
+                                     d_mask=dev(d_mask), want_argmax=True)
+        assert ops.device_status() == 0
+        q_off = np.arange(Nq + 1) * Lq
+        ref_s, ref_a, gap = oracle.fwd_packed(Q.reshape(-1, dim), q_off, D, cu, dtype, d_mask=d_mask)
+        assert_scores(s, ref_s, Lq)
+        assert_argmax(a, ref_a, gap)
+        assert (s.cpu().numpy()[:, lens == 0] == 0).all()
+
+
+def test_varlen_packed_queries():
+    dtype, dim = "f16", 64
+    qlens = np.array([5, 32, 1, 70, 17])
+    dlens = np.array([40, 200, 0, 129, 7, 64])
+    rng = np.random.default_rng(9)
+    cu_q = np.concatenate([[0], np.cumsum(qlens)])
+    cu_d = np.concatenate([[0], np.cumsum(dlens)])
+    Q = datagen.float_to_bits(integer_rows(rng, int(cu_q[-1]), dim), dtype)
+    D = datagen.float_to_bits(integer_rows(rng, int(cu_d[-1]), dim), dtype)
+    qm = (rng.random(int(cu_q[-1])) > 0.2).astype(np.uint8)
+    max_lq = int(qlens.max())
+    s, a = ops.maxsim_fwd_varlen(dev_bits(Q, dtype), dev(cu_q.astype(np.int32)), max_lq, dev_bits(D, dtype),
+                                 dev(cu_d.astype(np.int32)), q_mask=dev(qm), want_argmax=True)
+    assert ops.device_status() == 0
+    ref_s, ref_a, _ = oracle.fwd_packed(Q, cu_q, D, cu_d, dtype, q_mask=qm, lq_stride=max_lq)
+    assert np.array_equal(s.cpu().numpy().astype(np.float64), ref_s)   # integer inputs: exact
+    assert np.array_equal(a.cpu().numpy(), ref_a)
+
+
+def test_varlen_equals_dense_with_trailing_mask():
+    # "same as the padded path": a trailing d_mask equals shorter packed documents
+    dtype, Nq, Lq, Nd, Ld, dim = "bf16", 2, 32, 5, 200, 128
+    Q = datagen.gaussian_rows(6, 1, Nq * Lq, dim, dtype).reshape(Nq, Lq, dim)
+    D = datagen.gaussian_rows(6, 2, Nd * Ld, dim, dtype).reshape(Nd, Ld, dim)
+    lens = np.array([200, 150, 0, 1, 77])
+    dm = (np.arange(Ld)[None, :] < lens[:, None]).astype(np.uint8)
+    s_dense, a_dense = ops.maxsim_fwd(dev_bits(Q, dtype), dev_bits(D, dtype), None, dev(dm), want_argmax=True)
+    packed = np.concatenate([D[j, :lens[j]] for j in range(Nd)])
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    s_var, a_var = ops.maxsim_fwd_varlen(dev_bits(Q, dtype), None, Lq, dev_bits(packed, dtype), dev(cu),
+                                         want_argmax=True)
+    assert ops.device_status() == 0
+    assert torch.equal(a_dense, a_var)
+    assert torch.allclose(s_dense, s_var, rtol=0, atol=1e-5)
+
+
+def test_bad_cu_seqlens_reported_on_device():
+    dim = 16
+    D = dev_bits(datagen.gaussian_rows(1, 2, 50, dim, "f16"), "f16")
+    Q = dev_bits(datagen.gaussian_rows(1, 1, 4, dim, "f16").reshape(1, 4, dim), "f16")
+    cu = dev(np.array([0, 30, 20, 50], np.int32))  # decreasing: invalid
+    ops.maxsim_fwd_varlen(Q, None, 4, D, cu)
+    assert ops.device_status() == 6
+    assert ops.device_status() == 0  # reading clears it
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_backward_parity(dtype):
+    Nq, Lq, Nd, Ld, dim = 5, 24, 6, 300, 128
+    seed = 31
+    Q = datagen.gaussian_rows(seed, 1, Nq * Lq, dim, dtype).reshape(Nq, Lq, dim)
+    D = datagen.gaussian_rows(seed, 2, Nd * Ld, dim, dtype).reshape(Nd, Ld, dim)
+    qm = datagen.mask_drop_tail(seed, 4, Nq, Lq, 8)
+    dm = np.ones((Nd, Ld), np.uint8)
+    dm[2] = 0  # sentinel sources
+    g = datagen.normal_f32(seed, 6, Nq * Nd).reshape(Nq, Nd)
+    Qd, Dd = dev_bits(Q, dtype), dev_bits(D, dtype)
+    _, a = ops.maxsim_fwd(Qd, Dd, dev(qm), dev(dm), want_argmax=True)
+    dQ, dD, rp, col = ops.maxsim_bwd(Qd, Dd, a, dev(g), dev(qm), want_csr=True)
+    assert ops.device_status() == 0
+    am = a.cpu().numpy()
+    ref_dQ, ref_dD, ref_rp, ref_col = oracle.bwd(Q, D, dtype, am, g, q_mask=qm)
+    assert np.array_equal(rp.cpu().numpy(), ref_rp)
+    assert np.array_equal(col.cpu().numpy()[: ref_rp[-1]], ref_col)
+    assert_grad(dQ, ref_dQ)
+    assert_grad(dD, ref_dD)
+    # bitwise reproducible (no atomics)
+    dQ2, dD2, rp2, col2 = ops.maxsim_bwd(Qd, Dd, a, dev(g), dev(qm), want_csr=True)
+    assert torch.equal(dQ, dQ2) and torch.equal(dD, dD2) and torch.equal(col, col2)
+
+
+def test_backward_hot_token_contention():
+    # every query token of every query picks the same document token
+    Nq, Lq, Nd, Ld, dim = 16, 32, 2, 64, 32
+    rng = np.random.default_rng(4)
+    Q = datagen.float_to_bits(np.abs(integer_rows(rng, Nq * Lq, dim)), "bf16").reshape(Nq, Lq, dim)
+    Dv = np.zeros((Nd * Ld, dim))
+    Dv[::Ld] = 1.0  # token 0 of each document dominates
+    D = datagen.float_to_bits(Dv, "bf16").reshape(Nd, Ld, dim)
+    g = datagen.normal_f32(2, 6, Nq * Nd).reshape(Nq, Nd)
+    Qd, Dd = dev_bits(Q, "bf16"), dev_bits(D, "bf16")
+    _, a = ops.maxsim_fwd(Qd, Dd, want_argmax=True)
+    dQ, dD, rp, col = ops.maxsim_bwd(Qd, Dd, a, dev(g), want_csr=True)
+    am = a.cpu().numpy()
+    ref_dQ, ref_dD, ref_rp, ref_col = oracle.bwd(Q, D, "bf16", am, g)
+    assert np.array_equal(rp.cpu().numpy(), ref_rp) and np.array_equal(col.cpu().numpy()[: ref_rp[-1]], ref_col)
+    assert_grad(dQ, ref_dQ)
+    assert_grad(dD, ref_dD)
+
+
+def test_backward_out_of_range_argmax_reported():
+    Nq, Lq, Nd, Ld, dim = 1, 4, 2, 8, 16
+    Q = dev_bits(datagen.gaussian_rows(1, 1, Nq * Lq, dim, "f16").reshape(Nq, Lq, dim), "f16")
+    D = dev_bits(datagen.gaussian_rows(1, 2, Nd * Ld, dim, "f16").reshape(Nd, Ld, dim), "f16")
+    a = dev(np.array([[0, 1, 9, -1], [2, 3, 4, -7]], np.int32))
+    g = dev(np.ones((Nq, Nd), np.float32))
+    ops.maxsim_bwd(Q, D, a, g, want_csr=True)
+    assert ops.device_status() == 6
+
+
+def test_autograd_wrapper():
+    from maxsim_scoring_gb300 import maxsim
+    Nq, Lq, Nd, Ld, dim = 3, 16, 4, 90, 64
+    Q = dev_bits(datagen.gaussian_rows(2, 1, Nq * Lq, dim, "bf16").reshape(Nq, Lq, dim), "bf16").requires_grad_()
+    D = dev_bits(datagen.gaussian_rows(2, 2, Nd * Ld, dim, "bf16").reshape(Nd, Ld, dim), "bf16").requires_grad_()
+    s = maxsim(Q, D)
+    s.sum().backward()
+    # reference through materialised similarities (float32)
+    Qr = Q.detach().float().requires_grad_()
+    Dr = D.detach().float().requires_grad_()
+    S = torch.einsum("isk,jtk->ijst", Qr, Dr)
+    S.max(dim=3).values.sum(dim=2).sum().backward()
+    assert torch.allclose(s.detach(), S.max(dim=3).values.sum(dim=2).detach(), atol=1e-3 * Lq)
+    assert torch.allclose(Q.grad.float(), Qr.grad, atol=2e-2)
+    assert torch.allclose(D.grad.float(), Dr.grad, atol=2e-2)
