@@ -170,6 +170,35 @@ const char *maxsim_status_string(maxsim_status status);
  */
 maxsim_status maxsim_device_status(void *stream);
 
+/*
+ * Allocation-free variant of maxsim_fwd_varlen (the pages have no counterpart:
+ * this is a deployment convenience of this library).
+ *
+ * Some callers cannot allocate device memory: a plugin inside a serving stack
+ * that is handed only its input and output buffers, a C host with no device
+ * allocator of its own or with a fixed memory budget that forbids a
+ * cudaMalloc in the serving loop. They cannot provide the workspace that
+ * maxsim_fwd_varlen needs for its repacked query rows. This entry point takes
+ * the same arguments minus the workspace, and uses instead a scratch array of
+ * MAXSIM_NOALLOC_SCRATCH_BYTES compiled into the library's device image. It
+ * calls no cudaMalloc, cudaFree or allocating library routine.
+ *  - The scratch exists on every GPU that loads the library, until exit.
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array, so calls that overlap on the
+ *    GPU (other streams, other host threads) race on it: serialise them.
+ *  - Shapes whose workspace (maxsim_workspace_size(MAXSIM_OP_FWD_VARLEN, ...))
+ *    exceeds MAXSIM_NOALLOC_SCRATCH_BYTES return MAXSIM_ERR_UNSUPPORTED
+ *    without launching; at dim = 128 that is about 64K padded query rows.
+ * Results are identical to maxsim_fwd_varlen's for the same inputs.
+ */
+#define MAXSIM_NOALLOC_SCRATCH_BYTES (16u << 20)
+maxsim_status maxsim_fwd_varlen_noalloc(const void *Q, const int32_t *cu_seqlens_q, int64_t max_lq,
+                                        const void *D, const int32_t *cu_seqlens_d, int64_t total_d,
+                                        maxsim_dtype dtype, int64_t Nq, int64_t Nd, int64_t dim,
+                                        const uint8_t *q_mask, const uint8_t *d_mask,
+                                        float *scores, int32_t *argmax, void *stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int maxsim_version(void);
 

@@ -38,6 +38,8 @@ SIGNATURES = {
                         _VP]),
     "maxsim_fwd_int8": (_I, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
                              _VP]),
+    "maxsim_fwd_varlen_noalloc": (_I, [_VP, _VP, _I64, _VP, _VP, _I64, _I, _I64, _I64, _I64, _VP, _VP, _VP, _VP,
+                                       _VP]),
     "maxsim_workspace_size": (_SZ, [_I, _I64, _I64, _I64, _I64, _I64]),
     "maxsim_status_string": (ctypes.c_char_p, [_I]),
     "maxsim_device_status": (_I, [_VP]),

@@ -560,3 +560,54 @@ maxsim_status maxsim_fwd_int8(const int8_t* Q, const float* q_scale, const int8_
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free varlen forward
+//
+// Scratch for callers that cannot allocate device memory: a fixed array in
+// this module's device image. Every GPU that loads the library holds it until
+// the process exits; all calls on a device share it, so calls that overlap on
+// the GPU race on it.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MAXSIM_NOALLOC_SCRATCH_BYTES];
+
+namespace maxsim {
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array for the current device, looked up once
+// per device (with that device current). The host-side symbol is only a
+// stand-in and must never be handed to a kernel.
+maxsim_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MAXSIM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MAXSIM_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MAXSIM_OK;
+}
+
+}  // namespace
+}  // namespace maxsim
+
+extern "C" maxsim_status maxsim_fwd_varlen_noalloc(const void* Q, const int32_t* cu_seqlens_q, int64_t max_lq,
+                                                   const void* D, const int32_t* cu_seqlens_d, int64_t total_d,
+                                                   maxsim_dtype dtype, int64_t Nq, int64_t Nd, int64_t dim,
+                                                   const uint8_t* q_mask, const uint8_t* d_mask, float* scores,
+                                                   int32_t* argmax, void* stream) {
+    const size_t need = maxsim_workspace_size(MAXSIM_OP_FWD_VARLEN, Nq, max_lq, Nd, total_d, dim);
+    if (need == static_cast<size_t>(-1)) return MAXSIM_ERR_INVALID_ARG;
+    if (need > static_cast<size_t>(MAXSIM_NOALLOC_SCRATCH_BYTES)) return MAXSIM_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if (need > 0) {
+        const maxsim_status rc = noalloc_scratch(&scratch);
+        if (rc != MAXSIM_OK) return rc;
+    }
+    return maxsim_fwd_varlen(Q, cu_seqlens_q, max_lq, D, cu_seqlens_d, total_d, dtype, Nq, Nd, dim, q_mask, d_mask,
+                             scores, argmax, scratch, need > 0 ? static_cast<size_t>(MAXSIM_NOALLOC_SCRATCH_BYTES) : 0,
+                             stream);
+}
