@@ -138,8 +138,12 @@ maxsim_status maxsim_bwd(const void *Q, const void *D, maxsim_dtype dtype,
  *   score    = sum_s q_mask * q_scale[i,s] * m_s
  *   Q [Nq, Lq, dim] i8, q_scale [Nq, Lq] f32 (> 0)
  *   D [Nd, Ld, dim] i8, d_scale [Nd, Ld] f32 (> 0)
- *   win_dot [Nq * Nd, Lq] i32 (out, optional): the exact dot at the argmax
- *   (0 where argmax is -1).
+ *   argmax  [Nq * Nd, Lq] i32 (out, optional)
+ *   win_dot [Nq * Nd, Lq] i32 (out, optional; needs argmax): the exact dot at
+ *   the argmax (0 where argmax is -1).
+ * The tensor cores of sm_103a have no 8-bit integer MMA kind: the INT8 tiles
+ * are converted to binary16 in shared memory (exact for |v| <= 127) and
+ * accumulated in fp32, which is exact for |dot| < 2^24.
  * The integer products are exact (|dot| < 2^24 for dim <= 256 with values in
  * [-127, 127]).
  */

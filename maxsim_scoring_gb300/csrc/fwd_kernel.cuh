@@ -1,5 +1,5 @@
 // Fused MaxSim forward for sm_103a: TMA -> tcgen05.mma -> TMEM -> fused
-// mask / running max / argmax / sum epilogue. The [rows, doc tokens]
+// running max / argmax / sum epilogue. The [query rows, document tokens]
 // similarity tile exists only in tensor memory and registers.
 //
 // Work decomposition (one persistent CTA per SM):
@@ -7,25 +7,35 @@
 //    to 4 M-tiles of 128 rows that stay resident in shared memory. A query
 //    longer than a row block is split into chunks whose partial scores are
 //    summed afterwards ("late-interaction-kernels" design notes, "Long-query
-//    chunking"; the sum of maxima decomposes over query tokens).
+//    chunking": the sum of maxima decomposes over query tokens).
 //  * Documents are packed token rows (dense D is the special case
 //    cu[j] = j * Ld). A "doc range" is a run of whole documents holding about
-//    total_d / n_dr tokens. A work unit is (row block, doc range).
-//  * Tiles of BN = 128 consecutive document tokens stream through a shared
-//    memory ring by TMA. A tile may span several documents: the epilogue folds
-//    each document's columns separately, so no MMA work is spent on padding
-//    ("Flash-MaxSim" Sec. 4.3.2: work proportional to the real tokens).
+//    total_d / n_dr tokens; a work unit is (row block, doc range).
+//  * Each document is cut into tiles of up to 128 of its own tokens; the MMA N
+//    of a tile is its token count rounded up to 16, so work follows the real
+//    tokens ("Flash-MaxSim" Sec. 4.3.2) and a tile never spans two documents.
+//  * Masking without per-element work in the epilogue: the prep warps
+//    overwrite, in shared memory, the operand rows of masked tokens and of the
+//    padding up to N with NaN. Every similarity in those columns is then NaN,
+//    and max.f32 returns its non-NaN operand, so those columns can never win:
+//    the same effect as setting them to -inf before the max ("Flash-MaxSim"
+//    Sec. 4.1.1; design notes, "Mask handling"). A row whose every column is
+//    masked keeps m = -inf.
 //  * For every (tile, M-tile) one MMA chain S = Q_blk * D_tile^T (K = dim)
 //    accumulates in one of four 128-column TMEM buffers; the epilogue warps
 //    read it with tcgen05.ld while the tensor core fills the next buffer.
+//  * INT8 mode ("Flash-MaxSim" Sec. 4.3.1): the tensor-core kind for 8-bit
+//    integers is not available on sm_103a, so the prep warps convert the INT8
+//    document tile to f16 in shared memory (exact: |v| <= 127), the MMA
+//    accumulates in fp32 (exact: |dot| < 2^24 for dim <= 256), and the
+//    epilogue applies the per-token scales: v = dot * d_scale[t] before the
+//    max, q_scale[s] on the row maximum.
 //
-// Epilogue semantics ("late-interaction-kernels" notes, "Forward" and "Mask
-// handling"; "Flash-MaxSim" Sec. 4.1.1):
-//  * masked / out-of-document columns are -inf before the max;
-//  * running max per query row: m <- max(m, tile max); argmax moves only on a
-//    strictly greater tile max, and inside a tile the lowest column wins, so
-//    the overall lowest index wins among equal maxima;
-//  * at a document end: m <- 0 unless finite and the row is active, then the
+// Epilogue ("late-interaction-kernels" notes, "Forward"):
+//  * running max per query row: m <- max(m, chunk max); the argmax moves only
+//    on a strictly greater chunk max and, inside a 32-column chunk, takes the
+//    lowest column: the overall lowest index wins among equal maxima;
+//  * at a document's end: m <- 0 unless finite and the row is active, then the
 //    rows of each query are summed (warp shuffles, then a fixed-order sum of
 //    per-warp partials), so the scores are bitwise reproducible.
 #pragma once
@@ -37,13 +47,15 @@
 
 namespace maxsim {
 
-constexpr int kBN = 128;          // document tokens per tile (MMA N)
+constexpr int kBN = 128;          // document tokens per tile (largest MMA N)
 constexpr int kBM = 128;          // query rows per M-tile (MMA M)
 constexpr int kMaxMT = 4;         // M-tiles per row block
 constexpr int kNAcc = 4;          // TMEM accumulator buffers (4 x 128 columns)
-constexpr int kThreads = 256;     // warp 0 TMA, warp 1 MMA, warps 4-7 epilogue
+constexpr int kThreads = 256;     // warp 0 TMA, warp 1 MMA, warps 2-3 prep, warps 4-7 epilogue
 constexpr int kEpiWarp0 = 4;
-constexpr int kAtomBytes = 128 * 128;  // one 128-row x 64-element (128 B) swizzled block
+constexpr int kPrepThreads = 64;
+constexpr int kAtomBytes = 128 * 128;  // one 128-row x 128-byte swizzled block
+constexpr int kMaxStages = 8;
 
 // Device status codes (match maxsim_status).
 constexpr int kStatusTimeout = 4;
@@ -56,7 +68,8 @@ struct FwdArgs {
     int32_t lq_out;       // argmax columns per (i, j) row
     const uint8_t* q_active;  // [R] nonzero = row contributes (NULL = all)
     const uint8_t* q_real;    // [R] nonzero = a real token (NULL = all)
-    int32_t rb_rows;      // rows per row block (multiple of 32, or of lq_pad if smaller)
+    const float* q_scale;     // [R] INT8 mode: per-row query scale
+    int32_t rb_rows;      // rows per row block
     int32_t n_chunks;     // row blocks per query (> 1 only when lq_pad > rb_rows)
     int32_t n_rb;
     // documents (packed token rows)
@@ -64,7 +77,8 @@ struct FwdArgs {
     int32_t nd;
     int32_t ld;
     int32_t total_d;
-    const uint8_t* d_mask;  // [total_d] or NULL
+    const uint8_t* d_mask;   // [total_d] or NULL
+    const float* d_scale;    // [total_d] INT8 mode: per-token document scale
     int32_t n_dr;         // document ranges
     int32_t n_units;      // n_rb * n_dr
     // outputs
@@ -73,10 +87,14 @@ struct FwdArgs {
     int32_t* argmax;      // [nq * nd, lq_out] or NULL
     // operand geometry
     int32_t k_steps;      // dim / 16 MMA instructions per tile
-    int32_t k_atoms;      // ceil(dim / 64) swizzled 64-element blocks per row
-    int32_t stages;       // D ring depth
-    int32_t q_slots;      // M-tiles of Q resident in shared memory (>= every row block's mt)
-    uint32_t idesc;       // tcgen05 instruction descriptor
+    int32_t k_atoms;      // 64-element (128-byte) blocks of a 16-bit operand row
+    int32_t k8_atoms;     // 128-element blocks of an INT8 row (INT8 mode)
+    int32_t dim;
+    int32_t stages;       // operand ring depth
+    int32_t stages8;      // INT8 staging ring depth (INT8 mode)
+    int32_t q_slots;      // M-tiles of Q resident in shared memory
+    uint32_t idesc;       // tcgen05 instruction descriptor without N
+    uint32_t nan_pair;    // two 16-bit NaNs of the operand type
     int* status;          // device status word
     uint64_t timeout_ns;  // bound on any single wait
 };
@@ -136,35 +154,73 @@ __device__ __forceinline__ int32_t range_first_doc(const FwdArgs& a, int32_t dr)
 struct Unit {
     RowBlock rb;
     int32_t j0, j1;      // documents [j0, j1)
-    int32_t tok0, tok1;  // their tokens [tok0, tok1)
-    int32_t ntiles;
+    int32_t tok0;        // first token of document j0
 };
 
 __device__ __forceinline__ Unit make_unit(const FwdArgs& a, int32_t u) {
     Unit w;
-    int32_t rb = u % a.n_rb;
-    int32_t dr = u / a.n_rb;
-    w.rb = row_block(a, rb);
+    w.rb = row_block(a, u % a.n_rb);
+    const int32_t dr = u / a.n_rb;
     w.j0 = range_first_doc(a, dr);
     w.j1 = range_first_doc(a, dr + 1);
     w.tok0 = doc_start(a, w.j0);
-    w.tok1 = doc_start(a, w.j1);
-    w.ntiles = w.tok1 > w.tok0 ? (w.tok1 - w.tok0 + kBN - 1) / kBN : 0;
     return w;
 }
 
+// Walks the tiles of a unit in order: documents j0..j1-1, each cut into tiles
+// of up to kBN of its own tokens; empty documents have no tile.
+struct TileWalk {
+    int32_t j, j1, ds, de, de_next, t0;
+    __device__ __forceinline__ void begin(const FwdArgs& a, const Unit& w) {
+        j = w.j0;
+        j1 = w.j1;
+        ds = w.tok0;
+        de = j < j1 ? doc_start(a, j + 1) : ds;
+        de_next = j + 1 < j1 ? doc_start(a, j + 2) : de;
+        t0 = 0;
+        skip_empty(a);
+    }
+    __device__ __forceinline__ void next_doc(const FwdArgs& a) {
+        ++j;
+        ds = de;
+        de = de_next;
+        de_next = j + 1 < j1 ? doc_start(a, j + 2) : de;
+        t0 = 0;
+    }
+    __device__ __forceinline__ void skip_empty(const FwdArgs& a) {
+        while (j < j1 && de <= ds) next_doc(a);
+    }
+    __device__ __forceinline__ bool valid() const { return j < j1; }
+    __device__ __forceinline__ int32_t row() const { return ds + t0; }                 // first token row
+    __device__ __forceinline__ int32_t ntok() const { return min(kBN, de - ds - t0); }  // real tokens
+    __device__ __forceinline__ bool last_of_doc() const { return ds + t0 + kBN >= de; }
+    __device__ __forceinline__ void advance(const FwdArgs& a) {
+        if (last_of_doc()) {
+            next_doc(a);
+            skip_empty(a);
+        } else {
+            t0 += kBN;
+        }
+    }
+};
+
+__device__ __forceinline__ int32_t mma_n(int32_t ntok) { return (ntok + 15) & ~15; }
+
 // Shared-memory control block (after the operand buffers).
-struct SmemCtl {
+struct alignas(16) SmemCtl {
     uint64_t q_full, q_empty;
-    uint64_t d_full[8], d_empty[8];
+    uint64_t d_full[kMaxStages], d_ready[kMaxStages], d_empty[kMaxStages];
+    uint64_t d8_full[kMaxStages], d8_empty[kMaxStages];
     uint64_t acc_full[kNAcc], acc_empty[kNAcc];
     uint64_t mma_done;
     uint64_t epi_bar;  // rendezvous of the four epilogue warps
     uint32_t tmem_base;
     volatile int32_t abort;
-    int32_t slot_doc[kBN];
-    float wslot[kBN][kMaxMT * 4];
+    float wslot[kMaxMT * 4];   // per-warp partial sums of the document being closed
 };
+// INT8 mode only: after the control block, a per-warp copy of the tile's
+// document scales, float[4][kBN].
+constexpr int kDScaleBytes = 4 * kBN * 4;
 
 __device__ __forceinline__ void record_status(const FwdArgs& a, int code) {
     if (a.status) atomicCAS(a.status, 0, code);
@@ -200,6 +256,7 @@ __device__ __forceinline__ bool epi_sync(const FwdArgs& a, SmemCtl* ctl, uint32_
 
 // ---------------------------------------------------------------- epilogue helpers
 
+// max over 32 values and m; NaN entries are ignored by max.f32.
 __device__ __forceinline__ float chunk_max(const float (&x)[32], float m) {
     float a0 = fmax3(x[0], x[1], x[2]), a1 = fmax3(x[3], x[4], x[5]), a2 = fmax3(x[6], x[7], x[8]);
     float a3 = fmax3(x[9], x[10], x[11]), a4 = fmax3(x[12], x[13], x[14]), a5 = fmax3(x[15], x[16], x[17]);
@@ -209,27 +266,16 @@ __device__ __forceinline__ float chunk_max(const float (&x)[32], float m) {
     return fmax3(b1, b2, b3);
 }
 
-// Fold columns whose bit is set in `valid` into (m, am). `col0` is the index,
-// relative to the document start, of column 0 of the chunk.
+// Fold one 32-column chunk into (m, am); col0 = index of column 0 relative to
+// the document's first token.
 template <bool kArg>
-__device__ __forceinline__ void fold_chunk(const float (&x)[32], uint32_t valid, int32_t col0, float& m,
-                                           int32_t& am) {
-    const float kNegInf = __int_as_float(0xff800000u);
+__device__ __forceinline__ void fold_chunk(const float (&y)[32], int32_t col0, float& m, int32_t& am) {
     if constexpr (!kArg) {
-        if (valid == 0xFFFFFFFFu) {
-            m = chunk_max(x, m);
-        } else {
-            float y[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) y[e] = (valid >> e) & 1u ? x[e] : kNegInf;
-            m = chunk_max(y, m);
-        }
+        m = chunk_max(y, m);
     } else {
-        float y[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) y[e] = (valid >> e) & 1u ? x[e] : kNegInf;
+        const float kNegInf = __int_as_float(0xff800000u);
         const float cm = chunk_max(y, kNegInf);
-        const bool upd = cm > m;
+        const bool upd = cm > m;  // false for NaN
         if (__any_sync(0xFFFFFFFFu, upd)) {
             int32_t idx = 31;
 #pragma unroll
@@ -242,34 +288,44 @@ __device__ __forceinline__ void fold_chunk(const float (&x)[32], uint32_t valid,
     }
 }
 
-__device__ __forceinline__ uint32_t seg_bits(int32_t lo, int32_t hi) {  // bits [lo, hi), 0 <= lo < hi <= 32
-    uint32_t upto = hi >= 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u);
-    return upto & ~((1u << lo) - 1u);
-}
-
 // ---------------------------------------------------------------- the kernel
 
-template <bool kArg, bool kDMask>
+template <bool kArg, bool kInt8>
 __global__ void __launch_bounds__(kThreads, 1)
     maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_d,
                       const FwdArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int32_t q_tile_bytes = a.k_atoms * kAtomBytes;   // one 128-row M-tile of Q
-    const int32_t d_stage_bytes = a.k_atoms * kAtomBytes;  // one 128-token tile of D
+    const int32_t q_tile_bytes = a.k_atoms * kAtomBytes;    // one 128-row M-tile of Q
+    const int32_t d_stage_bytes = a.k_atoms * kAtomBytes;   // one 128-token operand tile
+    const int32_t d8_stage_bytes = a.k8_atoms * kAtomBytes; // one 128-token INT8 tile
     uint8_t* sQ = smem;
     uint8_t* sD = smem + a.q_slots * q_tile_bytes;
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sD + a.stages * d_stage_bytes);
+    uint8_t* sD8 = sD + a.stages * d_stage_bytes;
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sD8 + (kInt8 ? a.stages8 * d8_stage_bytes : 0));
+    float* dscale = reinterpret_cast<float*>(ctl + 1);  // [4][kBN], INT8 mode
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+
+    // Ring depths index fixed-size barrier arrays: refuse a launch that breaks them.
+    if (a.stages < 1 || a.stages > kMaxStages || (kInt8 && (a.stages8 < 1 || a.stages8 > kMaxStages)) ||
+        a.q_slots < 1 || a.q_slots > kMaxMT) {
+        if (threadIdx.x == 0) record_status(a, kStatusBadInput);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&ctl->q_full), 1);
         mbar_init(smem_u32(&ctl->q_empty), 1);
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(smem_u32(&ctl->d_full[s]), 1);
+            mbar_init(smem_u32(&ctl->d_ready[s]), 2);
             mbar_init(smem_u32(&ctl->d_empty[s]), 1);
+        }
+        for (int s = 0; s < a.stages8; ++s) {
+            mbar_init(smem_u32(&ctl->d8_full[s]), 1);
+            mbar_init(smem_u32(&ctl->d8_empty[s]), 2);
         }
         for (int b = 0; b < kNAcc; ++b) {
             mbar_init(smem_u32(&ctl->acc_full[b]), 1);
@@ -295,66 +351,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol_stream = l2_policy_evict_first();
+            // f16/bf16: tiles go straight into the operand ring; INT8: into the staging ring
+            const int32_t ring = kInt8 ? a.stages8 : a.stages;
+            const int32_t bytes = kInt8 ? d8_stage_bytes : d_stage_bytes;
+            const int32_t boxes = kInt8 ? a.k8_atoms : a.k_atoms;
+            const int32_t box_cols = kInt8 ? 128 : 64;
+            uint8_t* base = kInt8 ? sD8 : sD;
             int32_t stage = 0;
-            uint32_t phase = 0;
-            uint32_t q_phase = 0;
+            uint32_t phase = 0, q_phase = 0;
             bool first_unit = true;
             int64_t issued = 0;
-            for (int32_t u = blockIdx.x; u < a.n_units; u += gridDim.x) {
-                Unit w = make_unit(a, u);
+            bool ok = true;
+            for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+                const Unit w = make_unit(a, u);
                 if (!first_unit) {
                     if (!wait_bar(a, ctl, smem_u32(&ctl->q_empty), q_phase)) break;
                     q_phase ^= 1u;
                 }
                 first_unit = false;
-                uint32_t qbar = smem_u32(&ctl->q_full);
+                const uint32_t qbar = smem_u32(&ctl->q_full);
                 mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(w.rb.mt * q_tile_bytes));
                 for (int32_t k = 0; k < w.rb.mt; ++k)
                     for (int32_t ka = 0; ka < a.k_atoms; ++ka)
                         tma_load_2d(smem_u32(sQ + k * q_tile_bytes + ka * kAtomBytes), &tm_q, qbar, ka * 64,
                                     w.rb.row0 + k * kBM);
-                bool ok = true;
-                for (int32_t t = 0; t < w.ntiles; ++t) {
-                    if (!wait_bar(a, ctl, smem_u32(&ctl->d_empty[stage]), phase ^ 1u)) { ok = false; break; }
-                    uint32_t dbar = smem_u32(&ctl->d_full[stage]);
-                    mbar_arrive_expect_tx(dbar, static_cast<uint32_t>(d_stage_bytes));
-                    for (int32_t ka = 0; ka < a.k_atoms; ++ka)
-                        tma_load_2d_hint(smem_u32(sD + stage * d_stage_bytes + ka * kAtomBytes), &tm_d, dbar,
-                                         ka * 64, w.tok0 + t * kBN, pol_stream);
+                TileWalk tw;
+                for (tw.begin(a, w); tw.valid(); tw.advance(a)) {
+                    const uint32_t empty = smem_u32(kInt8 ? &ctl->d8_empty[stage] : &ctl->d_empty[stage]);
+                    if (!wait_bar(a, ctl, empty, phase ^ 1u)) { ok = false; break; }
+                    const uint32_t fullb = smem_u32(kInt8 ? &ctl->d8_full[stage] : &ctl->d_full[stage]);
+                    mbar_arrive_expect_tx(fullb, static_cast<uint32_t>(bytes));
+                    for (int32_t ka = 0; ka < boxes; ++ka)
+                        tma_load_2d_hint(smem_u32(base + stage * bytes + ka * kAtomBytes), &tm_d, fullb,
+                                         ka * box_cols, tw.row(), pol_stream);
                     ++issued;
-                    if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+                    if (++stage == ring) { stage = 0; phase ^= 1u; }
                 }
-                if (!ok) break;
             }
             if (ctl->abort) {
                 // Let every copy still in flight land before the CTA exits.
-                int64_t outstanding = issued < a.stages ? issued : a.stages;
+                const int64_t outstanding = issued < ring ? issued : ring;
                 int32_t s = stage;
                 uint32_t ph = phase;
                 for (int64_t n = 0; n < outstanding; ++n) {
-                    if (--s < 0) { s = a.stages - 1; ph ^= 1u; }
-                    uint64_t t0 = global_timer_ns();
-                    while (!mbar_try_wait(smem_u32(&ctl->d_full[s]), ph) && global_timer_ns() - t0 < a.timeout_ns) {}
+                    if (--s < 0) { s = ring - 1; ph ^= 1u; }
+                    const uint32_t fullb = smem_u32(kInt8 ? &ctl->d8_full[s] : &ctl->d_full[s]);
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait(fullb, ph) && global_timer_ns() - t0 < a.timeout_ns) {}
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int32_t stage = 0;
-            uint32_t phase = 0;
-            int32_t acc = 0;
-            uint32_t acc_phase = 0;
-            uint32_t q_phase = 0;
+            int32_t stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0, q_phase = 0;
             bool ok = true;
             for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-                Unit w = make_unit(a, u);
+                const Unit w = make_unit(a, u);
                 if (!wait_bar(a, ctl, smem_u32(&ctl->q_full), q_phase)) break;
                 q_phase ^= 1u;
                 tc_fence_after();
-                for (int32_t t = 0; t < w.ntiles; ++t) {
-                    if (!wait_bar(a, ctl, smem_u32(&ctl->d_full[stage]), phase)) { ok = false; break; }
+                TileWalk tw;
+                for (tw.begin(a, w); tw.valid() && ok; tw.advance(a)) {
+                    if (!wait_bar(a, ctl, smem_u32(&ctl->d_ready[stage]), phase)) { ok = false; break; }
                     tc_fence_after();
+                    const uint32_t idesc = a.idesc | (static_cast<uint32_t>(mma_n(tw.ntok()) >> 3) << 17);
                     const uint32_t d_base = smem_u32(sD + stage * d_stage_bytes);
                     for (int32_t k = 0; k < w.rb.mt; ++k) {
                         if (!wait_bar(a, ctl, smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u)) { ok = false; break; }
@@ -363,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
                         for (int32_t ks = 0; ks < a.k_steps; ++ks) {
                             const uint32_t off = static_cast<uint32_t>((ks >> 2) * kAtomBytes + (ks & 3) * 32);
-                            mma_f16_ss(d_tmem, sdesc_k_sw128(q_base + off), sdesc_k_sw128(d_base + off), a.idesc,
+                            mma_f16_ss(d_tmem, sdesc_k_sw128(q_base + off), sdesc_k_sw128(d_base + off), idesc,
                                        ks > 0 ? 1u : 0u);
                         }
                         mma_commit(smem_u32(&ctl->acc_full[acc]));
@@ -378,45 +440,114 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Drain: wait until every MMA issued above has completed.
             mma_commit(smem_u32(&ctl->mma_done));
-            uint64_t t0 = global_timer_ns();
+            const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(smem_u32(&ctl->mma_done), 0) && global_timer_ns() - t0 < a.timeout_ns) {}
         }
-    } else if (warp >= kEpiWarp0) {
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------------ operand prep
+        // f16/bf16: NaN-fill masked / padding rows in place. INT8: convert the
+        // staged INT8 tile to f16 rows (NaN for masked / padding rows).
+        const int pt = threadIdx.x - 64;  // 0..63
+        int32_t stage = 0, stage8 = 0;
+        uint32_t phase = 0, phase8 = 0;
+        bool ok = true;
+        for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+            const Unit w = make_unit(a, u);
+            TileWalk tw;
+            for (tw.begin(a, w); tw.valid(); tw.advance(a)) {
+                const int32_t n = tw.ntok(), N = mma_n(n), row0 = tw.row();
+                uint8_t* dst = sD + stage * d_stage_bytes;
+                if constexpr (kInt8) {
+                    if (!wait_bar(a, ctl, smem_u32(&ctl->d8_full[stage8]), phase8)) { ok = false; break; }
+                    if (!wait_bar(a, ctl, smem_u32(&ctl->d_empty[stage]), phase ^ 1u)) { ok = false; break; }
+                    const uint8_t* src = sD8 + stage8 * d8_stage_bytes;
+                    const int32_t chunks = a.dim >> 4;  // 16-byte INT8 chunks per row
+                    for (int32_t x = pt; x < N * chunks; x += kPrepThreads) {
+                        const int32_t r = x / chunks, c = x - (x / chunks) * chunks;
+                        const bool nan_row = r >= n || (a.d_mask != nullptr && a.d_mask[row0 + r] == 0);
+                        uint4 lo, hi;
+                        if (nan_row) {
+                            lo = make_uint4(a.nan_pair, a.nan_pair, a.nan_pair, a.nan_pair);
+                            hi = lo;
+                        } else {
+                            // INT8 rows: 128-byte swizzled rows of 128 elements per staging block
+                            const int32_t blk = c >> 3, cc = c & 7;
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                src + blk * kAtomBytes + r * 128 + ((cc ^ (r & 7)) << 4));
+                            lo = i8x8_to_f16x8(v.x, v.y);
+                            hi = i8x8_to_f16x8(v.z, v.w);
+                        }
+                        // 16 f16 values = two 16-byte chunks of a 64-element swizzled atom
+                        const int32_t atom = c >> 2, c16 = (c & 3) * 2;
+                        uint8_t* rowp = dst + atom * kAtomBytes + r * 128;
+                        *reinterpret_cast<uint4*>(rowp + (((c16 + 0) ^ (r & 7)) << 4)) = lo;
+                        *reinterpret_cast<uint4*>(rowp + (((c16 + 1) ^ (r & 7)) << 4)) = hi;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&ctl->d_ready[stage]));
+                        mbar_arrive(smem_u32(&ctl->d8_empty[stage8]));
+                    }
+                    if (++stage8 == a.stages8) { stage8 = 0; phase8 ^= 1u; }
+                } else {
+                    if (!wait_bar(a, ctl, smem_u32(&ctl->d_full[stage]), phase)) { ok = false; break; }
+                    if (a.d_mask != nullptr || N != n) {
+                        const uint4 nan4 = make_uint4(a.nan_pair, a.nan_pair, a.nan_pair, a.nan_pair);
+                        for (int32_t r = pt; r < N; r += kPrepThreads) {
+                            if (r < n && (a.d_mask == nullptr || a.d_mask[row0 + r] != 0)) continue;
+                            for (int32_t ka = 0; ka < a.k_atoms; ++ka) {
+                                uint4* rowp = reinterpret_cast<uint4*>(dst + ka * kAtomBytes + r * 128);
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) rowp[c] = nan4;
+                            }
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ctl->d_ready[stage]));
+                }
+                if (++stage == a.stages) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else {
         // ------------------------------------------------------------ epilogue
         const float kNegInf = __int_as_float(0xff800000u);
-        const int e = warp - kEpiWarp0;      // TMEM lane quadrant
+        const float kNaN = __int_as_float(0x7fffffffu);
+        const int e = warp - kEpiWarp0;               // TMEM lane quadrant
         const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..127
         int32_t acc = 0;
-        uint32_t acc_phase = 0;
-        uint32_t epi_phase = 0;
+        uint32_t acc_phase = 0, epi_phase = 0;
         bool ok = true;
         for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
             const Unit w = make_unit(a, u);
             const RowBlock& rb = w.rb;
+            const bool chunked = a.n_chunks > 1;
             // per-row facts for each M-tile this thread reads
             int32_t row_i[kMaxMT], row_s[kMaxMT];
             bool in_rb[kMaxMT], real[kMaxMT], active[kMaxMT];
+            float qsc[kMaxMT];
 #pragma unroll
             for (int k = 0; k < kMaxMT; ++k) {
-                int32_t r = rb.row0 + k * kBM + e * 32 + lane;
+                const int32_t r = rb.row0 + k * kBM + e * 32 + lane;
                 in_rb[k] = k < rb.mt && r < rb.row_end;
                 row_i[k] = r / a.lq_pad;
                 row_s[k] = r - row_i[k] * a.lq_pad;
                 real[k] = in_rb[k] && (a.q_real == nullptr || a.q_real[r] != 0);
                 active[k] = real[k] && (a.q_active == nullptr || a.q_active[r] != 0);
+                qsc[k] = (kInt8 && in_rb[k]) ? a.q_scale[r] : 1.f;
             }
-            const bool chunked = a.n_chunks > 1;
             // empty documents: score 0 and argmax -1, written up front
             for (int32_t j = w.j0 + et; j < w.j1; j += 128) {
-                if (doc_start(a, j + 1) != doc_start(a, j)) continue;
+                if (doc_start(a, j + 1) > doc_start(a, j)) continue;
                 for (int32_t q = 0; q < rb.nqb; ++q) {
-                    int32_t i = rb.q0 + q;
+                    const int32_t i = rb.q0 + q;
                     if (chunked) a.partial[(static_cast<int64_t>(rb.chunk) * a.nq + i) * a.nd + j] = 0.f;
                     else a.scores[static_cast<int64_t>(i) * a.nd + j] = 0.f;
                 }
                 if (kArg) {
                     for (int32_t r = rb.row0; r < rb.row_end; ++r) {
-                        int32_t i = r / a.lq_pad, s = r - (r / a.lq_pad) * a.lq_pad;
+                        const int32_t i = r / a.lq_pad, s = r - (r / a.lq_pad) * a.lq_pad;
                         if (s < a.lq_out) a.argmax[(static_cast<int64_t>(i) * a.nd + j) * a.lq_out + s] = -1;
                     }
                 }
@@ -425,26 +556,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t am[kMaxMT];
 #pragma unroll
             for (int k = 0; k < kMaxMT; ++k) { m[k] = kNegInf; am[k] = -1; }
-            // document cursor: first non-empty document at or after j0
-            int32_t cj = w.j0;
-            int32_t cds = w.tok0;
-            int32_t cde = w.j0 < w.j1 ? doc_start(a, w.j0 + 1) : w.tok0;
 
-            for (int32_t t = 0; t < w.ntiles && ok; ++t) {
-                const int32_t ts = w.tok0 + t * kBN;
-                const int32_t te = min(ts + kBN, w.tok1);
-                uint32_t dmw[4];
+            TileWalk tw;
+            for (tw.begin(a, w); tw.valid() && ok; tw.advance(a)) {
+                const int32_t n = tw.ntok(), N = mma_n(n);
+                const int32_t nfull = N >> 5;
+                const bool half = (N & 31) != 0;
+                const bool closes = tw.last_of_doc();
+                if constexpr (kInt8) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (kDMask) {
-                        int32_t col = ts + c * 32 + lane;
-                        dmw[c] = __ballot_sync(0xFFFFFFFFu, col < te && col < a.total_d && a.d_mask[col] != 0);
-                    } else {
-                        dmw[c] = 0xFFFFFFFFu;
+                    for (int c = 0; c < 4; ++c) {
+                        const int32_t t = c * 32 + lane;
+                        dscale[e * kBN + t] = t < n ? __ldg(a.d_scale + tw.row() + t) : 0.f;
                     }
+                    __syncwarp();
                 }
-                int32_t nslot = 0;
-                int32_t end_j = cj, end_ds = cds, end_de = cde;
 #pragma unroll
                 for (int k = 0; k < kMaxMT; ++k) {
                     if (k >= rb.mt) break;
@@ -454,85 +580,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(e * 32) << 16) +
                                            static_cast<uint32_t>(acc * kBN);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_ld32(taddr + c * 32, v[c]);
+                    for (int c = 0; c < 4; ++c) {
+                        if (c < nfull) {
+                            tmem_ld32(taddr + c * 32, v[c]);
+                        } else if (c == nfull && half) {
+                            tmem_ld16(taddr + c * 32, v[c]);
+#pragma unroll
+                            for (int x = 16; x < 32; ++x) v[c][x] = kNaN;
+                        }
+                    }
                     tmem_wait_ld();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[acc]));
                     if (++acc == kNAcc) { acc = 0; acc_phase ^= 1u; }
-
-                    // walk the documents covered by this tile
-                    int32_t jj = cj, ds = cds, de = cde;
-                    int32_t pos = ts;
-                    int32_t slot = 0;
-                    auto flush = [&](int32_t jdoc) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (c < nfull + (half ? 1 : 0)) {
+                            if constexpr (kInt8) {
+                                const float4* sc = reinterpret_cast<const float4*>(dscale + e * kBN + c * 32);
+#pragma unroll
+                                for (int x = 0; x < 8; ++x) {
+                                    const float4 s4 = sc[x];
+                                    v[c][4 * x + 0] *= s4.x;
+                                    v[c][4 * x + 1] *= s4.y;
+                                    v[c][4 * x + 2] *= s4.z;
+                                    v[c][4 * x + 3] *= s4.w;
+                                }
+                            }
+                            fold_chunk<kArg>(v[c], tw.t0 + c * 32, m[k], am[k]);
+                        }
+                    }
+                    if (closes) {
                         const bool has = m[k] > kNegInf;
                         if (kArg && in_rb[k] && row_s[k] < a.lq_out)
-                            a.argmax[(static_cast<int64_t>(row_i[k]) * a.nd + jdoc) * a.lq_out + row_s[k]] =
+                            a.argmax[(static_cast<int64_t>(row_i[k]) * a.nd + tw.j) * a.lq_out + row_s[k]] =
                                 (real[k] && has) ? am[k] : -1;
-                        float val = (active[k] && has) ? m[k] : 0.f;
+                        float val = (active[k] && has) ? m[k] * qsc[k] : 0.f;
                         if (a.lq_pad >= 32) {
 #pragma unroll
                             for (int o = 16; o > 0; o >>= 1) val += __shfl_xor_sync(0xFFFFFFFFu, val, o);
-                            if (lane == 0) ctl->wslot[slot][k * 4 + e] = val;
-                            if (k == 0 && e == 0 && lane == 0) ctl->slot_doc[slot] = jdoc;
+                            if (a.lq_pad == 32 && !chunked) {
+                                if (lane == 0 && in_rb[k]) a.scores[static_cast<int64_t>(row_i[k]) * a.nd + tw.j] = val;
+                            } else if (lane == 0) {
+                                ctl->wslot[k * 4 + e] = val;
+                            }
                         } else {
                             for (int o = a.lq_pad >> 1; o > 0; o >>= 1) val += __shfl_xor_sync(0xFFFFFFFFu, val, o);
                             if (in_rb[k] && (lane & (a.lq_pad - 1)) == 0)
-                                a.scores[static_cast<int64_t>(row_i[k]) * a.nd + jdoc] = val;
+                                a.scores[static_cast<int64_t>(row_i[k]) * a.nd + tw.j] = val;
                         }
-                        ++slot;
                         m[k] = kNegInf;
                         am[k] = -1;
-                    };
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int32_t cs = ts + c * 32;
-                        if (cs < te) {
-                            const int32_t ce = min(cs + 32, te);
-                            while (true) {
-                                while (jj < w.j1 && de <= pos) {
-                                    if (de > ds) flush(jj);
-                                    ++jj;
-                                    ds = de;
-                                    de = jj < w.j1 ? doc_start(a, jj + 1) : de;
-                                }
-                                if (jj >= w.j1 || pos >= ce) break;
-                                const int32_t hi = min(de, ce);
-                                const uint32_t valid = seg_bits(pos - cs, hi - cs) & dmw[c];
-                                fold_chunk<kArg>(v[c], valid, cs - ds, m[k], am[k]);
-                                pos = hi;
-                            }
-                        }
                     }
-                    while (jj < w.j1 && de <= pos) {
-                        if (de > ds) flush(jj);
-                        ++jj;
-                        ds = de;
-                        de = jj < w.j1 ? doc_start(a, jj + 1) : de;
-                    }
-                    nslot = slot;
-                    end_j = jj;
-                    end_ds = ds;
-                    end_de = de;
                 }
                 if (!ok) break;
-                cj = end_j;
-                cds = end_ds;
-                cde = end_de;
-                if (a.lq_pad >= 32 && nslot > 0) {
+                if (closes && (a.lq_pad > 32 || (a.lq_pad == 32 && chunked))) {
                     if (!epi_sync(a, ctl, epi_phase)) { ok = false; break; }
-                    const int32_t wpq = a.lq_pad / 32;  // warps per query (capped by the block)
-                    for (int32_t x = et; x < nslot * rb.nqb; x += 128) {
-                        const int32_t sl = x / rb.nqb, q = x - (x / rb.nqb) * rb.nqb;
-                        const int32_t wb = q * wpq;
+                    if (et < rb.nqb) {
+                        const int32_t wpq = a.lq_pad / 32;  // warps per query (capped by the block)
+                        const int32_t wb = et * wpq;
                         const int32_t we = min(wb + wpq, (rb.row_end - rb.row0) / 32);
                         float sum = 0.f;
-                        for (int32_t ww = wb; ww < we; ++ww) sum += ctl->wslot[sl][ww];
-                        const int32_t jdoc = ctl->slot_doc[sl];
-                        const int32_t i = rb.q0 + q;
-                        if (chunked) a.partial[(static_cast<int64_t>(rb.chunk) * a.nq + i) * a.nd + jdoc] = sum;
-                        else a.scores[static_cast<int64_t>(i) * a.nd + jdoc] = sum;
+                        for (int32_t ww = wb; ww < we; ++ww) sum += ctl->wslot[ww];
+                        const int32_t i = rb.q0 + et;
+                        if (chunked) a.partial[(static_cast<int64_t>(rb.chunk) * a.nq + i) * a.nd + tw.j] = sum;
+                        else a.scores[static_cast<int64_t>(i) * a.nd + tw.j] = sum;
                     }
                     if (!epi_sync(a, ctl, epi_phase)) { ok = false; break; }
                 }

@@ -24,6 +24,7 @@ namespace {
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s bound on any single device-side wait
 constexpr int kMaxDevices = 64;
+constexpr size_t kSmemBudget = 232448;          // 227 KB: opt-in shared memory per block on sm_100 / sm_103
 
 struct DeviceInfo {
     bool init = false;
@@ -55,6 +56,7 @@ maxsim_status device_info(DeviceInfo** out) {
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (major != 10 || minor != 3) return MAXSIM_ERR_UNSUPPORTED;  // built for sm_103a only
+        if (static_cast<size_t>(d.smem_optin) < kSmemBudget) return MAXSIM_ERR_UNSUPPORTED;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return MAXSIM_ERR_CUDA;
         d.status = static_cast<int*>(p);
@@ -73,10 +75,11 @@ maxsim_status device_info(DeviceInfo** out) {
     return MAXSIM_OK;
 }
 
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline bool aligned16(const void* p) { return aligned(p, 16); }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// 2-D row-major [rows, cols] tensor, loaded as 64-element x box_rows boxes with
+// 2-D row-major [rows, cols] tensor, loaded as box_cols x box_rows boxes with
 // the 128-byte swizzle (the layout the tcgen05 descriptors expect).
 bool encode_rows(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t cols,
                  uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
@@ -96,10 +99,11 @@ struct FwdPlan {
     int64_t lq_pad = 0;
     int32_t rb_rows = 0, n_chunks = 1;
     int64_t n_rb = 0;
-    int32_t k_atoms = 0, k_steps = 0, mt_max = 0;
+    int32_t k_atoms = 0, k8_atoms = 0, k_steps = 0, mt_max = 0, stages = 0, stages8 = 0;
     int64_t rows = 0;  // padded query rows
-    bool repack = false;
-    size_t off_q = 0, off_real = 0, off_active = 0, off_partial = 0, ws_bytes = 0;
+    bool repack = false, int8 = false, ok = false;
+    size_t smem = 0;
+    size_t off_q = 0, off_real = 0, off_active = 0, off_qscale = 0, off_partial = 0, ws_bytes = 0;
 };
 
 inline int64_t pad_lq(int64_t lq) {
@@ -111,16 +115,51 @@ inline int64_t pad_lq(int64_t lq) {
     return (lq + 31) / 32 * 32;
 }
 
-// mt_max by operand width: the resident query block plus two document stages
-// must fit in shared memory.
-inline int32_t mt_for_atoms(int32_t k_atoms) { return k_atoms <= 2 ? 4 : (k_atoms == 3 ? 2 : 1); }
+size_t fwd_smem_bytes(int32_t mt, int32_t k_atoms, int32_t stages, int32_t k8_atoms, int32_t stages8) {
+    size_t b = 1024 + static_cast<size_t>(mt) * k_atoms * kAtomBytes +
+               static_cast<size_t>(stages) * k_atoms * kAtomBytes + sizeof(SmemCtl);
+    if (stages8 > 0) b += static_cast<size_t>(stages8) * k8_atoms * kAtomBytes + kDScaleBytes;
+    return b;
+}
 
-FwdPlan plan_fwd(int64_t nq, int64_t lq, int64_t nd, int64_t dim, int elem_bytes, bool varlen_q, bool int8) {
+// Resident query M-tiles and ring depths: the most query rows per pass, then
+// the deepest document rings that fit (the 16-bit operand ring keeps two
+// stages when it can; wide INT8 rows fall back to one). Returns false when
+// nothing fits; the entry points then reject the shape.
+bool choose_pipeline(FwdPlan& p) {
+    for (int32_t min_stages = 2; min_stages >= 1; --min_stages) {
+        for (int32_t mt = kMaxMT; mt >= 1; --mt) {
+            if (!p.int8) {
+                if (min_stages < 2 || fwd_smem_bytes(mt, p.k_atoms, 2, 0, 0) > kSmemBudget) continue;
+                int32_t s = kMaxStages;
+                while (fwd_smem_bytes(mt, p.k_atoms, s, 0, 0) > kSmemBudget) --s;
+                p.mt_max = mt;
+                p.stages = s;
+                p.stages8 = 0;
+            } else {
+                if (fwd_smem_bytes(mt, p.k_atoms, min_stages, p.k8_atoms, 2) > kSmemBudget) continue;
+                int32_t s8 = kMaxStages;
+                while (fwd_smem_bytes(mt, p.k_atoms, min_stages, p.k8_atoms, s8) > kSmemBudget) --s8;
+                p.mt_max = mt;
+                p.stages = min_stages;
+                p.stages8 = s8;
+            }
+            p.smem = fwd_smem_bytes(p.mt_max, p.k_atoms, p.stages, p.k8_atoms, p.stages8);
+            return true;
+        }
+    }
+    return false;
+}
+
+FwdPlan plan_fwd(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varlen_q, bool int8) {
     FwdPlan p;
+    p.int8 = int8;
     p.lq_pad = pad_lq(lq);
     p.k_atoms = static_cast<int32_t>((dim + 63) / 64);
+    p.k8_atoms = int8 ? static_cast<int32_t>((dim + 127) / 128) : 0;
     p.k_steps = static_cast<int32_t>(dim / 16);
-    p.mt_max = mt_for_atoms(p.k_atoms);
+    p.ok = choose_pipeline(p);
+    if (!p.ok) p.mt_max = 1;  // keeps the sizes below defined; the entry points reject the shape
     const int64_t rb_max = static_cast<int64_t>(kBM) * p.mt_max;
     if (p.lq_pad <= rb_max) {
         int64_t qpb = rb_max / p.lq_pad;
@@ -137,31 +176,22 @@ FwdPlan plan_fwd(int64_t nq, int64_t lq, int64_t nd, int64_t dim, int elem_bytes
     size_t off = 0;
     if (p.repack) {
         p.off_q = off;
-        off = round_up(off + static_cast<size_t>(p.rows) * dim * 2, 256);  // bf16/f16 operand
+        off = round_up(off + static_cast<size_t>(p.rows) * dim * 2, 256);  // 16-bit operand rows
         p.off_real = off;
         off = round_up(off + static_cast<size_t>(p.rows), 256);
         p.off_active = off;
         off = round_up(off + static_cast<size_t>(p.rows), 256);
     }
+    if (int8) {
+        p.off_qscale = off;
+        off = round_up(off + static_cast<size_t>(p.rows) * sizeof(float), 256);
+    }
     if (p.n_chunks > 1) {
         p.off_partial = off;
         off = round_up(off + static_cast<size_t>(p.n_chunks) * nq * nd * sizeof(float), 256);
     }
-    (void)elem_bytes;
     p.ws_bytes = off;
     return p;
-}
-
-size_t fwd_smem_bytes(int32_t mt_max, int32_t k_atoms, int32_t stages) {
-    return 1024 + static_cast<size_t>(mt_max) * k_atoms * kAtomBytes +
-           static_cast<size_t>(stages) * k_atoms * kAtomBytes + sizeof(SmemCtl);
-}
-
-// Deepest document ring (2..8 stages) that fits; 0 if even two do not fit.
-int32_t fwd_stages(int32_t mt_max, int32_t k_atoms, int smem_optin) {
-    int32_t s = 8;
-    while (s >= 2 && fwd_smem_bytes(mt_max, k_atoms, s) > static_cast<size_t>(smem_optin)) --s;
-    return s >= 2 ? s : 0;
 }
 
 int64_t choose_doc_ranges(int64_t n_rb, int64_t total_d, int64_t nd, int num_sms) {
@@ -175,9 +205,15 @@ int64_t choose_doc_ranges(int64_t n_rb, int64_t total_d, int64_t nd, int num_sms
 
 // ---------------------------------------------------------------- small kernels
 
-__global__ void repack_q_kernel(const uint16_t* __restrict__ q, const int32_t* __restrict__ cu_q, int64_t lq_dense,
+// Query rows into the padded layout [Nq * lq_pad, dim] of 16-bit values, with
+// per-row flags (real token, active token) and, for INT8 queries, the row's
+// scale. INT8 values are converted to binary16 exactly.
+template <bool kInt8In>
+__global__ void repack_q_kernel(const void* __restrict__ q, const int32_t* __restrict__ cu_q, int64_t lq_dense,
                                 int64_t lq_pad, int64_t nq, int64_t dim, const uint8_t* __restrict__ q_mask,
-                                uint16_t* __restrict__ qp, uint8_t* __restrict__ real, uint8_t* __restrict__ active) {
+                                const float* __restrict__ q_scale_in, uint16_t* __restrict__ qp,
+                                uint8_t* __restrict__ real, uint8_t* __restrict__ active,
+                                float* __restrict__ q_scale_out) {
     const int64_t rows = nq * lq_pad;
     for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.y) + threadIdx.y; r < rows;
          r += static_cast<int64_t>(gridDim.x) * blockDim.y) {
@@ -186,10 +222,21 @@ __global__ void repack_q_kernel(const uint16_t* __restrict__ q, const int32_t* _
         const int64_t len = cu_q ? static_cast<int64_t>(cu_q[i + 1]) - cu_q[i] : lq_dense;
         const bool is_real = s < len;
         const int64_t src = start + s;
-        for (int64_t k = threadIdx.x; k < dim; k += blockDim.x) qp[r * dim + k] = is_real ? q[src * dim + k] : 0;
+        for (int64_t k = threadIdx.x; k < dim; k += blockDim.x) {
+            uint16_t v = 0;
+            if (is_real) {
+                if constexpr (kInt8In) {
+                    v = __half_as_ushort(__int2half_rn(static_cast<const int8_t*>(q)[src * dim + k]));
+                } else {
+                    v = static_cast<const uint16_t*>(q)[src * dim + k];
+                }
+            }
+            qp[r * dim + k] = v;
+        }
         if (threadIdx.x == 0) {
             real[r] = is_real ? 1 : 0;
             active[r] = (is_real && (q_mask == nullptr || q_mask[src] != 0)) ? 1 : 0;
+            if (q_scale_out) q_scale_out[r] = is_real ? q_scale_in[src] : 0.f;
         }
     }
 }
@@ -223,15 +270,36 @@ __global__ void fill_kernel(float* scores, int64_t ns, int32_t* argmax, int64_t 
     }
 }
 
+// INT8: the exact integer dot product at each argmax (0 where there is none).
+// One thread per (i, j, s), 4-byte dot-product steps.
+__global__ void win_dot_kernel(const int8_t* __restrict__ q, const int8_t* __restrict__ d,
+                               const int32_t* __restrict__ argmax, int64_t nq, int64_t lq, int64_t nd, int64_t ld,
+                               int64_t dim, int32_t* __restrict__ win) {
+    const int64_t n = nq * nd * lq;
+    for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < n;
+         x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t s = x % lq, ij = x / lq;
+        const int64_t i = ij / nd, j = ij - (ij / nd) * nd;
+        const int32_t a = argmax[x];
+        int32_t acc = 0;
+        if (a >= 0 && a < ld) {
+            const int* qr = reinterpret_cast<const int*>(q + (i * lq + s) * dim);
+            const int* dr = reinterpret_cast<const int*>(d + (j * ld + a) * dim);
+            for (int64_t k = 0; k < dim / 4; ++k) acc = __dp4a(qr[k], dr[k], acc);
+        }
+        win[x] = acc;
+    }
+}
+
 inline int grid_for(int64_t n, int per_block, int num_sms) {
     int64_t g = (n + per_block - 1) / per_block;
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g, static_cast<int64_t>(num_sms) * 8)));
 }
 
-template <bool kArg, bool kDMask>
+template <bool kArg, bool kInt8>
 maxsim_status launch_fwd_kernel(DeviceInfo* dev, int slot, const CUtensorMap& tq, const CUtensorMap& td,
                                 const FwdArgs& a, size_t smem, int grid, cudaStream_t st) {
-    auto kern = maxsim_fwd_kernel<kArg, kDMask>;
+    auto kern = maxsim_fwd_kernel<kArg, kInt8>;
     if (!dev->attrs_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev->smem_optin) != cudaSuccess)
             return MAXSIM_ERR_CUDA;
@@ -241,66 +309,92 @@ maxsim_status launch_fwd_kernel(DeviceInfo* dev, int slot, const CUtensorMap& tq
     return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
 }
 
-// Shared path of the three forward entry points once the operands are
-// f16/bf16 rows in device memory: Q as padded rows [rows, dim] (possibly in the
-// workspace), D as packed token rows [total_d, dim].
-maxsim_status run_fwd(DeviceInfo* dev, const FwdPlan& p, const void* q_rows, const uint8_t* q_real,
-                      const uint8_t* q_active, const void* d_rows, CUtensorMapDataType tdt, uint32_t ab_format,
-                      int64_t nq, int64_t lq_out, int64_t nd, int64_t ld, const int32_t* cu_d, int64_t total_d,
-                      int64_t dim, const uint8_t* d_mask, float* scores, int32_t* argmax, uint8_t* ws,
-                      cudaStream_t st) {
+// Shared path of the forward entry points once the query rows are 16-bit rows
+// in device memory: Q as padded rows [rows, dim] (possibly in the workspace),
+// D as packed token rows [total_d, dim] (16-bit, or INT8 in INT8 mode).
+struct FwdCall {
+    const void* q_rows;
+    const uint8_t* q_real;
+    const uint8_t* q_active;
+    const float* q_scale;
+    const void* d_rows;
+    const float* d_scale;
+    CUtensorMapDataType q_dt, d_dt;
+    uint32_t ab_format;   // 0 = f16, 1 = bf16
+    uint32_t nan_pair;
+    int64_t nq, lq_out, nd, ld, total_d, dim;
+    const int32_t* cu_d;
+    const uint8_t* d_mask;
+    float* scores;
+    int32_t* argmax;
+};
+
+maxsim_status run_fwd(DeviceInfo* dev, const FwdPlan& p, const FwdCall& c, uint8_t* ws, cudaStream_t st) {
+    if (!p.ok || p.stages < 1 || p.stages > kMaxStages || (p.int8 && (p.stages8 < 1 || p.stages8 > kMaxStages)) ||
+        p.smem > kSmemBudget)
+        return MAXSIM_ERR_UNSUPPORTED;
     CUtensorMap tq, td;
-    if (!encode_rows(&tq, q_rows, tdt, 2, static_cast<uint64_t>(dim), static_cast<uint64_t>(p.rows), 64, kBM))
+    if (!encode_rows(&tq, c.q_rows, c.q_dt, 2, static_cast<uint64_t>(c.dim), static_cast<uint64_t>(p.rows), 64, kBM))
         return MAXSIM_ERR_CUDA;
     // With no document tokens the D map is never read; point it at Q.
-    const void* dbase = total_d > 0 ? d_rows : q_rows;
-    const uint64_t drows = total_d > 0 ? static_cast<uint64_t>(total_d) : static_cast<uint64_t>(p.rows);
-    if (!encode_rows(&td, dbase, tdt, 2, static_cast<uint64_t>(dim), drows, 64, kBN)) return MAXSIM_ERR_CUDA;
+    const bool has_d = c.total_d > 0;
+    const int d_elem = p.int8 ? 1 : 2;
+    if (has_d) {
+        if (!encode_rows(&td, c.d_rows, c.d_dt, d_elem, static_cast<uint64_t>(c.dim), static_cast<uint64_t>(c.total_d),
+                         p.int8 ? 128 : 64, kBN))
+            return MAXSIM_ERR_CUDA;
+    } else if (!encode_rows(&td, c.q_rows, c.q_dt, 2, static_cast<uint64_t>(c.dim), static_cast<uint64_t>(p.rows), 64,
+                            kBN)) {
+        return MAXSIM_ERR_CUDA;
+    }
 
     FwdArgs a{};
-    a.nq = static_cast<int32_t>(nq);
+    a.nq = static_cast<int32_t>(c.nq);
     a.lq_pad = static_cast<int32_t>(p.lq_pad);
-    a.lq_out = static_cast<int32_t>(lq_out);
-    a.q_active = q_active;
-    a.q_real = q_real;
+    a.lq_out = static_cast<int32_t>(c.lq_out);
+    a.q_active = c.q_active;
+    a.q_real = c.q_real;
+    a.q_scale = c.q_scale;
     a.rb_rows = p.rb_rows;
     a.n_chunks = p.n_chunks;
     a.n_rb = static_cast<int32_t>(p.n_rb);
-    a.cu_d = cu_d;
-    a.nd = static_cast<int32_t>(nd);
-    a.ld = static_cast<int32_t>(ld);
-    a.total_d = static_cast<int32_t>(total_d);
-    a.d_mask = d_mask;
-    const int64_t n_dr = choose_doc_ranges(p.n_rb, total_d, nd, dev->num_sms);
+    a.cu_d = c.cu_d;
+    a.nd = static_cast<int32_t>(c.nd);
+    a.ld = static_cast<int32_t>(c.ld);
+    a.total_d = static_cast<int32_t>(c.total_d);
+    a.d_mask = c.d_mask;
+    a.d_scale = c.d_scale;
+    const int64_t n_dr = choose_doc_ranges(p.n_rb, c.total_d, c.nd, dev->num_sms);
     a.n_dr = static_cast<int32_t>(n_dr);
     a.n_units = static_cast<int32_t>(n_dr * p.n_rb);
-    a.scores = scores;
+    a.scores = c.scores;
     a.partial = p.n_chunks > 1 ? reinterpret_cast<float*>(ws + p.off_partial) : nullptr;
-    a.argmax = argmax;
+    a.argmax = c.argmax;
     a.k_steps = p.k_steps;
     a.k_atoms = p.k_atoms;
-    a.stages = fwd_stages(p.mt_max, p.k_atoms, dev->smem_optin);
-    if (a.stages == 0) return MAXSIM_ERR_UNSUPPORTED;
+    a.k8_atoms = p.k8_atoms;
+    a.dim = static_cast<int32_t>(c.dim);
+    a.stages = p.stages;
+    a.stages8 = p.stages8;
     a.q_slots = p.mt_max;
-    a.idesc = idesc_f16_f32(ab_format, kBM, kBN);
+    a.idesc = idesc_f16_f32(c.ab_format, kBM, 0);
+    a.nan_pair = c.nan_pair;
     a.status = dev->status;
     a.timeout_ns = kTimeoutNs;
-    // One CTA per SM: the request below always exceeds half of an SM's shared memory.
-    size_t smem = std::max<size_t>(fwd_smem_bytes(p.mt_max, p.k_atoms, a.stages),
-                                   static_cast<size_t>(dev->smem_optin / 2 + 1024));
-    smem = std::min<size_t>(smem, static_cast<size_t>(dev->smem_optin));
+    // One CTA per SM: the request always exceeds half of an SM's shared memory.
+    const size_t smem = std::max<size_t>(p.smem, kSmemBudget / 2 + 1024);
     const int grid = static_cast<int>(std::min<int64_t>(a.n_units, dev->num_sms));
 
     maxsim_status rc;
-    const bool arg = argmax != nullptr, dm = d_mask != nullptr;
-    if (arg && dm) rc = launch_fwd_kernel<true, true>(dev, 0, tq, td, a, smem, grid, st);
-    else if (arg) rc = launch_fwd_kernel<true, false>(dev, 1, tq, td, a, smem, grid, st);
-    else if (dm) rc = launch_fwd_kernel<false, true>(dev, 2, tq, td, a, smem, grid, st);
-    else rc = launch_fwd_kernel<false, false>(dev, 3, tq, td, a, smem, grid, st);
+    const bool arg = c.argmax != nullptr;
+    if (p.int8) rc = arg ? launch_fwd_kernel<true, true>(dev, 0, tq, td, a, smem, grid, st)
+                         : launch_fwd_kernel<false, true>(dev, 1, tq, td, a, smem, grid, st);
+    else rc = arg ? launch_fwd_kernel<true, false>(dev, 2, tq, td, a, smem, grid, st)
+                  : launch_fwd_kernel<false, false>(dev, 3, tq, td, a, smem, grid, st);
     if (rc != MAXSIM_OK) return rc;
     if (p.n_chunks > 1) {
-        const int64_t n = nq * nd;
-        sum_chunks_kernel<<<grid_for(n, 256, dev->num_sms), 256, 0, st>>>(a.partial, p.n_chunks, n, scores);
+        const int64_t n = c.nq * c.nd;
+        sum_chunks_kernel<<<grid_for(n, 256, dev->num_sms), 256, 0, st>>>(a.partial, p.n_chunks, n, c.scores);
         if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
     }
     return MAXSIM_OK;
@@ -313,6 +407,12 @@ maxsim_status check_dim(int64_t dim, int64_t multiple) {
 }
 
 constexpr int64_t kI32Max = 2147483647;
+constexpr uint32_t kNaNPairF16 = 0x7E007E00u;
+constexpr uint32_t kNaNPairBF16 = 0x7FC07FC0u;
+
+inline CUtensorMapDataType half_map(maxsim_dtype dt) {
+    return dt == MAXSIM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
 
 }  // namespace
 }  // namespace maxsim
@@ -321,7 +421,7 @@ using namespace maxsim;
 
 extern "C" {
 
-int maxsim_version(void) { return 100; }
+int maxsim_version(void) { return 200; }
 
 const char* maxsim_status_string(maxsim_status s) {
     switch (s) {
@@ -353,11 +453,11 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
     if (Nq < 0 || Lq < 0 || Nd < 0 || Ld < 0 || dim <= 0) return static_cast<size_t>(-1);
     switch (op) {
     case MAXSIM_OP_FWD:
-        return plan_fwd(Nq, Lq, Nd, dim, 2, false, false).ws_bytes;
+        return plan_fwd(Nq, Lq, Nd, dim, false, false).ws_bytes;
     case MAXSIM_OP_FWD_VARLEN:
-        return plan_fwd(Nq, Lq, Nd, dim, 2, true, false).ws_bytes;
+        return plan_fwd(Nq, Lq, Nd, dim, true, false).ws_bytes;
     case MAXSIM_OP_FWD_INT8:
-        return plan_fwd(Nq, Lq, Nd, dim, 1, false, true).ws_bytes;
+        return plan_fwd(Nq, Lq, Nd, dim, false, true).ws_bytes;
     case MAXSIM_OP_BWD: {
         size_t off = 0;
         off = round_up(off + static_cast<size_t>(Nd) * 4, 256);          // doc_cnt
@@ -382,7 +482,8 @@ maxsim_status maxsim_fwd(const void* Q, const void* D, maxsim_dtype dtype, int64
     if ((Lq > 0 && (!Q || !aligned16(Q))) || (Ld > 0 && (!D || !aligned16(D)))) return MAXSIM_ERR_INVALID_ARG;
     if (Nd * Ld > kI32Max || Nq * pad_lq(Lq) > kI32Max || Nq * Nd > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
     if (argmax && Nq * Nd * Lq > (int64_t(1) << 40)) return MAXSIM_ERR_UNSUPPORTED;
-    const FwdPlan p = plan_fwd(Nq, Lq, Nd, dim, 2, false, false);
+    const FwdPlan p = plan_fwd(Nq, Lq, Nd, dim, false, false);
+    if (!p.ok) return MAXSIM_ERR_UNSUPPORTED;
     if (workspace_bytes < p.ws_bytes || (p.ws_bytes > 0 && !workspace)) return MAXSIM_ERR_WORKSPACE;
     DeviceInfo* dev = nullptr;
     if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
@@ -392,24 +493,33 @@ maxsim_status maxsim_fwd(const void* Q, const void* D, maxsim_dtype dtype, int64
         return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const void* q_rows = Q;
-    const uint8_t* q_real = nullptr;
-    const uint8_t* q_active = q_mask;
+    FwdCall c{};
+    c.q_rows = Q;
+    c.q_active = q_mask;
     if (p.repack) {
         uint16_t* qp = reinterpret_cast<uint16_t*>(ws + p.off_q);
-        uint8_t* real = ws + p.off_real;
-        uint8_t* act = ws + p.off_active;
         dim3 blk(32, 8);
-        repack_q_kernel<<<grid_for(p.rows, 8, dev->num_sms), blk, 0, st>>>(
-            static_cast<const uint16_t*>(Q), nullptr, Lq, p.lq_pad, Nq, dim, q_mask, qp, real, act);
+        repack_q_kernel<false><<<grid_for(p.rows, 8, dev->num_sms), blk, 0, st>>>(
+            Q, nullptr, Lq, p.lq_pad, Nq, dim, q_mask, nullptr, qp, ws + p.off_real, ws + p.off_active, nullptr);
         if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
-        q_rows = qp;
-        q_real = real;
-        q_active = act;
+        c.q_rows = qp;
+        c.q_real = ws + p.off_real;
+        c.q_active = ws + p.off_active;
     }
-    const CUtensorMapDataType tdt = dtype == MAXSIM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    return run_fwd(dev, p, q_rows, q_real, q_active, D, tdt, dtype == MAXSIM_BF16 ? 1u : 0u, Nq, Lq, Nd, Ld,
-                   nullptr, Nd * Ld, dim, d_mask, scores, argmax, ws, st);
+    c.d_rows = D;
+    c.q_dt = c.d_dt = half_map(dtype);
+    c.ab_format = dtype == MAXSIM_BF16 ? 1u : 0u;
+    c.nan_pair = dtype == MAXSIM_BF16 ? kNaNPairBF16 : kNaNPairF16;
+    c.nq = Nq;
+    c.lq_out = Lq;
+    c.nd = Nd;
+    c.ld = Ld;
+    c.total_d = Nd * Ld;
+    c.dim = dim;
+    c.d_mask = d_mask;
+    c.scores = scores;
+    c.argmax = argmax;
+    return run_fwd(dev, p, c, ws, st);
 }
 
 maxsim_status maxsim_fwd_varlen(const void* Q, const int32_t* cu_seqlens_q, int64_t max_lq, const void* D,
@@ -426,7 +536,8 @@ maxsim_status maxsim_fwd_varlen(const void* Q, const int32_t* cu_seqlens_q, int6
     if ((max_lq > 0 && (!Q || !aligned16(Q))) || (total_d > 0 && (!D || !aligned16(D))))
         return MAXSIM_ERR_INVALID_ARG;
     if (total_d > kI32Max || Nq * pad_lq(max_lq) > kI32Max || Nq * Nd > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
-    const FwdPlan p = plan_fwd(Nq, max_lq, Nd, dim, 2, true, false);
+    const FwdPlan p = plan_fwd(Nq, max_lq, Nd, dim, true, false);
+    if (!p.ok) return MAXSIM_ERR_UNSUPPORTED;
     if (workspace_bytes < p.ws_bytes || (p.ws_bytes > 0 && !workspace)) return MAXSIM_ERR_WORKSPACE;
     DeviceInfo* dev = nullptr;
     if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
@@ -441,16 +552,29 @@ maxsim_status maxsim_fwd_varlen(const void* Q, const int32_t* cu_seqlens_q, int6
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint16_t* qp = reinterpret_cast<uint16_t*>(ws + p.off_q);
-    uint8_t* real = ws + p.off_real;
-    uint8_t* act = ws + p.off_active;
     dim3 blk(32, 8);
-    repack_q_kernel<<<grid_for(p.rows, 8, dev->num_sms), blk, 0, st>>>(static_cast<const uint16_t*>(Q), cu_seqlens_q,
-                                                                       max_lq, p.lq_pad, Nq, dim, q_mask, qp, real,
-                                                                       act);
+    repack_q_kernel<false><<<grid_for(p.rows, 8, dev->num_sms), blk, 0, st>>>(
+        Q, cu_seqlens_q, max_lq, p.lq_pad, Nq, dim, q_mask, nullptr, qp, ws + p.off_real, ws + p.off_active, nullptr);
     if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
-    const CUtensorMapDataType tdt = dtype == MAXSIM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    return run_fwd(dev, p, qp, real, act, D, tdt, dtype == MAXSIM_BF16 ? 1u : 0u, Nq, max_lq, Nd, 0, cu_seqlens_d,
-                   total_d, dim, d_mask, scores, argmax, ws, st);
+    FwdCall c{};
+    c.q_rows = qp;
+    c.q_real = ws + p.off_real;
+    c.q_active = ws + p.off_active;
+    c.d_rows = D;
+    c.q_dt = c.d_dt = half_map(dtype);
+    c.ab_format = dtype == MAXSIM_BF16 ? 1u : 0u;
+    c.nan_pair = dtype == MAXSIM_BF16 ? kNaNPairBF16 : kNaNPairF16;
+    c.nq = Nq;
+    c.lq_out = max_lq;
+    c.nd = Nd;
+    c.ld = 0;
+    c.total_d = total_d;
+    c.dim = dim;
+    c.cu_d = cu_seqlens_d;
+    c.d_mask = d_mask;
+    c.scores = scores;
+    c.argmax = argmax;
+    return run_fwd(dev, p, c, ws, st);
 }
 
 maxsim_status maxsim_bwd(const void* Q, const void* D, maxsim_dtype dtype, int64_t Nq, int64_t Lq, int64_t Nd,
@@ -553,14 +677,62 @@ maxsim_status maxsim_fwd_int8(const int8_t* Q, const float* q_scale, const int8_
                               int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim, const uint8_t* q_mask,
                               const uint8_t* d_mask, float* scores, int32_t* argmax, int32_t* win_dot,
                               void* workspace, size_t workspace_bytes, void* stream) {
-    (void)Q; (void)q_scale; (void)D; (void)d_scale; (void)Nq; (void)Lq; (void)Nd; (void)Ld; (void)dim;
-    (void)q_mask; (void)d_mask; (void)scores; (void)argmax; (void)win_dot; (void)workspace;
-    (void)workspace_bytes; (void)stream;
-    return MAXSIM_ERR_UNSUPPORTED;
+    if (Nq < 0 || Lq < 0 || Nd < 0 || Ld < 0) return MAXSIM_ERR_INVALID_ARG;
+    maxsim_status rc = check_dim(dim, 32);
+    if (rc != MAXSIM_OK) return rc;
+    if (Nq * Nd == 0) return MAXSIM_OK;
+    if (!scores || (win_dot && !argmax)) return MAXSIM_ERR_INVALID_ARG;
+    if (Lq > 0 && (!Q || !aligned16(Q) || !q_scale || !aligned(q_scale, 4))) return MAXSIM_ERR_INVALID_ARG;
+    if (Ld > 0 && (!D || !aligned16(D) || !d_scale || !aligned(d_scale, 4))) return MAXSIM_ERR_INVALID_ARG;
+    if (Nd * Ld > kI32Max || Nq * pad_lq(Lq) > kI32Max || Nq * Nd > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
+    const FwdPlan p = plan_fwd(Nq, Lq, Nd, dim, false, true);
+    if (!p.ok) return MAXSIM_ERR_UNSUPPORTED;
+    if (workspace_bytes < p.ws_bytes || (p.ws_bytes > 0 && !workspace)) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Lq == 0) {
+        fill_kernel<<<grid_for(Nq * Nd, 256, dev->num_sms), 256, 0, st>>>(scores, Nq * Nd, nullptr, 0);
+        return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint16_t* qp = reinterpret_cast<uint16_t*>(ws + p.off_q);
+    float* qs = reinterpret_cast<float*>(ws + p.off_qscale);
+    dim3 blk(32, 8);
+    repack_q_kernel<true><<<grid_for(p.rows, 8, dev->num_sms), blk, 0, st>>>(
+        Q, nullptr, Lq, p.lq_pad, Nq, dim, q_mask, q_scale, qp, ws + p.off_real, ws + p.off_active, qs);
+    if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+    FwdCall c{};
+    c.q_rows = qp;
+    c.q_real = ws + p.off_real;
+    c.q_active = ws + p.off_active;
+    c.q_scale = qs;
+    c.d_rows = D;
+    c.d_scale = d_scale;
+    c.q_dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    c.d_dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    c.ab_format = 0u;
+    c.nan_pair = kNaNPairF16;
+    c.nq = Nq;
+    c.lq_out = Lq;
+    c.nd = Nd;
+    c.ld = Ld;
+    c.total_d = Nd * Ld;
+    c.dim = dim;
+    c.d_mask = d_mask;
+    c.scores = scores;
+    c.argmax = argmax;
+    rc = run_fwd(dev, p, c, ws, st);
+    if (rc != MAXSIM_OK) return rc;
+    if (win_dot) {
+        const int64_t n = Nq * Nd * Lq;
+        win_dot_kernel<<<grid_for(n, 256, dev->num_sms), 256, 0, st>>>(Q, D, argmax, Nq, Lq, Nd, Ld, dim, win_dot);
+        if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+    }
+    return MAXSIM_OK;
 }
 
 }  // extern "C"
-
 // ---------------------------------------------------------------- allocation-free varlen forward
 //
 // Scratch for callers that cannot allocate device memory: a fixed array in

@@ -163,6 +163,40 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         : "r"(taddr));
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[32]) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// ---------------------------------------------------------------- INT8 -> f16
+
+// Eight signed bytes (w0: elements 0-3, w1: elements 4-7, little-endian) to
+// eight binary16 values, exactly. Each byte b is biased to u = b + 128, placed
+// as the low mantissa byte of the binary16 1024.0 (exponent 10, unit ulp), so
+// the half is 1024 + u, and 1152 = 1024 + 128 is subtracted: the result is b.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t biased, uint32_t selector) {
+    uint32_t h, d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(h) : "r"(biased), "r"(0x64646464u), "r"(selector));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(0x64806480u));
+    return d;
+}
+
+__device__ __forceinline__ uint4 i8x8_to_f16x8(uint32_t w0, uint32_t w1) {
+    const uint32_t u0 = w0 ^ 0x80808080u, u1 = w1 ^ 0x80808080u;
+    uint4 r;
+    r.x = i8x2_to_f16x2(u0, 0x4140u);  // bytes 0, 1
+    r.y = i8x2_to_f16x2(u0, 0x4342u);  // bytes 2, 3
+    r.z = i8x2_to_f16x2(u1, 0x4140u);
+    r.w = i8x2_to_f16x2(u1, 0x4342u);
+    return r;
+}
+
 // ---------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for a K-major operand stored with the

@@ -56,6 +56,26 @@ def test_varlen_packed_queries():
     assert np.array_equal(a.cpu().numpy(), ref_a)
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_varlen_every_tail_length_exact(dtype):
+    # documents of 1..140 tokens: every MMA width from 16 to 128 and every
+    # padding amount inside the last 16-column group; integer inputs are exact
+    dim, Nq, Lq = 32, 2, 32
+    lens = np.arange(1, 141)
+    rng = np.random.default_rng(3)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    Q = datagen.float_to_bits(integer_rows(rng, Nq * Lq, dim), dtype).reshape(Nq, Lq, dim)
+    D = datagen.float_to_bits(integer_rows(rng, int(cu[-1]), dim), dtype)
+    dm = (rng.random(int(cu[-1])) > 0.15).astype(np.uint8)
+    for d_mask in (None, dm):
+        s, a = ops.maxsim_fwd_varlen(dev_bits(Q, dtype), None, Lq, dev_bits(D, dtype), dev(cu.astype(np.int32)),
+                                     d_mask=dev(d_mask), want_argmax=True)
+        assert ops.device_status() == 0
+        ref_s, ref_a, _ = oracle.fwd_packed(Q.reshape(-1, dim), np.arange(Nq + 1) * Lq, D, cu, dtype, d_mask=d_mask)
+        assert np.array_equal(s.cpu().numpy().astype(np.float64), ref_s)
+        assert np.array_equal(a.cpu().numpy(), ref_a)
+
+
 def test_varlen_equals_dense_with_trailing_mask():
     # "same as the padded path": a trailing d_mask equals shorter packed documents
     dtype, Nq, Lq, Nd, Ld, dim = "bf16", 2, 32, 5, 200, 128
