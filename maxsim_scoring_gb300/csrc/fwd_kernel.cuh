@@ -51,7 +51,9 @@ constexpr int kBN = 128;          // document tokens per tile (largest MMA N)
 constexpr int kBM = 128;          // query rows per M-tile (MMA M)
 constexpr int kMaxMT = 4;         // M-tiles per row block
 constexpr int kNAcc = 4;          // TMEM accumulator buffers (4 x 128 columns)
-constexpr int kThreads = 256;     // warp 0 TMA, warp 1 MMA, warps 2-3 prep, warps 4-7 epilogue
+constexpr int kEpiGroups = 2;     // epilogue warpgroups; group g owns the M-tiles k with k % 2 == g
+constexpr int kEpiWarps = 4 * kEpiGroups;
+constexpr int kThreads = 128 + 32 * kEpiWarps;  // warp 0 TMA, warp 1 MMA, warps 2-3 prep, then the epilogue
 constexpr int kEpiWarp0 = 4;
 constexpr int kPrepThreads = 64;
 constexpr int kAtomBytes = 128 * 128;  // one 128-row x 128-byte swizzled block
@@ -213,24 +215,25 @@ struct alignas(16) SmemCtl {
     uint64_t d8_full[kMaxStages], d8_empty[kMaxStages];
     uint64_t acc_full[kNAcc], acc_empty[kNAcc];
     uint64_t mma_done;
-    uint64_t epi_bar;  // rendezvous of the four epilogue warps
+    uint64_t epi_bar;  // rendezvous of the epilogue warps
     uint32_t tmem_base;
     volatile int32_t abort;
     float wslot[kMaxMT * 4];   // per-warp partial sums of the document being closed
 };
 // INT8 mode only: after the control block, a per-warp copy of the tile's
-// document scales, float[4][kBN].
-constexpr int kDScaleBytes = 4 * kBN * 4;
+// document scales, float[kEpiWarps][kBN].
+constexpr int kDScaleBytes = kEpiWarps * kBN * 4;
 
 __device__ __forceinline__ void record_status(const FwdArgs& a, int code) {
     if (a.status) atomicCAS(a.status, 0, code);
 }
 
 // Bounded wait: gives up after timeout_ns (records the status and raises the
-// CTA abort flag) or when another role has already aborted.
-__device__ __forceinline__ bool wait_bar(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = global_timer_ns();
+// CTA abort flag) or when another role has already aborted. The slow path is
+// kept out of line so that every role's hot loop stays small in the
+// instruction cache.
+__device__ __noinline__ bool wait_bar_slow(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
@@ -244,7 +247,12 @@ __device__ __forceinline__ bool wait_bar(const FwdArgs& a, SmemCtl* ctl, uint32_
     }
 }
 
-// Bounded rendezvous of the four epilogue warps (an mbarrier phase per use),
+__device__ __forceinline__ bool wait_bar(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(a, ctl, bar, parity);
+}
+
+// Bounded rendezvous of the epilogue warps (an mbarrier phase per use),
 // so that a warp that gave up on a wait can never strand the others.
 __device__ __forceinline__ bool epi_sync(const FwdArgs& a, SmemCtl* ctl, uint32_t& phase) {
     __syncwarp();
@@ -303,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sD = smem + a.q_slots * q_tile_bytes;
     uint8_t* sD8 = sD + a.stages * d_stage_bytes;
     SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sD8 + (kInt8 ? a.stages8 * d8_stage_bytes : 0));
-    float* dscale = reinterpret_cast<float*>(ctl + 1);  // [4][kBN], INT8 mode
+    float* dscale = reinterpret_cast<float*>(ctl + 1);  // [kEpiWarps][kBN], INT8 mode
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -332,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctl->acc_empty[b]), 4);
         }
         mbar_init(smem_u32(&ctl->mma_done), 1);
-        mbar_init(smem_u32(&ctl->epi_bar), 4);
+        mbar_init(smem_u32(&ctl->epi_bar), kEpiWarps);
         ctl->abort = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_q);
@@ -406,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int32_t stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0, q_phase = 0;
+            const uint64_t q_desc0 = sdesc_k_sw128(smem_u32(sQ));
             bool ok = true;
             for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
                 const Unit w = make_unit(a, u);
@@ -417,16 +426,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(a, ctl, smem_u32(&ctl->d_ready[stage]), phase)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t idesc = a.idesc | (static_cast<uint32_t>(mma_n(tw.ntok()) >> 3) << 17);
-                    const uint32_t d_base = smem_u32(sD + stage * d_stage_bytes);
+                    const uint64_t b_desc0 = sdesc_k_sw128(smem_u32(sD + stage * d_stage_bytes));
                     for (int32_t k = 0; k < w.rb.mt; ++k) {
                         if (!wait_bar(a, ctl, smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t q_base = smem_u32(sQ + k * q_tile_bytes);
+                        const uint64_t a_desc0 = q_desc0 + static_cast<uint64_t>((k * q_tile_bytes) >> 4);
                         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-                        for (int32_t ks = 0; ks < a.k_steps; ++ks) {
-                            const uint32_t off = static_cast<uint32_t>((ks >> 2) * kAtomBytes + (ks & 3) * 32);
-                            mma_f16_ss(d_tmem, sdesc_k_sw128(q_base + off), sdesc_k_sw128(d_base + off), idesc,
-                                       ks > 0 ? 1u : 0u);
+                        // whole 64-element K blocks four MMAs at a time, then the
+                        // remaining 16-element steps one by one
+                        int32_t ks = 0;
+                        if (a.k_steps == 8) {  // dim 128: fully unrolled
+                            const uint32_t alo = static_cast<uint32_t>(a_desc0), ahi = static_cast<uint32_t>(a_desc0 >> 32);
+                            const uint32_t blo = static_cast<uint32_t>(b_desc0), bhi = static_cast<uint32_t>(b_desc0 >> 32);
+#pragma unroll
+                            for (int s8 = 0; s8 < 8; ++s8) {
+                                const uint32_t o = static_cast<uint32_t>(((s8 >> 2) * kAtomBytes + (s8 & 3) * 32) >> 4);
+                                mma_f16_ss_words(d_tmem, alo + o, ahi, blo + o, bhi, idesc, s8 > 0 ? 1u : 0u);
+                            }
+                            ks = 8;
+                        }
+                        for (; ks + 4 <= a.k_steps; ks += 4) {
+                            const uint64_t o = static_cast<uint64_t>(((ks >> 2) * kAtomBytes) >> 4);
+                            mma_f16_ss_k64(d_tmem, a_desc0 + o, b_desc0 + o, idesc, ks > 0 ? 1u : 0u);
+                        }
+                        for (; ks < a.k_steps; ++ks) {
+                            const uint64_t o = static_cast<uint64_t>(((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4);
+                            mma_f16_ss(d_tmem, a_desc0 + o, b_desc0 + o, idesc, ks > 0 ? 1u : 0u);
                         }
                         mma_commit(smem_u32(&ctl->acc_full[acc]));
                         if (++acc == kNAcc) { acc = 0; acc_phase ^= 1u; }
@@ -512,33 +537,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // Warpgroup g owns the M-tiles k = g, g + kEpiGroups, ...; each of its
+        // threads owns one query row of each of those M-tiles.
+        constexpr int kKPer = kMaxMT / kEpiGroups;
         const float kNegInf = __int_as_float(0xff800000u);
         const float kNaN = __int_as_float(0x7fffffffu);
-        const int e = warp - kEpiWarp0;               // TMEM lane quadrant
-        const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..127
-        int32_t acc = 0;
-        uint32_t acc_phase = 0, epi_phase = 0;
+        const int ew = warp - kEpiWarp0;              // epilogue warp 0..kEpiWarps-1
+        const int g = ew >> 2;                        // warpgroup
+        const int e = ew & 3;                         // TMEM lane quadrant
+        const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..32*kEpiWarps-1
+        int64_t buf = 0;                              // global index of the tile's first buffer
+        uint32_t epi_phase = 0;
         bool ok = true;
         for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
             const Unit w = make_unit(a, u);
             const RowBlock& rb = w.rb;
             const bool chunked = a.n_chunks > 1;
-            // per-row facts for each M-tile this thread reads
-            int32_t row_i[kMaxMT], row_s[kMaxMT];
-            bool in_rb[kMaxMT], real[kMaxMT], active[kMaxMT];
-            float qsc[kMaxMT];
+            int32_t row_i[kKPer], row_s[kKPer];
+            bool in_rb[kKPer], real[kKPer], active[kKPer];
+            float qsc[kKPer];
 #pragma unroll
-            for (int k = 0; k < kMaxMT; ++k) {
+            for (int q = 0; q < kKPer; ++q) {
+                const int k = g + kEpiGroups * q;
                 const int32_t r = rb.row0 + k * kBM + e * 32 + lane;
-                in_rb[k] = k < rb.mt && r < rb.row_end;
-                row_i[k] = r / a.lq_pad;
-                row_s[k] = r - row_i[k] * a.lq_pad;
-                real[k] = in_rb[k] && (a.q_real == nullptr || a.q_real[r] != 0);
-                active[k] = real[k] && (a.q_active == nullptr || a.q_active[r] != 0);
-                qsc[k] = (kInt8 && in_rb[k]) ? a.q_scale[r] : 1.f;
+                in_rb[q] = k < rb.mt && r < rb.row_end;
+                row_i[q] = r / a.lq_pad;
+                row_s[q] = r - row_i[q] * a.lq_pad;
+                real[q] = in_rb[q] && (a.q_real == nullptr || a.q_real[r] != 0);
+                active[q] = real[q] && (a.q_active == nullptr || a.q_active[r] != 0);
+                qsc[q] = (kInt8 && in_rb[q]) ? a.q_scale[r] : 1.f;
             }
             // empty documents: score 0 and argmax -1, written up front
-            for (int32_t j = w.j0 + et; j < w.j1; j += 128) {
+            for (int32_t j = w.j0 + et; j < w.j1; j += 32 * kEpiWarps) {
                 if (doc_start(a, j + 1) > doc_start(a, j)) continue;
                 for (int32_t q = 0; q < rb.nqb; ++q) {
                     const int32_t i = rb.q0 + q;
@@ -552,89 +582,102 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            float m[kMaxMT];
-            int32_t am[kMaxMT];
+            float m[kKPer];
+            int32_t am[kKPer];
 #pragma unroll
-            for (int k = 0; k < kMaxMT; ++k) { m[k] = kNegInf; am[k] = -1; }
+            for (int q = 0; q < kKPer; ++q) { m[q] = kNegInf; am[q] = -1; }
 
             TileWalk tw;
             for (tw.begin(a, w); tw.valid() && ok; tw.advance(a)) {
                 const int32_t n = tw.ntok(), N = mma_n(n);
                 const int32_t nfull = N >> 5;
                 const bool half = (N & 31) != 0;
+                const int32_t nchunks = nfull + (half ? 1 : 0);
                 const bool closes = tw.last_of_doc();
                 if constexpr (kInt8) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int32_t t = c * 32 + lane;
-                        dscale[e * kBN + t] = t < n ? __ldg(a.d_scale + tw.row() + t) : 0.f;
+                        dscale[ew * kBN + t] = t < n ? __ldg(a.d_scale + tw.row() + t) : 0.f;
                     }
                     __syncwarp();
                 }
 #pragma unroll
-                for (int k = 0; k < kMaxMT; ++k) {
+                for (int q = 0; q < kKPer; ++q) {
+                    const int k = g + kEpiGroups * q;
                     if (k >= rb.mt) break;
-                    if (!wait_bar(a, ctl, smem_u32(&ctl->acc_full[acc]), acc_phase)) { ok = false; break; }
+                    const int64_t idx = buf + k;
+                    const int32_t slot = static_cast<int32_t>(idx % kNAcc);
+                    const uint32_t ph = static_cast<uint32_t>((idx / kNAcc) & 1);
+                    if (!wait_bar(a, ctl, smem_u32(&ctl->acc_full[slot]), ph)) { ok = false; break; }
                     tc_fence_after();
-                    float v[4][32];
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(e * 32) << 16) +
-                                           static_cast<uint32_t>(acc * kBN);
+                                           static_cast<uint32_t>(slot * kBN);
+                    // columns in two halves of up to 64 (registers are the limit)
+                    auto fold = [&](float (&vc)[32], int c) {
+                        if constexpr (kInt8) {
+                            const float4* sc = reinterpret_cast<const float4*>(dscale + ew * kBN + c * 32);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c < nfull) {
-                            tmem_ld32(taddr + c * 32, v[c]);
-                        } else if (c == nfull && half) {
-                            tmem_ld16(taddr + c * 32, v[c]);
-#pragma unroll
-                            for (int x = 16; x < 32; ++x) v[c][x] = kNaN;
-                        }
-                    }
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[acc]));
-                    if (++acc == kNAcc) { acc = 0; acc_phase ^= 1u; }
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c < nfull + (half ? 1 : 0)) {
-                            if constexpr (kInt8) {
-                                const float4* sc = reinterpret_cast<const float4*>(dscale + e * kBN + c * 32);
-#pragma unroll
-                                for (int x = 0; x < 8; ++x) {
-                                    const float4 s4 = sc[x];
-                                    v[c][4 * x + 0] *= s4.x;
-                                    v[c][4 * x + 1] *= s4.y;
-                                    v[c][4 * x + 2] *= s4.z;
-                                    v[c][4 * x + 3] *= s4.w;
-                                }
+                            for (int x = 0; x < 8; ++x) {
+                                const float4 s4 = sc[x];
+                                vc[4 * x + 0] *= s4.x;
+                                vc[4 * x + 1] *= s4.y;
+                                vc[4 * x + 2] *= s4.z;
+                                vc[4 * x + 3] *= s4.w;
                             }
-                            fold_chunk<kArg>(v[c], tw.t0 + c * 32, m[k], am[k]);
                         }
+                        fold_chunk<kArg>(vc, tw.t0 + c * 32, m[q], am[q]);
+                    };
+                    float v[2][32];
+                    const int nh = nchunks > 2 ? 2 : 1;
+#pragma unroll 1
+                    for (int h = 0; h < nh; ++h) {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const int cc = 2 * h + c;
+                            if (cc < nfull) {
+                                tmem_ld32(taddr + cc * 32, v[c]);
+                            } else if (cc == nfull && half) {
+                                tmem_ld16(taddr + cc * 32, v[c]);
+#pragma unroll
+                                for (int x = 16; x < 32; ++x) v[c][x] = kNaN;
+                            }
+                        }
+                        tmem_wait_ld();
+                        if (h == nh - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[slot]));
+                        }
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            if (2 * h + c < nchunks) fold(v[c], 2 * h + c);
                     }
                     if (closes) {
-                        const bool has = m[k] > kNegInf;
-                        if (kArg && in_rb[k] && row_s[k] < a.lq_out)
-                            a.argmax[(static_cast<int64_t>(row_i[k]) * a.nd + tw.j) * a.lq_out + row_s[k]] =
-                                (real[k] && has) ? am[k] : -1;
-                        float val = (active[k] && has) ? m[k] * qsc[k] : 0.f;
+                        const bool has = m[q] > kNegInf;
+                        if (kArg && in_rb[q] && row_s[q] < a.lq_out)
+                            a.argmax[(static_cast<int64_t>(row_i[q]) * a.nd + tw.j) * a.lq_out + row_s[q]] =
+                                (real[q] && has) ? am[q] : -1;
+                        float val = (active[q] && has) ? m[q] * qsc[q] : 0.f;
                         if (a.lq_pad >= 32) {
 #pragma unroll
                             for (int o = 16; o > 0; o >>= 1) val += __shfl_xor_sync(0xFFFFFFFFu, val, o);
                             if (a.lq_pad == 32 && !chunked) {
-                                if (lane == 0 && in_rb[k]) a.scores[static_cast<int64_t>(row_i[k]) * a.nd + tw.j] = val;
+                                if (lane == 0 && in_rb[q]) a.scores[static_cast<int64_t>(row_i[q]) * a.nd + tw.j] = val;
                             } else if (lane == 0) {
                                 ctl->wslot[k * 4 + e] = val;
                             }
                         } else {
                             for (int o = a.lq_pad >> 1; o > 0; o >>= 1) val += __shfl_xor_sync(0xFFFFFFFFu, val, o);
-                            if (in_rb[k] && (lane & (a.lq_pad - 1)) == 0)
-                                a.scores[static_cast<int64_t>(row_i[k]) * a.nd + tw.j] = val;
+                            if (in_rb[q] && (lane & (a.lq_pad - 1)) == 0)
+                                a.scores[static_cast<int64_t>(row_i[q]) * a.nd + tw.j] = val;
                         }
-                        m[k] = kNegInf;
-                        am[k] = -1;
+                        m[q] = kNegInf;
+                        am[q] = -1;
                     }
                 }
                 if (!ok) break;
+                buf += rb.mt;
                 if (closes && (a.lq_pad > 32 || (a.lq_pad == 32 && chunked))) {
                     if (!epi_sync(a, ctl, epi_phase)) { ok = false; break; }
                     if (et < rb.nqb) {

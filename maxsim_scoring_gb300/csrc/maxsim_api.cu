@@ -10,7 +10,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/maxsim.h"
+#include "maxsim.h"
 #include "bwd_kernels.cuh"
 #include "fwd_kernel.cuh"
 
