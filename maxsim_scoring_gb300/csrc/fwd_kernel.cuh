@@ -24,6 +24,13 @@
 //  * For every (tile, M-tile) one MMA chain S = Q_blk * D_tile^T (K = dim)
 //    accumulates in one of four 128-column TMEM buffers; the epilogue warps
 //    read it with tcgen05.ld while the tensor core fills the next buffer.
+//  * Pair mode (a cluster of two CTAs on two SMs): the MMA is
+//    tcgen05.mma.cta_group::2 with M = 256, issued by the even CTA. Each CTA
+//    keeps its own row block of query rows (the A half of the MMA) and loads
+//    half of every document tile (the B half): one instruction drives both
+//    tensor cores and each document tile is read once per pair. The prep and
+//    epilogue warps of both CTAs report to the even CTA's barriers; the MMA
+//    completion is multicast to both.
 //  * INT8 mode ("Flash-MaxSim" Sec. 4.3.1): the tensor-core kind for 8-bit
 //    integers is not available on sm_103a, so the prep warps convert the INT8
 //    document tile to f16 in shared memory (exact: |v| <= 127), the MMA
@@ -95,6 +102,7 @@ struct FwdArgs {
     int32_t stages;       // operand ring depth
     int32_t stages8;      // INT8 staging ring depth (INT8 mode)
     int32_t q_slots;      // M-tiles of Q resident in shared memory
+    int32_t n_pr;         // pair mode: row-block pairs (ceil(n_rb / 2))
     uint32_t idesc;       // tcgen05 instruction descriptor without N
     uint32_t nan_pair;    // two 16-bit NaNs of the operand type
     int* status;          // device status word
@@ -110,6 +118,14 @@ struct RowBlock {
 
 __device__ __forceinline__ RowBlock row_block(const FwdArgs& a, int32_t rb) {
     RowBlock b;
+    if (rb >= a.n_rb) {  // the odd CTA of a last, half-empty pair
+        b.row0 = b.row_end = a.nq * a.lq_pad;
+        b.q0 = a.nq;
+        b.nqb = 0;
+        b.chunk = 0;
+        b.mt = 0;
+        return b;
+    }
     if (a.n_chunks == 1) {
         int32_t qpb = a.rb_rows / a.lq_pad;
         b.q0 = rb * qpb;
@@ -155,14 +171,25 @@ __device__ __forceinline__ int32_t range_first_doc(const FwdArgs& a, int32_t dr)
 
 struct Unit {
     RowBlock rb;
+    int32_t mt;          // M-tiles computed per tile (the pair's larger block in pair mode)
     int32_t j0, j1;      // documents [j0, j1)
     int32_t tok0;        // first token of document j0
 };
 
-__device__ __forceinline__ Unit make_unit(const FwdArgs& a, int32_t u) {
+template <bool kPair>
+__device__ __forceinline__ Unit make_unit(const FwdArgs& a, int32_t u, uint32_t rank) {
     Unit w;
-    w.rb = row_block(a, u % a.n_rb);
-    const int32_t dr = u / a.n_rb;
+    int32_t dr;
+    if constexpr (kPair) {
+        const int32_t pr = u % a.n_pr;
+        dr = u / a.n_pr;
+        w.rb = row_block(a, 2 * pr + static_cast<int32_t>(rank));
+        w.mt = max(w.rb.mt, row_block(a, 2 * pr + 1 - static_cast<int32_t>(rank)).mt);
+    } else {
+        w.rb = row_block(a, u % a.n_rb);
+        w.mt = w.rb.mt;
+        dr = u / a.n_rb;
+    }
     w.j0 = range_first_doc(a, dr);
     w.j1 = range_first_doc(a, dr + 1);
     w.tok0 = doc_start(a, w.j0);
@@ -213,6 +240,7 @@ struct alignas(16) SmemCtl {
     uint64_t q_full, q_empty;
     uint64_t d_full[kMaxStages], d_ready[kMaxStages], d_empty[kMaxStages];
     uint64_t d8_full[kMaxStages], d8_empty[kMaxStages];
+    uint64_t q_ready;  // pair mode: both CTAs' query rows have landed
     uint64_t acc_full[kNAcc], acc_empty[kNAcc];
     uint64_t mma_done;
     uint64_t epi_bar;  // rendezvous of the epilogue warps
@@ -232,10 +260,11 @@ __device__ __forceinline__ void record_status(const FwdArgs& a, int code) {
 // CTA abort flag) or when another role has already aborted. The slow path is
 // kept out of line so that every role's hot loop stays small in the
 // instruction cache.
+template <bool kCluster>
 __device__ __noinline__ bool wait_bar_slow(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (ctl->abort) return false;
             if (global_timer_ns() - t0 > a.timeout_ns) {
@@ -247,9 +276,12 @@ __device__ __noinline__ bool wait_bar_slow(const FwdArgs& a, SmemCtl* ctl, uint3
     }
 }
 
+// kCluster: the barrier also receives arrivals from the other CTA of a pair
+// (acquire at cluster scope).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_bar_slow(a, ctl, bar, parity);
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow<kCluster>(a, ctl, bar, parity);
 }
 
 // Bounded rendezvous of the epilogue warps (an mbarrier phase per use),
@@ -298,15 +330,18 @@ __device__ __forceinline__ void fold_chunk(const float (&y)[32], int32_t col0, f
 
 // ---------------------------------------------------------------- the kernel
 
-template <bool kArg, bool kInt8>
+template <bool kArg, bool kInt8, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_d,
                       const FwdArgs a) {
+    constexpr int kG = kPair ? 2 : 1;              // tcgen05 CTA group
+    constexpr int kDRows = kPair ? kBN / 2 : kBN;  // document rows per operand stage in this CTA
+    constexpr int kDAtom = kDRows * 128;           // bytes of one 128-byte-wide K block of a stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int32_t q_tile_bytes = a.k_atoms * kAtomBytes;    // one 128-row M-tile of Q
-    const int32_t d_stage_bytes = a.k_atoms * kAtomBytes;   // one 128-token operand tile
-    const int32_t d8_stage_bytes = a.k8_atoms * kAtomBytes; // one 128-token INT8 tile
+    const int32_t q_tile_bytes = a.k_atoms * kAtomBytes;  // one 128-row M-tile of Q
+    const int32_t d_stage_bytes = a.k_atoms * kDAtom;     // this CTA's rows of one operand tile
+    const int32_t d8_stage_bytes = a.k8_atoms * kDAtom;   // this CTA's rows of one INT8 tile
     uint8_t* sQ = smem;
     uint8_t* sD = smem + a.q_slots * q_tile_bytes;
     uint8_t* sD8 = sD + a.stages * d_stage_bytes;
@@ -315,8 +350,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    // shared::cluster address of a barrier of this CTA in the pair's even CTA
+    auto at_leader = [&](const uint64_t* bar) -> uint32_t {
+        return kPair ? map_shared_rank(smem_u32(bar), 0) : smem_u32(bar);
+    };
+    auto arrive_leader = [&](const uint64_t* bar) {
+        if constexpr (kPair) mbar_arrive_cluster(at_leader(bar));
+        else mbar_arrive(smem_u32(bar));
+    };
 
-    // Ring depths index fixed-size barrier arrays: refuse a launch that breaks them.
+    // Ring depths index fixed-size barrier arrays: refuse a launch that breaks
+    // them (both CTAs of a pair see the same arguments and return together).
     if (a.stages < 1 || a.stages > kMaxStages || (kInt8 && (a.stages8 < 1 || a.stages8 > kMaxStages)) ||
         a.q_slots < 1 || a.q_slots > kMaxMT) {
         if (threadIdx.x == 0) record_status(a, kStatusBadInput);
@@ -324,11 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (threadIdx.x == 0) {
+        const uint32_t ctas = kPair ? 2u : 1u;
         mbar_init(smem_u32(&ctl->q_full), 1);
         mbar_init(smem_u32(&ctl->q_empty), 1);
+        mbar_init(smem_u32(&ctl->q_ready), ctas);
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(smem_u32(&ctl->d_full[s]), 1);
-            mbar_init(smem_u32(&ctl->d_ready[s]), 2);
+            mbar_init(smem_u32(&ctl->d_ready[s]), 2 * ctas);
             mbar_init(smem_u32(&ctl->d_empty[s]), 1);
         }
         for (int s = 0; s < a.stages8; ++s) {
@@ -337,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < kNAcc; ++b) {
             mbar_init(smem_u32(&ctl->acc_full[b]), 1);
-            mbar_init(smem_u32(&ctl->acc_empty[b]), 4);
+            mbar_init(smem_u32(&ctl->acc_empty[b]), 4 * ctas);
         }
         mbar_init(smem_u32(&ctl->mma_done), 1);
         mbar_init(smem_u32(&ctl->epi_bar), kEpiWarps);
@@ -347,13 +395,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_d);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), kNAcc * kBN);
-        tmem_relinquish();
+        tmem_alloc<kG>(smem_u32(&ctl->tmem_base), kNAcc * kBN);
+        tmem_relinquish<kG>();
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();  // barriers of both CTAs exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
+    const int32_t n_units = a.n_units;
+    const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
+    const int32_t u_step = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -370,16 +422,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool first_unit = true;
             int64_t issued = 0;
             bool ok = true;
-            for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-                const Unit w = make_unit(a, u);
+            for (int32_t u = u0; u < n_units && ok; u += u_step) {
+                const Unit w = make_unit<kPair>(a, u, rank);
                 if (!first_unit) {
                     if (!wait_bar(a, ctl, smem_u32(&ctl->q_empty), q_phase)) break;
                     q_phase ^= 1u;
                 }
                 first_unit = false;
                 const uint32_t qbar = smem_u32(&ctl->q_full);
-                mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(w.rb.mt * q_tile_bytes));
-                for (int32_t k = 0; k < w.rb.mt; ++k)
+                mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(w.mt * q_tile_bytes));
+                for (int32_t k = 0; k < w.mt; ++k)
                     for (int32_t ka = 0; ka < a.k_atoms; ++ka)
                         tma_load_2d(smem_u32(sQ + k * q_tile_bytes + ka * kAtomBytes), &tm_q, qbar, ka * 64,
                                     w.rb.row0 + k * kBM);
@@ -389,9 +441,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(a, ctl, empty, phase ^ 1u)) { ok = false; break; }
                     const uint32_t fullb = smem_u32(kInt8 ? &ctl->d8_full[stage] : &ctl->d_full[stage]);
                     mbar_arrive_expect_tx(fullb, static_cast<uint32_t>(bytes));
+                    // this CTA's rows of the tile: all of them, or its half in pair mode
+                    const int32_t y = tw.row() + (kPair ? static_cast<int32_t>(rank) * (mma_n(tw.ntok()) >> 1) : 0);
                     for (int32_t ka = 0; ka < boxes; ++ka)
-                        tma_load_2d_hint(smem_u32(base + stage * bytes + ka * kAtomBytes), &tm_d, fullb,
-                                         ka * box_cols, tw.row(), pol_stream);
+                        tma_load_2d_hint(smem_u32(base + stage * bytes + ka * kDAtom), &tm_d, fullb, ka * box_cols, y,
+                                         pol_stream);
                     ++issued;
                     if (++stage == ring) { stage = 0; phase ^= 1u; }
                 }
@@ -410,86 +464,98 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer (even CTA of a pair)
+        if (lane == 0 && leader) {
             int32_t stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0, q_phase = 0;
             const uint64_t q_desc0 = sdesc_k_sw128(smem_u32(sQ));
+            const uint32_t idesc_m = a.idesc | (static_cast<uint32_t>((kPair ? 2 * kBM : kBM) >> 4) << 24);
             bool ok = true;
-            for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-                const Unit w = make_unit(a, u);
-                if (!wait_bar(a, ctl, smem_u32(&ctl->q_full), q_phase)) break;
+            for (int32_t u = u0; u < n_units && ok; u += u_step) {
+                const Unit w = make_unit<kPair>(a, u, rank);
+                if constexpr (kPair) {
+                    if (!wait_bar<true>(a, ctl, smem_u32(&ctl->q_ready), q_phase)) break;
+                } else {
+                    if (!wait_bar(a, ctl, smem_u32(&ctl->q_full), q_phase)) break;
+                }
                 q_phase ^= 1u;
                 tc_fence_after();
                 TileWalk tw;
                 for (tw.begin(a, w); tw.valid() && ok; tw.advance(a)) {
-                    if (!wait_bar(a, ctl, smem_u32(&ctl->d_ready[stage]), phase)) { ok = false; break; }
+                    if (!wait_bar<kPair>(a, ctl, smem_u32(&ctl->d_ready[stage]), phase)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t idesc = a.idesc | (static_cast<uint32_t>(mma_n(tw.ntok()) >> 3) << 17);
+                    const uint32_t idesc = idesc_m | (static_cast<uint32_t>(mma_n(tw.ntok()) >> 3) << 17);
                     const uint64_t b_desc0 = sdesc_k_sw128(smem_u32(sD + stage * d_stage_bytes));
-                    for (int32_t k = 0; k < w.rb.mt; ++k) {
-                        if (!wait_bar(a, ctl, smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u)) { ok = false; break; }
+                    for (int32_t k = 0; k < w.mt; ++k) {
+                        if (!wait_bar<kPair>(a, ctl, smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u)) { ok = false; break; }
                         tc_fence_after();
                         const uint64_t a_desc0 = q_desc0 + static_cast<uint64_t>((k * q_tile_bytes) >> 4);
                         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-                        // whole 64-element K blocks four MMAs at a time, then the
-                        // remaining 16-element steps one by one
-                        int32_t ks = 0;
                         if (a.k_steps == 8) {  // dim 128: fully unrolled
                             const uint32_t alo = static_cast<uint32_t>(a_desc0), ahi = static_cast<uint32_t>(a_desc0 >> 32);
                             const uint32_t blo = static_cast<uint32_t>(b_desc0), bhi = static_cast<uint32_t>(b_desc0 >> 32);
 #pragma unroll
                             for (int s8 = 0; s8 < 8; ++s8) {
-                                const uint32_t o = static_cast<uint32_t>(((s8 >> 2) * kAtomBytes + (s8 & 3) * 32) >> 4);
-                                mma_f16_ss_words(d_tmem, alo + o, ahi, blo + o, bhi, idesc, s8 > 0 ? 1u : 0u);
+                                const uint32_t oa = static_cast<uint32_t>(((s8 >> 2) * kAtomBytes + (s8 & 3) * 32) >> 4);
+                                const uint32_t ob = static_cast<uint32_t>(((s8 >> 2) * kDAtom + (s8 & 3) * 32) >> 4);
+                                mma_f16_ss_words<kG>(d_tmem, alo + oa, ahi, blo + ob, bhi, idesc, s8 > 0 ? 1u : 0u);
                             }
-                            ks = 8;
+                        } else {
+                            for (int32_t ks = 0; ks < a.k_steps; ++ks) {
+                                const uint64_t oa = static_cast<uint64_t>(((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4);
+                                const uint64_t ob = static_cast<uint64_t>(((ks >> 2) * kDAtom + (ks & 3) * 32) >> 4);
+                                mma_f16_ss<kG>(d_tmem, a_desc0 + oa, b_desc0 + ob, idesc, ks > 0 ? 1u : 0u);
+                            }
                         }
-                        for (; ks + 4 <= a.k_steps; ks += 4) {
-                            const uint64_t o = static_cast<uint64_t>(((ks >> 2) * kAtomBytes) >> 4);
-                            mma_f16_ss_k64(d_tmem, a_desc0 + o, b_desc0 + o, idesc, ks > 0 ? 1u : 0u);
-                        }
-                        for (; ks < a.k_steps; ++ks) {
-                            const uint64_t o = static_cast<uint64_t>(((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4);
-                            mma_f16_ss(d_tmem, a_desc0 + o, b_desc0 + o, idesc, ks > 0 ? 1u : 0u);
-                        }
-                        mma_commit(smem_u32(&ctl->acc_full[acc]));
+                        mma_commit<kG>(smem_u32(&ctl->acc_full[acc]));
                         if (++acc == kNAcc) { acc = 0; acc_phase ^= 1u; }
                     }
                     if (!ok) break;
-                    mma_commit(smem_u32(&ctl->d_empty[stage]));
+                    mma_commit<kG>(smem_u32(&ctl->d_empty[stage]));
                     if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&ctl->q_empty));
+                mma_commit<kG>(smem_u32(&ctl->q_empty));
             }
             // Drain: wait until every MMA issued above has completed.
-            mma_commit(smem_u32(&ctl->mma_done));
+            mma_commit<kG>(smem_u32(&ctl->mma_done), 1);
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(smem_u32(&ctl->mma_done), 0) && global_timer_ns() - t0 < a.timeout_ns) {}
         }
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------------ operand prep
         // f16/bf16: NaN-fill masked / padding rows in place. INT8: convert the
-        // staged INT8 tile to f16 rows (NaN for masked / padding rows).
+        // staged INT8 tile to f16 rows (NaN for masked / padding rows). In pair
+        // mode each CTA handles its half of the tile's rows.
         const int pt = threadIdx.x - 64;  // 0..63
         int32_t stage = 0, stage8 = 0;
-        uint32_t phase = 0, phase8 = 0;
+        uint32_t phase = 0, phase8 = 0, q_phase = 0;
         bool ok = true;
-        for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-            const Unit w = make_unit(a, u);
+        for (int32_t u = u0; u < n_units && ok; u += u_step) {
+            const Unit w = make_unit<kPair>(a, u, rank);
+            if constexpr (kPair) {
+                // report this CTA's query rows to the MMA issuer
+                if (pt == 0) {
+                    if (!wait_bar(a, ctl, smem_u32(&ctl->q_full), q_phase)) { ok = false; break; }
+                    arrive_leader(&ctl->q_ready);
+                }
+                q_phase ^= 1u;
+            }
             TileWalk tw;
             for (tw.begin(a, w); tw.valid(); tw.advance(a)) {
-                const int32_t n = tw.ntok(), N = mma_n(n), row0 = tw.row();
+                const int32_t n = tw.ntok(), N = mma_n(n);
+                const int32_t rows = kPair ? (N >> 1) : N;                      // this CTA's rows
+                const int32_t tr0 = kPair ? static_cast<int32_t>(rank) * rows : 0;  // their first tile row
+                const int32_t row0 = tw.row() + tr0;
                 uint8_t* dst = sD + stage * d_stage_bytes;
                 if constexpr (kInt8) {
                     if (!wait_bar(a, ctl, smem_u32(&ctl->d8_full[stage8]), phase8)) { ok = false; break; }
                     if (!wait_bar(a, ctl, smem_u32(&ctl->d_empty[stage]), phase ^ 1u)) { ok = false; break; }
                     const uint8_t* src = sD8 + stage8 * d8_stage_bytes;
                     const int32_t chunks = a.dim >> 4;  // 16-byte INT8 chunks per row
-                    for (int32_t x = pt; x < N * chunks; x += kPrepThreads) {
+                    for (int32_t x = pt; x < rows * chunks; x += kPrepThreads) {
                         const int32_t r = x / chunks, c = x - (x / chunks) * chunks;
-                        const bool nan_row = r >= n || (a.d_mask != nullptr && a.d_mask[row0 + r] == 0);
+                        const bool nan_row = tr0 + r >= n || (a.d_mask != nullptr && a.d_mask[row0 + r] == 0);
                         uint4 lo, hi;
                         if (nan_row) {
                             lo = make_uint4(a.nan_pair, a.nan_pair, a.nan_pair, a.nan_pair);
@@ -498,31 +564,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // INT8 rows: 128-byte swizzled rows of 128 elements per staging block
                             const int32_t blk = c >> 3, cc = c & 7;
                             const uint4 v = *reinterpret_cast<const uint4*>(
-                                src + blk * kAtomBytes + r * 128 + ((cc ^ (r & 7)) << 4));
+                                src + blk * kDAtom + r * 128 + ((cc ^ (r & 7)) << 4));
                             lo = i8x8_to_f16x8(v.x, v.y);
                             hi = i8x8_to_f16x8(v.z, v.w);
                         }
                         // 16 f16 values = two 16-byte chunks of a 64-element swizzled atom
                         const int32_t atom = c >> 2, c16 = (c & 3) * 2;
-                        uint8_t* rowp = dst + atom * kAtomBytes + r * 128;
+                        uint8_t* rowp = dst + atom * kDAtom + r * 128;
                         *reinterpret_cast<uint4*>(rowp + (((c16 + 0) ^ (r & 7)) << 4)) = lo;
                         *reinterpret_cast<uint4*>(rowp + (((c16 + 1) ^ (r & 7)) << 4)) = hi;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(smem_u32(&ctl->d_ready[stage]));
+                        arrive_leader(&ctl->d_ready[stage]);
                         mbar_arrive(smem_u32(&ctl->d8_empty[stage8]));
                     }
                     if (++stage8 == a.stages8) { stage8 = 0; phase8 ^= 1u; }
                 } else {
                     if (!wait_bar(a, ctl, smem_u32(&ctl->d_full[stage]), phase)) { ok = false; break; }
-                    if (a.d_mask != nullptr || N != n) {
+                    if (a.d_mask != nullptr || tr0 + rows > n) {
                         const uint4 nan4 = make_uint4(a.nan_pair, a.nan_pair, a.nan_pair, a.nan_pair);
-                        for (int32_t r = pt; r < N; r += kPrepThreads) {
-                            if (r < n && (a.d_mask == nullptr || a.d_mask[row0 + r] != 0)) continue;
+                        for (int32_t r = pt; r < rows; r += kPrepThreads) {
+                            if (tr0 + r < n && (a.d_mask == nullptr || a.d_mask[row0 + r] != 0)) continue;
                             for (int32_t ka = 0; ka < a.k_atoms; ++ka) {
-                                uint4* rowp = reinterpret_cast<uint4*>(dst + ka * kAtomBytes + r * 128);
+                                uint4* rowp = reinterpret_cast<uint4*>(dst + ka * kDAtom + r * 128);
 #pragma unroll
                                 for (int c = 0; c < 8; ++c) rowp[c] = nan4;
                             }
@@ -530,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fence_proxy_async_smem();
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctl->d_ready[stage]));
+                    if (lane == 0) arrive_leader(&ctl->d_ready[stage]);
                 }
                 if (++stage == a.stages) { stage = 0; phase ^= 1u; }
             }
@@ -549,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t buf = 0;                              // global index of the tile's first buffer
         uint32_t epi_phase = 0;
         bool ok = true;
-        for (int32_t u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-            const Unit w = make_unit(a, u);
+        for (int32_t u = u0; u < n_units && ok; u += u_step) {
+            const Unit w = make_unit<kPair>(a, u, rank);
             const RowBlock& rb = w.rb;
             const bool chunked = a.n_chunks > 1;
             int32_t row_i[kKPer], row_s[kKPer];
@@ -605,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < kKPer; ++q) {
                     const int k = g + kEpiGroups * q;
-                    if (k >= rb.mt) break;
+                    if (k >= w.mt) break;
                     const int64_t idx = buf + k;
                     const int32_t slot = static_cast<int32_t>(idx % kNAcc);
                     const uint32_t ph = static_cast<uint32_t>((idx / kNAcc) & 1);
@@ -647,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (h == nh - 1) {
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[slot]));
+                            if (lane == 0) arrive_leader(&ctl->acc_empty[slot]);
                         }
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
@@ -677,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                buf += rb.mt;
+                buf += w.mt;
                 if (closes && (a.lq_pad > 32 || (a.lq_pad == 32 && chunked))) {
                     if (!epi_sync(a, ctl, epi_phase)) { ok = false; break; }
                     if (et < rb.nqb) {
@@ -696,12 +762,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();  // no CTA leaves while its pair may still touch it
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        tmem_dealloc(tmem_base, kNAcc * kBN);
+        tmem_dealloc<kG>(tmem_base, kNAcc * kBN);
     }
 }
 

@@ -111,3 +111,31 @@ def test_repeatable_bitwise():
         again = ops.maxsim_fwd(Q, D, want_argmax=True)
         assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
     assert ops.device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", [
+    (40, 32, 7, 300, 128),   # 1280 query rows: three row blocks
+    (8, 128, 5, 260, 128),   # 1024 rows: one full pair of row blocks
+    (20, 48, 4, 97, 64),     # padded queries (48 -> 64 rows), 1280 rows
+])
+def test_several_row_blocks_integer_exact(dtype, shape):
+    # more than one 512-row block of query rows; exact integers make every
+    # argmax (ties included) comparable bit for bit
+    Nq, Lq, Nd, Ld, dim = shape
+    rng = np.random.default_rng(7 + sum(shape))
+    Q = datagen.float_to_bits(integer_rows(rng, Nq * Lq, dim), dtype).reshape(Nq, Lq, dim)
+    D = datagen.float_to_bits(integer_rows(rng, Nd * Ld, dim), dtype).reshape(Nd, Ld, dim)
+    qm = (rng.random((Nq, Lq)) > 0.2).astype(np.uint8)
+    dm = (rng.random((Nd, Ld)) > 0.2).astype(np.uint8)
+    run_case(Q, D, dtype, exact=True)
+    run_case(Q, D, dtype, q_mask=qm, d_mask=dm, exact=True)
+
+
+def test_colpali_like_gaussian():
+    Nq, Lq, Nd, Ld, dim = 16, 128, 6, 1024, 128
+    Q = datagen.gaussian_rows(12, 1, Nq * Lq, dim, "bf16").reshape(Nq, Lq, dim)
+    D = datagen.gaussian_rows(12, 2, Nd * Ld, dim, "bf16").reshape(Nd, Ld, dim)
+    qm = datagen.mask_drop_tail(12, 4, Nq, Lq, 40)
+    dm = datagen.mask_random_subset(12, 5, Nd, Ld, 200)
+    run_case(Q, D, "bf16", q_mask=qm, d_mask=dm)

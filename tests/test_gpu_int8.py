@@ -34,7 +34,11 @@ def run_int8(Q, qs, D, ds, q_mask=None, d_mask=None, exact=False, exact_scores=T
 
 
 @pytest.mark.parametrize("shape", [(2, 32, 5, 300, 128), (3, 8, 4, 130, 32), (1, 64, 3, 257, 256),
-                                   (2, 40, 3, 100, 96)])
+                                   (2, 40, 3, 100, 96),
+                                   # two or more row blocks: the two-CTA (cta_group::2) path, where each
+                                   # CTA holds half of every document tile; 1280 rows leave the last
+                                   # pair half empty
+                                   (40, 32, 3, 140, 128), (1, 1024, 3, 200, 128)])
 def test_int8_integer_exact(shape):
     # unit / power-of-two scales and |dot| * Lq < 2^24: every similarity and
     # every partial sum is exact in fp32, so scores, argmax (ties included)
@@ -47,8 +51,11 @@ def test_int8_integer_exact(shape):
     ds = np.where(rng.random((Nd, Ld)) > 0.5, 1.0, 0.5).astype(np.float32)  # powers of two stay exact
     qm = (rng.random((Nq, Lq)) > 0.2).astype(np.uint8)
     dm = (rng.random((Nd, Ld)) > 0.2).astype(np.uint8)
-    run_int8(Q, qs, D, ds, exact=True)
-    run_int8(Q, qs, D, ds, q_mask=qm, d_mask=dm, exact=True)
+    # scores are sums of Lq such values: exact in fp32 only while they stay
+    # well inside the 24-bit significand (half-integers need one bit more)
+    exact_scores = Lq * 127 * 7 * dim < (1 << 22)
+    run_int8(Q, qs, D, ds, exact=True, exact_scores=exact_scores)
+    run_int8(Q, qs, D, ds, q_mask=qm, d_mask=dm, exact=True, exact_scores=exact_scores)
 
 
 def test_int8_extreme_values_accumulate_exactly():

@@ -76,6 +76,26 @@ def test_varlen_every_tail_length_exact(dtype):
         assert np.array_equal(a.cpu().numpy(), ref_a)
 
 
+@pytest.mark.parametrize("dim", [128, 64])
+def test_varlen_two_row_blocks_every_tail_length_exact(dim):
+    # 32 queries x 32 tokens = 1024 rows (two row blocks, as in ColBERT
+    # reranking) against documents of 1..140 tokens
+    dtype, Nq, Lq = "f16", 32, 32
+    lens = np.concatenate([np.arange(1, 141), [0, 300, 0]])
+    rng = np.random.default_rng(5)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    Q = datagen.float_to_bits(integer_rows(rng, Nq * Lq, dim), dtype).reshape(Nq, Lq, dim)
+    D = datagen.float_to_bits(integer_rows(rng, int(cu[-1]), dim), dtype)
+    dm = (rng.random(int(cu[-1])) > 0.15).astype(np.uint8)
+    for d_mask in (None, dm):
+        s, a = ops.maxsim_fwd_varlen(dev_bits(Q, dtype), None, Lq, dev_bits(D, dtype), dev(cu.astype(np.int32)),
+                                     d_mask=dev(d_mask), want_argmax=True)
+        assert ops.device_status() == 0
+        ref_s, ref_a, _ = oracle.fwd_packed(Q.reshape(-1, dim), np.arange(Nq + 1) * Lq, D, cu, dtype, d_mask=d_mask)
+        assert np.array_equal(s.cpu().numpy().astype(np.float64), ref_s)
+        assert np.array_equal(a.cpu().numpy(), ref_a)
+
+
 def test_varlen_equals_dense_with_trailing_mask():
     # "same as the padded path": a trailing d_mask equals shorter packed documents
     dtype, Nq, Lq, Nd, Ld, dim = "bf16", 2, 32, 5, 200, 128
@@ -125,7 +145,9 @@ def test_backward_parity(dtype):
     assert_grad(dD, ref_dD)
     # bitwise reproducible (no atomics)
     dQ2, dD2, rp2, col2 = ops.maxsim_bwd(Qd, Dd, a, dev(g), dev(qm), want_csr=True)
-    assert torch.equal(dQ, dQ2) and torch.equal(dD, dD2) and torch.equal(col, col2)
+    n_src = int(ref_rp[-1])  # only the first row_ptr[-1] entries of col are written
+    assert torch.equal(dQ, dQ2) and torch.equal(dD, dD2) and torch.equal(rp, rp2)
+    assert torch.equal(col[:n_src], col2[:n_src])
 
 
 def test_backward_hot_token_contention():
