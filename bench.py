@@ -1,17 +1,26 @@
 #!/usr/bin/env python3
 """MaxSim throughput on one GB300 (docs scored / s) with its roofline.
 
-Default workload: ColBERT rerank over packed documents -- Nq = 32 queries of
-Lq = 32 tokens, Nd = 100,000 documents with lengths uniform in [32, 300],
-dim = 128, f16, l2-normalised Gaussian rows (seeded, synthetic). A step is one
-maxsim_fwd_varlen call scoring every document against every query.
+Default workload (the one the headline line reports): ColBERT rerank over
+packed documents -- Nq = 32 queries of Lq = 32 tokens, Nd = 100,000 documents
+with lengths uniform in [32, 300], dim = 128, f16, l2-normalised Gaussian rows
+(seeded, synthetic). A step is one maxsim_fwd_varlen call scoring every
+document against every query.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--shard weak|global]
+
+Other workloads (measured the same way, for the design notes):
+  tiny_rerank      1 x 32 tokens vs 1,000 x 180 (f16), scores + argmax
+  colpali_cross    128 x 128 vs 128 x 1024 (bf16), masks, scores + argmax
+  contrastive_bwd  the backward of 64 x 128 vs 64 x 1024 (bf16)
+  int8_rerank      1 x 1024 vs 10,000 x 1024 (INT8, per-token scales)
+Inputs smaller than L2 are timed step by step with an L2 flush between steps.
 
 Prints one JSON line (rank 0). Under torchrun every rank scores its own
-100,000 documents (weak scaling, no data-path communication); timing is the
-maximum over ranks between barriers.
+documents (--shard weak, the default: per-GPU work fixed) or its token-balanced
+share of one corpus (--shard global); there is no communication on the data
+path, and the time is the maximum over ranks between barriers.
 
 --impl reference times the CPU oracle (test infrastructure) on bounded samples
 of the same workload on the host cores.
@@ -36,6 +45,7 @@ if ROOT not in sys.path:
 
 METRIC = "MaxSim docs scored/s at 1 GB300 + % of roofline (HBM GB/s or tensor-pipe)"
 UNIT = "docs/s"
+L2_BYTES = 129 * 1024 * 1024
 
 # ---------------------------------------------------------------- byte / flop accounting
 
@@ -72,6 +82,23 @@ def varlen_algorithmic_bytes(nq: int, lq: int, dim: int, total_d: int, nd: int, 
     return nq * lq * dim * elem + total_d * dim * elem + (nd + 1) * 4 + nq * nd * 4
 
 
+def shard_documents(lens: np.ndarray, rank: int, world: int):
+    """Contiguous documents [j0, j1) of one rank, balanced by token count: the
+    first document whose start reaches rank * total / world opens the range."""
+    cu = np.concatenate([[0], np.cumsum(np.asarray(lens, dtype=np.int64))])
+    total = int(cu[-1])
+    nd = len(cu) - 1
+
+    def first(r):
+        if r <= 0:
+            return 0
+        if r >= world:
+            return nd
+        return int(np.searchsorted(cu[:-1], (total * r) // world, side="left"))
+
+    return first(rank), first(rank + 1)
+
+
 # ---------------------------------------------------------------- helpers
 
 def kernel_source_hash() -> str:
@@ -82,9 +109,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-# DRAM traffic of the forward kernel per launch on this workload, from one ncu
-# capture (profiles/maxsim_fwd_kernel__colbert_varlen.md), valid only for the
-# kernel sources whose hash is recorded with it.
+# DRAM traffic (read + write bytes) of the forward kernel per launch on the
+# default workload, scaled from one ncu capture of a 10,000-document instance
+# (profiles/maxsim_fwd_kernel__colbert_varlen.md); valid only for the kernel
+# sources whose hash is recorded with it.
 MEASURED_TRAFFIC = {}
 
 
@@ -155,25 +183,56 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workloads
 
-def build_workload(name: str, rank: int, nd: int = 0):
+def make_workload(name: str, rank: int, world: int, shard: str, nd: int = 0):
+    """Host arrays of a workload for this rank, plus a description."""
     from datagen import workloads
-    if name != "colbert_varlen":
-        raise SystemExit(f"unknown bench workload {name}")
+    if name not in workloads.SPECS:
+        raise SystemExit(f"unknown workload {name}; one of {sorted(workloads.SPECS)}")
     spec = dict(workloads.SPECS[name])
-    spec["seed"] = spec["seed"] + 1000 * rank  # every rank scores its own documents
+    if shard == "weak":
+        spec["seed"] = spec["seed"] + 1000 * rank  # every rank scores its own documents
     if nd:
         spec["Nd"] = nd  # smaller instance for profiler captures only
-    return workloads.varlen(**spec), spec
+    w = workloads.make(name, **spec)
+    w["name"] = name
+    if shard == "global" and world > 1:
+        if name != "colbert_varlen":
+            raise SystemExit("--shard global is implemented for colbert_varlen")
+        j0, j1 = shard_documents(w["lens"], rank, world)
+        cu = w["cu_seqlens_d"].astype(np.int64)
+        w["D"] = np.ascontiguousarray(w["D"][cu[j0]:cu[j1]])
+        w["lens"] = w["lens"][j0:j1]
+        w["cu_seqlens_d"] = (cu[j0:j1 + 1] - cu[j0]).astype(np.int32)
+        w["Nd"], w["total_d"] = j1 - j0, int(cu[j1] - cu[j0])
+    return w, spec
 
 
 def describe(w, spec):
-    return {
-        "workload": (f"colbert_varlen: Nq={w['Nq']} queries x Lq={w['Lq']} tokens vs Nd={w['Nd']} packed docs, "
-                     f"Ld~U[{spec['ld_min']},{spec['ld_max']}] (sum Ld={w['total_d']}), d={w['dim']}, f16, "
-                     f"l2-normalised Gaussian rows, seed {spec['seed']}"),
-        "Nq": w["Nq"], "Lq": w["Lq"], "Nd": w["Nd"], "total_d": w["total_d"], "dim": w["dim"],
-        "l2": "inputs larger than L2 (D alone is %.2f GB); no flush needed" % (w["total_d"] * w["dim"] * 2 / 1e9),
-    }
+    name = w["name"]
+    if name == "colbert_varlen":
+        text = (f"colbert_varlen: Nq={w['Nq']} queries x Lq={w['Lq']} tokens vs Nd={w['Nd']} packed docs, "
+                f"Ld~U[{spec['ld_min']},{spec['ld_max']}] (sum Ld={w['total_d']}), d={w['dim']}, f16, "
+                f"l2-normalised Gaussian rows, seed {spec['seed']}")
+        d_bytes = w["total_d"] * w["dim"] * 2
+    elif name == "int8_rerank":
+        text = (f"int8_rerank: Q int8 [{w['Nq']},{w['Lq']},{w['dim']}] (query rows in 512-row chunks), "
+                f"D int8 [{w['Nd']},{w['Ld']},{w['dim']}], per-token f32 scales of l2-normalised Gaussian rows, "
+                f"seed {spec['seed']}")
+        d_bytes = w["Nd"] * w["Ld"] * w["dim"]
+    else:
+        masks = (" q_mask drops the last U{0..40} tokens, d_mask hides U{0..200} random patches;"
+                 if name == "colpali_cross" else "")
+        text = (f"{name}: Q [{w['Nq']},{w['Lq']},{w['dim']}] vs D [{w['Nd']},{w['Ld']},{w['dim']}] {w['dtype']},"
+                f"{masks} l2-normalised Gaussian rows, seed {spec['seed']}")
+        d_bytes = w["Nd"] * w["Ld"] * w["dim"] * 2
+    cfg = {"workload": text}
+    for k in ("Nq", "Lq", "Nd", "Ld", "total_d", "dim"):
+        if k in w:
+            cfg[k] = w[k]
+    cfg["l2"] = ("inputs larger than L2 (D alone is %.2f GB); no flush needed" % (d_bytes / 1e9)
+                 if d_bytes > L2_BYTES else
+                 "inputs smaller than L2: a 256 MiB buffer is rewritten before every timed step")
+    return cfg
 
 
 # ---------------------------------------------------------------- the oracle arm
@@ -181,34 +240,42 @@ def describe(w, spec):
 def time_oracle(w, n_docs: int, threads: int = 0):
     """Oracle docs/s on the first n_docs documents (a bounded sample)."""
     import oracle
-    q_off = np.arange(w["Nq"] + 1, dtype=np.int64) * w["Lq"]
-    cu = w["cu_seqlens_d"].astype(np.int64)
     docs = np.arange(n_docs, dtype=np.int64)
     t0 = time.perf_counter()
-    oracle.fwd_packed(w["Q"].reshape(-1, w["dim"]), q_off, w["D"], cu, "f16", docs=docs, threads=threads)
+    name = w["name"]
+    if name == "colbert_varlen":
+        q_off = np.arange(w["Nq"] + 1, dtype=np.int64) * w["Lq"]
+        oracle.fwd_packed(w["Q"].reshape(-1, w["dim"]), q_off, w["D"], w["cu_seqlens_d"].astype(np.int64), "f16",
+                          docs=docs, threads=threads)
+    elif name == "int8_rerank":
+        oracle.fwd_int8(w["Q"], w["q_scale"], w["D"], w["d_scale"], docs=docs, threads=threads)
+    elif name == "contrastive_bwd":
+        raise SystemExit("the oracle arm times forward workloads")
+    else:
+        oracle.fwd_dense(w["Q"], w["D"], w["dtype"], q_mask=w.get("q_mask"), d_mask=w.get("d_mask"), docs=docs,
+                         threads=threads)
     dt = time.perf_counter() - t0
     return n_docs / dt, dt
 
 
 def calibrated_sample(w, target_s: float):
-    rate, _ = time_oracle(w, 32)
-    n = int(max(32, min(w["Nd"], rate * target_s)))
-    return n
+    probe = min(8, w["Nd"])
+    rate, _ = time_oracle(w, probe)
+    return int(max(probe, min(w["Nd"], rate * target_s)))
 
 
 def run_reference(args, rank, world):
     import oracle
     if rank != 0:
         return
-    w, spec = build_workload(args.workload, 0, args.nd)
+    w, spec = make_workload(args.workload, 0, 1, "weak", args.nd)
     cores = oracle.max_threads()
     n = calibrated_sample(w, target_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(w, n)
-    rates, times = [], []
+    times = []
     for _ in range(args.steps):
-        r, dt = time_oracle(w, n)
-        rates.append(r)
+        _, dt = time_oracle(w, n)
         times.append(dt)
     value = n * args.steps / sum(times)
     sample = f"first {n} of {w['Nd']} documents per step, all {w['Nq']} queries"
@@ -225,6 +292,119 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------- our arm
 
+class Case:
+    """One workload on one GPU: device inputs, the timed call, and the bytes /
+    FLOPs that bound it."""
+
+    def __init__(self, w, device):
+        import torch as t
+
+        from maxsim_scoring_gb300 import _native, ops
+        self.w, self.device, self.ops = w, device, ops
+        name = w["name"]
+        self.name = name
+
+        def pinned_half(bits, dtype):
+            return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(dtype).pin_memory()
+
+        def pinned(x):
+            return t.from_numpy(np.ascontiguousarray(x)).pin_memory()
+
+        self.h_in, self.d_in = {}, {}
+        if name == "int8_rerank":
+            for k in ("Q", "q_scale", "D", "d_scale"):
+                self.h_in[k] = pinned(w[k])
+        else:
+            dt = t.float16 if w["dtype"] == "f16" else t.bfloat16
+            self.h_in["Q"], self.h_in["D"] = pinned_half(w["Q"], dt), pinned_half(w["D"], dt)
+            for k in ("cu_seqlens_d", "q_mask", "d_mask", "grad"):
+                if w.get(k) is not None:
+                    self.h_in[k] = pinned(w[k])
+        for k, v in self.h_in.items():
+            self.d_in[k] = v.to(device)
+        self.e2e_in = {k: t.empty_like(v) for k, v in self.d_in.items()}
+        Nq, Nd, dim = w["Nq"], w["Nd"], w["dim"]
+        self.scores = t.empty((Nq, Nd), dtype=t.float32, device=device)
+        self.h_scores = t.empty((Nq, Nd), dtype=t.float32).pin_memory()
+        self.units = Nd
+        self.argmax = None
+        if name == "colbert_varlen":
+            Lq, T = w["Lq"], w["total_d"]
+            ws = ops.workspace_size(_native.OP_FWD_VARLEN, Nq, Lq, Nd, T, dim)
+            self.flops = maxsim_flops(Nq * Lq, dim, T)
+            self.bytes = varlen_algorithmic_bytes(Nq, Lq, dim, T, Nd)
+            self.bound, self.dtype, self.launches = "tensor", "f16", 3
+        elif name == "int8_rerank":
+            Lq, Ld = w["Lq"], w["Ld"]
+            ws = ops.workspace_size(_native.OP_FWD_INT8, Nq, Lq, Nd, Ld, dim)
+            self.flops = maxsim_flops(Nq * Lq, dim, Nd * Ld)
+            self.bytes = Nq * Lq * (dim + 4) + Nd * Ld * (dim + 4) + Nq * Nd * 4
+            self.bound, self.dtype, self.launches = "tensor", "int8 (f16 MMA, fp32 acc)", 3
+        else:
+            Lq, Ld = w["Lq"], w["Ld"]
+            self.argmax = t.empty((Nq * Nd, Lq), dtype=t.int32, device=device)
+            ws = max(ops.workspace_size(_native.OP_FWD, Nq, Lq, Nd, Ld, dim),
+                     ops.workspace_size(_native.OP_BWD, Nq, Lq, Nd, Ld, dim))
+            self.dtype = w["dtype"]
+            if name == "contrastive_bwd":
+                ops.maxsim_fwd(self.d_in["Q"], self.d_in["D"], argmax=self.argmax, want_argmax=True)
+                self.dQ = t.empty((Nq, Lq, dim), dtype=t.float32, device=device)
+                self.dD = t.empty((Nd, Ld, dim), dtype=t.float32, device=device)
+                self.flops = 2 * 2 * Nq * Nd * Lq * dim
+                # read Q, D, argmax (counts and placement), g; write the CSR and
+                # read it back; write dQ and dD
+                self.bytes = (Nq * Lq * dim * 2 + Nd * Ld * dim * 2 + 2 * Nq * Nd * Lq * 4 + Nq * Nd * 4
+                              + 2 * (Nd * Ld + 1 + Nq * Nd * Lq) * 4 + (Nq * Lq + Nd * Ld) * dim * 4)
+                self.bound, self.launches = "hbm", 5
+            else:
+                self.flops = maxsim_flops(Nq * Lq, dim, Nd * Ld)
+                self.bytes = (Nq * Lq * dim * 2 + Nd * Ld * dim * 2 + Nq * Nd * 4 + Nq * Nd * Lq * 4
+                              + (Nq * Lq + Nd * Ld if name == "colpali_cross" else 0))
+                self.bound = "hbm" if name == "tiny_rerank" else "tensor"
+                self.launches = 1
+        self.ws = t.empty(max(1, ws), dtype=t.uint8, device=device)
+        in_bytes = sum(v.numel() * v.element_size() for v in self.d_in.values())
+        self.flush_buf = (t.empty(256 * 1024 * 1024 // 4, dtype=t.float32, device=device)
+                          if in_bytes < 2 * L2_BYTES else None)
+
+    def call(self, d):
+        w, ops, name = self.w, self.ops, self.name
+        if name == "colbert_varlen":
+            ops.maxsim_fwd_varlen(d["Q"], None, w["Lq"], d["D"], d["cu_seqlens_d"], scores=self.scores,
+                                  workspace=self.ws)
+        elif name == "int8_rerank":
+            ops.maxsim_fwd_int8(d["Q"], d["q_scale"], d["D"], d["d_scale"], scores=self.scores, workspace=self.ws)
+        elif name == "contrastive_bwd":
+            ops.maxsim_bwd(d["Q"], d["D"], self.argmax, d["grad"], dQ=self.dQ, dD=self.dD, workspace=self.ws)
+        else:
+            ops.maxsim_fwd(d["Q"], d["D"], d.get("q_mask"), d.get("d_mask"), scores=self.scores,
+                           argmax=self.argmax, want_argmax=True, workspace=self.ws)
+
+    def step(self):
+        self.call(self.d_in)
+
+    def e2e_step(self):
+        for k, v in self.h_in.items():
+            self.e2e_in[k].copy_(v, non_blocking=True)
+        self.call(self.e2e_in)
+        if self.name == "contrastive_bwd":
+            self.dQ.cpu()  # the step's result comes back to the host
+        else:
+            self.h_scores.copy_(self.scores, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.h_in.values())
+
+    def d2h_bytes(self):
+        if self.name == "contrastive_bwd":
+            return self.dQ.numel() * 4
+        return self.scores.numel() * 4
+
+    def flush(self):
+        if self.flush_buf is not None:
+            self.flush_buf.add_(1.0)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -234,29 +414,17 @@ def run_ours(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     _native.lib()  # fail loudly without the extension
-    w, spec = build_workload(args.workload, rank, args.nd)
-    Nq, Lq, Nd, dim, total_d = w["Nq"], w["Lq"], w["Nd"], w["dim"], w["total_d"]
-
-    # pinned host copies (the e2e leg copies them in every step)
-    h_Q = torch.from_numpy(w["Q"].view(np.int16)).view(torch.float16).pin_memory()
-    h_D = torch.from_numpy(w["D"].view(np.int16)).view(torch.float16).pin_memory()
-    h_cu = torch.from_numpy(w["cu_seqlens_d"]).pin_memory()
-    h_scores = torch.empty((Nq, Nd), dtype=torch.float32).pin_memory()
-    Q, D, cu = h_Q.to(device), h_D.to(device), h_cu.to(device)
-    scores = torch.empty((Nq, Nd), dtype=torch.float32, device=device)
-    ws_bytes = ops.workspace_size(_native.OP_FWD_VARLEN, Nq, Lq, Nd, total_d, dim)
-    ws = torch.empty(max(1, ws_bytes), dtype=torch.uint8, device=device)
+    w, spec = make_workload(args.workload, rank, world, args.shard, args.nd)
+    case = Case(w, device)
     stream = torch.cuda.current_stream(device)
-
-    def step():
-        ops.maxsim_fwd_varlen(Q, None, Lq, D, cu, scores=scores, workspace=ws)
 
     def barrier():
         if world > 1:
             dist.barrier()
 
     for _ in range(max(3, args.warmup)):
-        step()
+        case.flush()
+        case.step()
     torch.cuda.synchronize(device)
     if ops.device_status(device) != 0:
         raise SystemExit("device status after warm-up is not OK")
@@ -265,79 +433,83 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     barrier()
     torch.cuda.synchronize(device)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    ev[0].record(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for k in range(args.steps):
-        step()
-        ev[k + 1].record(stream)
+        case.flush()  # outside the events (no-op for inputs larger than L2)
+        starts[k].record(stream)
+        case.step()
+        ends[k].record(stream)
     torch.cuda.synchronize(device)
     barrier()
     clk = clocks.stop()
-    per_step_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[args.steps])
+    per_step_ms = [starts[k].elapsed_time(ends[k]) for k in range(args.steps)]
+    total_ms = sum(per_step_ms)
     if ops.device_status(device) != 0:
         raise SystemExit("device status after the timed steps is not OK")
 
     # end to end through the same public call: H2D of the step's inputs, the
-    # call, D2H of the scores, all on the stream and inside the events
+    # call, D2H of the result, all on the stream and inside the events
     e2e_steps = max(1, min(args.steps, 5))
-    d_Q, d_D, d_cu = torch.empty_like(Q), torch.empty_like(D), torch.empty_like(cu)
-    h2d = h_Q.numel() * 2 + h_D.numel() * 2 + h_cu.numel() * 4
-    d2h = Nq * Nd * 4
     barrier()
     torch.cuda.synchronize(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        d_Q.copy_(h_Q, non_blocking=True)
-        d_D.copy_(h_D, non_blocking=True)
-        d_cu.copy_(h_cu, non_blocking=True)
-        ops.maxsim_fwd_varlen(d_Q, None, Lq, d_D, d_cu, scores=scores, workspace=ws)
-        h_scores.copy_(scores, non_blocking=True)
+        case.e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(device)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    # max over ranks
+    # max over ranks; units summed over ranks
     t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=device)
+    units = torch.tensor([case.units], dtype=torch.float64, device=device)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(t[0]), float(t[1])
+        dist.all_reduce(units, op=dist.ReduceOp.SUM)
+    total_ms, e2e_ms, all_units = float(t[0]), float(t[1]), float(units[0])
     if rank != 0:
         return
 
     ms = total_ms / args.steps
-    value = world * Nd / (ms / 1e3)
+    value = all_units / (ms / 1e3)
     peaks, peak_src = load_peaks()
-    flops = maxsim_flops(Nq * Lq, dim, total_d)
-    achieved_tflops = flops / (ms / 1e3) / 1e12
-    sustained = total_ms > 1000.0
-    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
-    traffic = MEASURED_TRAFFIC.get(kernel_source_hash())
+    if case.bound == "tensor":
+        achieved = case.flops / (ms / 1e3) / 1e12
+        sustained = total_ms > 1000.0
+        peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+        src = f"{peak_src} {'sustained' if sustained else 'burst'} dense bf16 (f16 runs at the same rate)"
+    else:
+        achieved = case.bytes / (ms / 1e3) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+        src = f"{peak_src} HBM copy bandwidth"
+    traffic = MEASURED_TRAFFIC.get(kernel_source_hash()) if case.name == "colbert_varlen" else None
     roofline = {
-        "bound": "tensor", "achieved": round(achieved_tflops, 2), "peak": peak, "unit": "TFLOP/s",
-        "frac": round(achieved_tflops / peak, 4), "traffic": traffic,
-        "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} dense bf16 (f16 runs at the same rate)",
-        "kernel": "maxsim_fwd_kernel (duration = whole entry-point call incl. two small helper kernels)",
-        "algorithmic_flops_per_launch": flops,
-        "algorithmic_bytes_per_launch": varlen_algorithmic_bytes(Nq, Lq, dim, total_d, Nd),
+        "bound": case.bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+        "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": src,
+        "kernel": ("maxsim_fwd_kernel (duration = whole entry-point call, which also runs small helper kernels)"
+                   if case.name != "contrastive_bwd" else "backward kernels (whole maxsim_bwd call)"),
+        "algorithmic_flops_per_launch": case.flops,
+        "algorithmic_bytes_per_launch": case.bytes,
     }
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic", "config": describe(w, spec), "clocks": clk, "roofline": roofline,
-        "e2e": {"value": world * Nd / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "strong" if args.shard == "global" else "weak",
+        "vs_baseline": None, "dtype": case.dtype, "data": "synthetic", "config": describe(w, spec), "clocks": clk,
+        "roofline": roofline,
+        "e2e": {"value": all_units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": case.h2d_bytes(),
+                "d2h_bytes_per_step": case.d2h_bytes()},
+        "gpu_launches": case.launches * args.steps,
         "step_ms_min_median_max": [min(per_step_ms), statistics.median(per_step_ms), max(per_step_ms)],
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and case.name != "contrastive_bwd":
         import oracle
         n = calibrated_sample(w, target_s=args.cpu_seconds)
         rate, dt = time_oracle(w, n)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-                                "sample": f"first {n} of {Nd} documents, all {Nq} queries ({dt:.1f} s)"}
+                                "sample": f"first {n} of {w['Nd']} documents, all {w['Nq']} queries ({dt:.1f} s)"}
     print(json.dumps(line), flush=True)
 
 
@@ -348,6 +520,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="colbert_varlen")
+    ap.add_argument("--shard", choices=["weak", "global"], default="weak")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--nd", type=int, default=0, help="override the document count (profiler captures only)")

@@ -129,6 +129,7 @@ def maxsim_fwd_varlen(Q: torch.Tensor, cu_seqlens_q: Optional[torch.Tensor], max
 
 def maxsim_bwd(Q: torch.Tensor, D: torch.Tensor, argmax: torch.Tensor, grad_scores: torch.Tensor, q_mask=None, *,
                want_dq: bool = True, want_dd: bool = True, want_csr: bool = False,
+               dQ: Optional[torch.Tensor] = None, dD: Optional[torch.Tensor] = None,
                workspace: Optional[torch.Tensor] = None):
     """dQ [Nq,Lq,d] f32, dD [Nd,Ld,d] f32 (and the CSR row_ptr / col)."""
     if Q.dtype not in _DT or D.dtype != Q.dtype:
@@ -142,8 +143,13 @@ def maxsim_bwd(Q: torch.Tensor, D: torch.Tensor, argmax: torch.Tensor, grad_scor
     if am.numel() != Nq * Nd * Lq or g.numel() != Nq * Nd:
         raise ValueError("argmax must be [Nq*Nd, Lq] and grad_scores [Nq, Nd]")
     qm = _mask(q_mask, "q_mask", dev)
-    dQ = torch.empty((Nq, Lq, dim), dtype=torch.float32, device=dev) if want_dq else None
-    dD = torch.empty((Nd, Ld, dim), dtype=torch.float32, device=dev) if want_dd else None
+    if dQ is None and want_dq:
+        dQ = torch.empty((Nq, Lq, dim), dtype=torch.float32, device=dev)
+    if dD is None and want_dd:
+        dD = torch.empty((Nd, Ld, dim), dtype=torch.float32, device=dev)
+    for t, shape, name in ((dQ, (Nq, Lq, dim), "dQ"), (dD, (Nd, Ld, dim), "dD")):
+        if t is not None and (tuple(t.shape) != shape or t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 tensor of shape {shape}")
     row_ptr = torch.empty(Nd * Ld + 1, dtype=torch.int32, device=dev) if want_csr else None
     col = torch.empty(max(1, Nq * Nd * Lq), dtype=torch.int32, device=dev) if want_csr else None
     ws, nbytes = _workspace(workspace_size(_native.OP_BWD, Nq, Lq, Nd, Ld, dim), dev, workspace)
