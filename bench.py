@@ -109,11 +109,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-# DRAM traffic (read + write bytes) of the forward kernel per launch on the
-# default workload, scaled from one ncu capture of a 10,000-document instance
-# (profiles/maxsim_fwd_kernel__colbert_varlen.md); valid only for the kernel
-# sources whose hash is recorded with it.
-MEASURED_TRAFFIC = {}
+# DRAM traffic (read + write bytes) of the forward kernel per launch on a
+# workload's default size, scaled by the document tokens from one ncu capture
+# of a smaller instance (profiles/maxsim_fwd_kernel__colbert_varlen.md,
+# profiles/maxsim_fwd_kernel_pair_int8__int8_rerank.md); valid only for the
+# kernel sources whose hash is recorded with it.
+MEASURED_TRAFFIC = {
+    ("colbert_varlen", "ee56a13d550698fe"): 4345643108,  # (428.94 + 3.82) MB x 16,644,526 / 1,657,544 tokens
+    ("int8_rerank", "ee56a13d550698fe"): 1369128960,     # (270.70 + 3.13) MB x 10,000 / 2,000 documents
+}
 
 
 def load_peaks():
@@ -485,7 +489,7 @@ def run_ours(args, rank, world, local_rank):
         achieved = case.bytes / (ms / 1e3) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
         src = f"{peak_src} HBM copy bandwidth"
-    traffic = MEASURED_TRAFFIC.get(kernel_source_hash()) if case.name == "colbert_varlen" else None
+    traffic = (MEASURED_TRAFFIC.get((case.name, kernel_source_hash())) if args.nd is None and world == 1 else None)
     roofline = {
         "bound": case.bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": src,
