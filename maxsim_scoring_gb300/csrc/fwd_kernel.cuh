@@ -22,9 +22,15 @@
 //    Sec. 4.1.1; design notes, "Mask handling"). A row whose every column is
 //    masked keeps m = -inf.
 //  * For every (tile, M-tile) one MMA chain S = Q_blk * D_tile^T (K = dim)
-//    accumulates in one of four 128-column TMEM buffers; the epilogue warps
-//    read it with tcgen05.ld while the tensor core fills the next buffer.
-//  * Pair mode (a cluster of two CTAs on two SMs): the MMA is
+//    accumulates in a 128-column TMEM buffer; the epilogue warps read it
+//    with tcgen05.ld while the tensor core fills the next buffer. A single
+//    CTA keeps its query M-tiles in tensor memory as the MMA's A operand
+//    (tcgen05.mma with A in TMEM: only the document tile is read from shared
+//    memory) next to two accumulator buffers; the epilogue warps stage the
+//    rows there at the start of each unit. One elected lane of the MMA warp
+//    issues each K = dim chain from a single asm block.
+//  * Pair mode (a cluster of two CTAs on two SMs, query rows in shared
+//    memory, four accumulator buffers): the MMA is
 //    tcgen05.mma.cta_group::2 with M = 256, issued by the even CTA. Each CTA
 //    keeps its own row block of query rows (the A half of the MMA) and loads
 //    half of every document tile (the B half): one instruction drives both
@@ -58,12 +64,20 @@ constexpr int kBN = 128;          // document tokens per tile (largest MMA N)
 constexpr int kBM = 128;          // query rows per M-tile (MMA M)
 constexpr int kMaxMT = 4;         // M-tiles per row block
 constexpr int kNAcc = 4;          // TMEM accumulator buffers (4 x 128 columns)
+constexpr int kAccBufsTS = 2;     // ... when the query rows share TMEM with them (two 128-column slots left for Q)
 constexpr int kEpiGroups = 2;     // epilogue warpgroups; group g owns the M-tiles k with k % 2 == g
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // warp 0 TMA, warp 1 MMA, warps 2-3 prep, then the epilogue
 constexpr int kEpiWarp0 = 4;
 constexpr int kPrepThreads = 64;
 constexpr int kAtomBytes = 128 * 128;  // one 128-row x 128-byte swizzled block
+// Registers per thread: the launch gives every thread kRegsLaunch; the
+// producer / MMA / prep warpgroup then hands registers to the two epilogue
+// warpgroups, which hold a whole accumulator buffer row (128 values).
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsCtl = 72;
+constexpr int kRegsEpi = 216;
+static_assert(kRegsCtl * 128 + kRegsEpi * 256 <= kRegsLaunch * (128 + 32 * kEpiWarps), "register split");
 constexpr int kMaxStages = 8;
 
 // Device status codes (match maxsim_status).
@@ -101,7 +115,9 @@ struct FwdArgs {
     int32_t dim;
     int32_t stages;       // operand ring depth
     int32_t stages8;      // INT8 staging ring depth (INT8 mode)
-    int32_t q_slots;      // M-tiles of Q resident in shared memory
+    int32_t q_slots;      // M-tiles of Q resident in shared memory (0: Q lives in tensor memory)
+    const uint16_t* q_rows;  // padded 16-bit query rows [R, dim] (read directly when Q lives in TMEM)
+    int32_t q_cols;       // TMEM columns of one M-tile of Q (dim / 2)
     int32_t n_pr;         // pair mode: row-block pairs (ceil(n_rb / 2))
     uint32_t idesc;       // tcgen05 instruction descriptor without N
     uint32_t nan_pair;    // two 16-bit NaNs of the operand type
@@ -257,11 +273,11 @@ __device__ __forceinline__ void record_status(const FwdArgs& a, int code) {
 }
 
 // Bounded wait: gives up after timeout_ns (records the status and raises the
-// CTA abort flag) or when another role has already aborted. The slow path is
-// kept out of line so that every role's hot loop stays small in the
-// instruction cache.
+// CTA abort flag) or when another role has already aborted. Inlined: the
+// kernel's warpgroups run under different register budgets (setmaxnreg),
+// which an out-of-line call shared between them cannot follow.
 template <bool kCluster>
-__device__ __noinline__ bool wait_bar_slow(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar_slow(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
@@ -282,6 +298,14 @@ template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     return wait_bar_slow<kCluster>(a, ctl, bar, parity);
+}
+
+// wait_bar for a whole warp that runs warp-uniform code: every lane polls,
+// and the warp continues together with one answer.
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_bar_warp(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
+    const bool ok = wait_bar<kCluster>(a, ctl, bar, parity);
+    return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // Bounded rendezvous of the epilogue warps (an mbarrier phase per use),
@@ -335,6 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_d,
                       const FwdArgs a) {
     constexpr int kG = kPair ? 2 : 1;              // tcgen05 CTA group
+    // Single CTAs keep the query rows in tensor memory (the MMA's A operand
+    // then costs no shared-memory bandwidth) next to two accumulator
+    // buffers; CTA pairs keep them in shared memory next to four.
+    constexpr bool kTS = !kPair;
+    constexpr int kAccBufs = kTS ? kAccBufsTS : kNAcc;
+    constexpr uint32_t kQCol0 = kAccBufs * kBN;    // first TMEM column of Q (TS)
     constexpr int kDRows = kPair ? kBN / 2 : kBN;  // document rows per operand stage in this CTA
     constexpr int kDAtom = kDRows * 128;           // bytes of one 128-byte-wide K block of a stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -364,14 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Ring depths index fixed-size barrier arrays: refuse a launch that breaks
     // them (both CTAs of a pair see the same arguments and return together).
     if (a.stages < 1 || a.stages > kMaxStages || (kInt8 && (a.stages8 < 1 || a.stages8 > kMaxStages)) ||
-        a.q_slots < 1 || a.q_slots > kMaxMT) {
+        (kTS ? (a.q_slots != 0 || a.q_cols < 8 ||
+                kQCol0 + ((a.rb_rows + kBM - 1) / kBM) * a.q_cols > static_cast<uint32_t>(kNAcc * kBN))
+             : (a.q_slots < 1 || a.q_slots > kMaxMT))) {
         if (threadIdx.x == 0) record_status(a, kStatusBadInput);
         return;
     }
 
     if (threadIdx.x == 0) {
         const uint32_t ctas = kPair ? 2u : 1u;
-        mbar_init(smem_u32(&ctl->q_full), 1);
+        mbar_init(smem_u32(&ctl->q_full), kTS ? kEpiWarps : 1);
         mbar_init(smem_u32(&ctl->q_empty), 1);
         mbar_init(smem_u32(&ctl->q_ready), ctas);
         for (int s = 0; s < a.stages; ++s) {
@@ -383,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctl->d8_full[s]), 1);
             mbar_init(smem_u32(&ctl->d8_empty[s]), 2);
         }
-        for (int b = 0; b < kNAcc; ++b) {
+        for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(smem_u32(&ctl->acc_full[b]), 1);
             mbar_init(smem_u32(&ctl->acc_empty[b]), 4 * ctas);
         }
@@ -407,6 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
     const int32_t u_step = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
 
+    // Warpgroup 0 (producer, MMA, prep) gives registers to the epilogue
+    // warpgroups; each branch below runs under its own register budget.
+    if (warp < kEpiWarp0) {
+    regs_release<kRegsCtl>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -424,17 +460,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int32_t u = u0; u < n_units && ok; u += u_step) {
                 const Unit w = make_unit<kPair>(a, u, rank);
-                if (!first_unit) {
-                    if (!wait_bar(a, ctl, smem_u32(&ctl->q_empty), q_phase)) break;
-                    q_phase ^= 1u;
+                if constexpr (!kTS) {
+                    if (!first_unit) {
+                        if (!wait_bar(a, ctl, smem_u32(&ctl->q_empty), q_phase)) break;
+                        q_phase ^= 1u;
+                    }
+                    first_unit = false;
+                    const uint32_t qbar = smem_u32(&ctl->q_full);
+                    mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(w.mt * q_tile_bytes));
+                    for (int32_t k = 0; k < w.mt; ++k)
+                        for (int32_t ka = 0; ka < a.k_atoms; ++ka)
+                            tma_load_2d(smem_u32(sQ + k * q_tile_bytes + ka * kAtomBytes), &tm_q, qbar, ka * 64,
+                                        w.rb.row0 + k * kBM);
                 }
-                first_unit = false;
-                const uint32_t qbar = smem_u32(&ctl->q_full);
-                mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(w.mt * q_tile_bytes));
-                for (int32_t k = 0; k < w.mt; ++k)
-                    for (int32_t ka = 0; ka < a.k_atoms; ++ka)
-                        tma_load_2d(smem_u32(sQ + k * q_tile_bytes + ka * kAtomBytes), &tm_q, qbar, ka * 64,
-                                    w.rb.row0 + k * kBM);
                 TileWalk tw;
                 for (tw.begin(a, w); tw.valid(); tw.advance(a)) {
                     const uint32_t empty = smem_u32(kInt8 ? &ctl->d8_empty[stage] : &ctl->d_empty[stage]);
@@ -465,64 +503,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA of a pair)
-        if (lane == 0 && leader) {
+        // The whole warp runs this loop with warp-uniform values; one elected
+        // lane issues the MMA chains and the commits.
+        if (leader) {
             int32_t stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0, q_phase = 0;
             const uint64_t q_desc0 = sdesc_k_sw128(smem_u32(sQ));
             const uint32_t idesc_m = a.idesc | (static_cast<uint32_t>((kPair ? 2 * kBM : kBM) >> 4) << 24);
+            constexpr uint32_t kA16 = kAtomBytes >> 4, kB16 = kDAtom >> 4;
             bool ok = true;
             for (int32_t u = u0; u < n_units && ok; u += u_step) {
                 const Unit w = make_unit<kPair>(a, u, rank);
+                TileWalk tw;
+                tw.begin(a, w);
+                // TS: the epilogue stages query rows only for units with tiles
+                if (kTS && !tw.valid()) continue;
                 if constexpr (kPair) {
-                    if (!wait_bar<true>(a, ctl, smem_u32(&ctl->q_ready), q_phase)) break;
+                    if (!wait_bar_warp<true>(a, ctl, smem_u32(&ctl->q_ready), q_phase)) break;
                 } else {
-                    if (!wait_bar(a, ctl, smem_u32(&ctl->q_full), q_phase)) break;
+                    if (!wait_bar_warp(a, ctl, smem_u32(&ctl->q_full), q_phase)) break;
                 }
                 q_phase ^= 1u;
                 tc_fence_after();
-                TileWalk tw;
-                for (tw.begin(a, w); tw.valid() && ok; tw.advance(a)) {
-                    if (!wait_bar<kPair>(a, ctl, smem_u32(&ctl->d_ready[stage]), phase)) { ok = false; break; }
+                for (; tw.valid() && ok; tw.advance(a)) {
+                    if (!wait_bar_warp<kPair>(a, ctl, smem_u32(&ctl->d_ready[stage]), phase)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t idesc = idesc_m | (static_cast<uint32_t>(mma_n(tw.ntok()) >> 3) << 17);
                     const uint64_t b_desc0 = sdesc_k_sw128(smem_u32(sD + stage * d_stage_bytes));
                     for (int32_t k = 0; k < w.mt; ++k) {
-                        if (!wait_bar<kPair>(a, ctl, smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint64_t a_desc0 = q_desc0 + static_cast<uint64_t>((k * q_tile_bytes) >> 4);
-                        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-                        if (a.k_steps == 8) {  // dim 128: fully unrolled
-                            const uint32_t alo = static_cast<uint32_t>(a_desc0), ahi = static_cast<uint32_t>(a_desc0 >> 32);
-                            const uint32_t blo = static_cast<uint32_t>(b_desc0), bhi = static_cast<uint32_t>(b_desc0 >> 32);
-#pragma unroll
-                            for (int s8 = 0; s8 < 8; ++s8) {
-                                const uint32_t oa = static_cast<uint32_t>(((s8 >> 2) * kAtomBytes + (s8 & 3) * 32) >> 4);
-                                const uint32_t ob = static_cast<uint32_t>(((s8 >> 2) * kDAtom + (s8 & 3) * 32) >> 4);
-                                mma_f16_ss_words<kG>(d_tmem, alo + oa, ahi, blo + ob, bhi, idesc, s8 > 0 ? 1u : 0u);
-                            }
-                        } else {
-                            for (int32_t ks = 0; ks < a.k_steps; ++ks) {
-                                const uint64_t oa = static_cast<uint64_t>(((ks >> 2) * kAtomBytes + (ks & 3) * 32) >> 4);
-                                const uint64_t ob = static_cast<uint64_t>(((ks >> 2) * kDAtom + (ks & 3) * 32) >> 4);
-                                mma_f16_ss<kG>(d_tmem, a_desc0 + oa, b_desc0 + ob, idesc, ks > 0 ? 1u : 0u);
-                            }
+                        if (!wait_bar_warp<kPair>(a, ctl, smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u)) {
+                            ok = false;
+                            break;
                         }
-                        mma_commit<kG>(smem_u32(&ctl->acc_full[acc]));
-                        if (++acc == kNAcc) { acc = 0; acc_phase ^= 1u; }
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+                        if constexpr (kTS) {
+                            const uint32_t a_tmem = tmem_base + kQCol0 + static_cast<uint32_t>(k * a.q_cols);
+                            if (a.k_steps == 8) {  // dim 128: one chain
+                                mma_chain8_ts<kG, kB16>(d_tmem, a_tmem, b_desc0, idesc, 0u);
+                            } else {
+                                for (int32_t ks = 0; ks < a.k_steps; ++ks)
+                                    mma_step_ts<kG>(d_tmem, a_tmem + ks * 8, b_desc0 + (ks >> 2) * kB16 + (ks & 3) * 2,
+                                                    idesc, ks > 0 ? 1u : 0u);
+                            }
+                        } else if (a.k_steps == 8) {  // dim 128: one chain
+                            const uint64_t a_desc0 = q_desc0 + static_cast<uint64_t>((k * q_tile_bytes) >> 4);
+                            mma_chain8_ss<kG, kA16, kB16>(d_tmem, a_desc0, b_desc0, idesc, 0u);
+                        } else {
+                            const uint64_t a_desc0 = q_desc0 + static_cast<uint64_t>((k * q_tile_bytes) >> 4);
+                            // 64-element atoms as 4-step chains, then single steps
+                            int32_t ks = 0;
+                            for (; ks + 4 <= a.k_steps; ks += 4)
+                                mma_chain4_ss<kG>(d_tmem, a_desc0 + (ks >> 2) * kA16, b_desc0 + (ks >> 2) * kB16, idesc,
+                                                  ks > 0 ? 1u : 0u);
+                            for (; ks < a.k_steps; ++ks)
+                                mma_step_ss<kG>(d_tmem, a_desc0 + (ks >> 2) * kA16 + (ks & 3) * 2,
+                                                b_desc0 + (ks >> 2) * kB16 + (ks & 3) * 2, idesc, ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit_elect<kG>(smem_u32(&ctl->acc_full[acc]));
+                        if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
                     }
                     if (!ok) break;
-                    mma_commit<kG>(smem_u32(&ctl->d_empty[stage]));
+                    mma_commit_elect<kG>(smem_u32(&ctl->d_empty[stage]));
                     if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit<kG>(smem_u32(&ctl->q_empty));
+                if constexpr (!kTS) mma_commit_elect<kG>(smem_u32(&ctl->q_empty));
             }
             // Drain: wait until every MMA issued above has completed.
-            mma_commit<kG>(smem_u32(&ctl->mma_done), 1);
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(smem_u32(&ctl->mma_done), 0) && global_timer_ns() - t0 < a.timeout_ns) {}
+            mma_commit_elect<kG>(smem_u32(&ctl->mma_done), 1);
+            if (lane == 0) {
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(smem_u32(&ctl->mma_done), 0) && global_timer_ns() - t0 < a.timeout_ns) {}
+            }
+            __syncwarp();
         }
-    } else if (warp < kEpiWarp0) {
+    } else {
         // ------------------------------------------------------------ operand prep
         // f16/bf16: NaN-fill masked / padding rows in place. INT8: convert the
         // staged INT8 tile to f16 rows (NaN for masked / padding rows). In pair
@@ -601,7 +657,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++stage == a.stages) { stage = 0; phase ^= 1u; }
             }
         }
+    }
     } else {
+        regs_claim<kRegsEpi>();
         // ------------------------------------------------------------ epilogue
         // Warpgroup g owns the M-tiles k = g, g + kEpiGroups, ...; each of its
         // threads owns one query row of each of those M-tiles.
@@ -632,6 +690,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 real[q] = in_rb[q] && (a.q_real == nullptr || a.q_real[r] != 0);
                 active[q] = real[q] && (a.q_active == nullptr || a.q_active[r] != 0);
                 qsc[q] = (kInt8 && in_rb[q]) ? a.q_scale[r] : 1.f;
+            }
+            if constexpr (kTS) {
+                // This warpgroup's M-tiles of the block's query rows into
+                // tensor memory, one row per thread (TMEM lane = row, column c
+                // = elements 2c and 2c + 1). Every MMA that read the previous
+                // unit's rows of these M-tiles completed before the last
+                // accumulator this warpgroup drained, so they can be
+                // overwritten. Units without tiles stage nothing (the MMA
+                // warp skips them the same way).
+                TileWalk probe;
+                probe.begin(a, w);
+                if (probe.valid()) {
+                    const int32_t pieces = a.q_cols >> 3;  // 8 columns = 16 values per store
+#pragma unroll
+                    for (int q = 0; q < kKPer; ++q) {
+                        const int k = g + kEpiGroups * q;
+                        if (k >= w.mt) break;
+                        const int32_t r = rb.row0 + k * kBM + e * 32 + lane;
+                        const bool have = r < rb.row_end;
+                        const uint4* src =
+                            reinterpret_cast<const uint4*>(a.q_rows + static_cast<int64_t>(have ? r : 0) * a.dim);
+                        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(e * 32) << 16) + kQCol0 +
+                                               static_cast<uint32_t>(k * a.q_cols);
+                        for (int32_t pc = 0; pc < pieces; ++pc) {
+                            const uint4 x = have ? __ldg(src + 2 * pc) : make_uint4(0u, 0u, 0u, 0u);
+                            const uint4 y = have ? __ldg(src + 2 * pc + 1) : make_uint4(0u, 0u, 0u, 0u);
+                            tmem_st8(taddr + pc * 8, x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w);
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ctl->q_full));
+                }
             }
             // empty documents: score 0 and argmax -1, written up front
             for (int32_t j = w.j0 + et; j < w.j1; j += 32 * kEpiWarps) {
@@ -673,8 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int k = g + kEpiGroups * q;
                     if (k >= w.mt) break;
                     const int64_t idx = buf + k;
-                    const int32_t slot = static_cast<int32_t>(idx % kNAcc);
-                    const uint32_t ph = static_cast<uint32_t>((idx / kNAcc) & 1);
+                    const int32_t slot = static_cast<int32_t>(idx % kAccBufs);
+                    const uint32_t ph = static_cast<uint32_t>((idx / kAccBufs) & 1);
                     if (!wait_bar(a, ctl, smem_u32(&ctl->acc_full[slot]), ph)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(e * 32) << 16) +
@@ -694,31 +786,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         fold_chunk<kArg>(vc, tw.t0 + c * 32, m[q], am[q]);
                     };
-                    float v[2][32];
-                    const int nh = nchunks > 2 ? 2 : 1;
-#pragma unroll 1
-                    for (int h = 0; h < nh; ++h) {
+                    // the whole row of the buffer in one round, so that it is handed back
+                    // to the MMA warp before the reduction
+                    float v[4][32];
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const int cc = 2 * h + c;
-                            if (cc < nfull) {
-                                tmem_ld32(taddr + cc * 32, v[c]);
-                            } else if (cc == nfull && half) {
-                                tmem_ld16(taddr + cc * 32, v[c]);
+                    for (int c = 0; c < 4; ++c) {
+                        if (c < nfull) {
+                            tmem_ld32(taddr + c * 32, v[c]);
+                        } else if (c == nfull && half) {
+                            tmem_ld16(taddr + c * 32, v[c]);
 #pragma unroll
-                                for (int x = 16; x < 32; ++x) v[c][x] = kNaN;
-                            }
+                            for (int x = 16; x < 32; ++x) v[c][x] = kNaN;
                         }
-                        tmem_wait_ld();
-                        if (h == nh - 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) arrive_leader(&ctl->acc_empty[slot]);
-                        }
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            if (2 * h + c < nchunks) fold(v[c], 2 * h + c);
                     }
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) arrive_leader(&ctl->acc_empty[slot]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (c < nchunks) fold(v[c], c);
                     if (closes) {
                         const bool has = m[q] > kNegInf;
                         if (kArg && in_rb[q] && row_s[q] < a.lq_out)

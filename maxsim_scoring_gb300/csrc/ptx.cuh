@@ -30,6 +30,19 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// Move registers between the warpgroups of a CTA: every warp of a
+// warpgroup executes the same call. inc waits until the pool the block was
+// launched with can supply the new count.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_release() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_claim() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -228,6 +241,172 @@ __device__ __forceinline__ void mma_f16_ss_words(uint32_t d_tmem, uint32_t a_lo,
             : "memory");
 }
 
+// MMA chains issued by one elected lane of the calling warp. Every lane of
+// the warp calls them with the same (warp-uniform) arguments; elect.sync with
+// a full mask always picks the same lane, so the chains and the commits that
+// track them come from one thread. Issuing a whole chain from one asm block
+// keeps the tensor pipe fed: one instruction per block would cost more issue
+// cycles than a 128 x 128 x 16 MMA takes to run.
+//
+// A K = 128 chain: eight K = 16 steps into d. A and B are K-major with the
+// 128-byte swizzle; a step advances both descriptors by 32 bytes (2 in the
+// 16-byte address field) and the fifth step moves to the next 64-element
+// atom, kAAtom16 / kBAtom16 (atom bytes >> 4) further on. The first step
+// accumulates into d only if `accumulate` is nonzero.
+#define MAXSIM_CHAIN8(GROUP)                                                               \
+    "{\n\t.reg .pred e, p0, pt;\n\t"                                                      \
+    ".reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n\t"               \
+    "setp.ne.b32 p0, %4, 0;\n\t"                                                          \
+    "setp.eq.b32 pt, %4, %4;\n\t"                                                         \
+    "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"                  \
+    "add.s64 a4, %1, %5;\n\tadd.s64 a5, %1, %6;\n\tadd.s64 a6, %1, %7;\n\tadd.s64 a7, %1, %8;\n\t" \
+    "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"                  \
+    "add.s64 b4, %2, %9;\n\tadd.s64 b5, %2, %10;\n\tadd.s64 b6, %2, %11;\n\tadd.s64 b7, %2, %12;\n\t" \
+    "elect.sync _|e, 0xffffffff;\n\t"                                                     \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], %1, %2, %3, p0;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a1, b1, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a2, b2, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a3, b3, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a4, b4, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a5, b5, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a6, b6, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a7, b7, %3, pt;\n\t}"
+
+template <int kGroup, uint32_t kAAtom16, uint32_t kBAtom16>
+__device__ __forceinline__ void mma_chain8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+    if constexpr (kGroup == 1)
+        asm volatile(MAXSIM_CHAIN8("1")::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(kAAtom16),
+                     "n"(kAAtom16 + 2), "n"(kAAtom16 + 4), "n"(kAAtom16 + 6), "n"(kBAtom16), "n"(kBAtom16 + 2),
+                     "n"(kBAtom16 + 4), "n"(kBAtom16 + 6)
+                     : "memory");
+    else
+        asm volatile(MAXSIM_CHAIN8("2")::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(kAAtom16),
+                     "n"(kAAtom16 + 2), "n"(kAAtom16 + 4), "n"(kAAtom16 + 6), "n"(kBAtom16), "n"(kBAtom16 + 2),
+                     "n"(kBAtom16 + 4), "n"(kBAtom16 + 6)
+                     : "memory");
+}
+#undef MAXSIM_CHAIN8
+
+// A K = 64 chain (one atom, four K = 16 steps), same conventions.
+#define MAXSIM_CHAIN4(GROUP)                                                    \
+    "{\n\t.reg .pred e, p0, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"      \
+    "setp.ne.b32 p0, %4, 0;\n\t"                                               \
+    "setp.eq.b32 pt, %4, %4;\n\t"                                              \
+    "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"       \
+    "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"       \
+    "elect.sync _|e, 0xffffffff;\n\t"                                          \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], %1, %2, %3, p0;\n\t" \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a1, b1, %3, pt;\n\t" \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a2, b2, %3, pt;\n\t" \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], a3, b3, %3, pt;\n\t}"
+
+template <int kGroup>
+__device__ __forceinline__ void mma_chain4_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+    if constexpr (kGroup == 1)
+        asm volatile(MAXSIM_CHAIN4("1")::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+    else
+        asm volatile(MAXSIM_CHAIN4("2")::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+#undef MAXSIM_CHAIN4
+
+// One K = 16 step, same conventions.
+template <int kGroup>
+__device__ __forceinline__ void mma_step_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    if constexpr (kGroup == 1)
+        asm volatile(
+            "{\n\t.reg .pred e, p0;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred e, p0;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p0;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
+// The same chains with A in tensor memory: `a` is the TMEM address of the
+// first K step of A (lane 0, first column); a K = 16 step of f16 / bf16
+// values spans 8 columns. B is the swizzled shared-memory operand as above.
+#define MAXSIM_CHAIN8_TS(GROUP)                                                              \
+    "{\n\t.reg .pred e, p0, pt;\n\t"                                                        \
+    ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t.reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"    \
+    "setp.ne.b32 p0, %4, 0;\n\t"                                                            \
+    "setp.eq.b32 pt, %4, %4;\n\t"                                                           \
+    "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\tadd.u32 a4, %1, 32;\n\t" \
+    "add.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\tadd.u32 a7, %1, 56;\n\t"                 \
+    "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"                    \
+    "add.s64 b4, %2, %5;\n\tadd.s64 b5, %2, %6;\n\tadd.s64 b6, %2, %7;\n\tadd.s64 b7, %2, %8;\n\t" \
+    "elect.sync _|e, 0xffffffff;\n\t"                                                       \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [%1], %2, %3, p0;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], b1, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a2], b2, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a3], b3, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a4], b4, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a5], b5, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a6], b6, %3, pt;\n\t"            \
+    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a7], b7, %3, pt;\n\t}"
+
+template <int kGroup, uint32_t kBAtom16>
+__device__ __forceinline__ void mma_chain8_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+    if constexpr (kGroup == 1)
+        asm volatile(MAXSIM_CHAIN8_TS("1")::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(kBAtom16),
+                     "n"(kBAtom16 + 2), "n"(kBAtom16 + 4), "n"(kBAtom16 + 6)
+                     : "memory");
+    else
+        asm volatile(MAXSIM_CHAIN8_TS("2")::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(kBAtom16),
+                     "n"(kBAtom16 + 2), "n"(kBAtom16 + 4), "n"(kBAtom16 + 6)
+                     : "memory");
+}
+#undef MAXSIM_CHAIN8_TS
+
+template <int kGroup>
+__device__ __forceinline__ void mma_step_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    if constexpr (kGroup == 1)
+        asm volatile(
+            "{\n\t.reg .pred e, p0;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t}" ::"r"(d),
+            "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred e, p0;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p0;\n\t}" ::"r"(d),
+            "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
+// tcgen05.commit from the elected lane (the lane that issued the chains).
+template <int kGroup = 1>
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar, uint16_t cta_mask = 3) {
+    if constexpr (kGroup == 1)
+        asm volatile(
+            "{\n\t.reg .pred e;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred e;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], "
+            "%1;\n\t}" ::"r"(bar),
+            "h"(cta_mask)
+            : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed. kGroup = 2: the arrival goes to the barrier at the same
 // offset in every CTA of the pair selected by cta_mask (bit r = rank r).
@@ -260,6 +439,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+
+// Store 8 consecutive 32-bit columns of this thread's TMEM lane (32x32b
+// shape, same lane rule as the loads); complete with tmem_wait_st.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
+                                         uint32_t r4, uint32_t r5, uint32_t r6, uint32_t r7) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(r4), "r"(r5), "r"(r6), "r"(r7)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[32]) {
