@@ -23,12 +23,16 @@
 //    masked keeps m = -inf.
 //  * For every (tile, M-tile) one MMA chain S = Q_blk * D_tile^T (K = dim)
 //    accumulates in a 128-column TMEM buffer; the epilogue warps read it
-//    with tcgen05.ld while the tensor core fills the next buffer. A single
-//    CTA keeps its query M-tiles in tensor memory as the MMA's A operand
-//    (tcgen05.mma with A in TMEM: only the document tile is read from shared
-//    memory) next to two accumulator buffers; the epilogue warps stage the
-//    rows there at the start of each unit. One elected lane of the MMA warp
-//    issues each K = dim chain from a single asm block.
+//    with tcgen05.ld while the tensor core fills the next buffer. For 16-bit
+//    operands the load itself returns each 32-column chunk's maximum
+//    (tcgen05.ld.red .max), so the running max costs one max per chunk. One
+//    elected lane of an MMA warp issues each K = dim chain from a single asm
+//    block; a single CTA has two MMA warps (M-tiles alternate between them)
+//    so that one issues while the other waits on a barrier.
+//  * The query rows can also sit in tensor memory as the MMA's A operand
+//    (tcgen05.mma with A in TMEM), staged by the epilogue warps; that path
+//    is kept but not selected: it leaves room for only two accumulator
+//    buffers, and the buffer turnaround then bounds the kernel.
 //  * Pair mode (a cluster of two CTAs on two SMs, query rows in shared
 //    memory, four accumulator buffers): the MMA is
 //    tcgen05.mma.cta_group::2 with M = 256, issued by the even CTA. Each CTA
@@ -69,7 +73,7 @@ constexpr int kEpiGroups = 2;     // epilogue warpgroups; group g owns the M-til
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // warp 0 TMA, warp 1 MMA, warps 2-3 prep, then the epilogue
 constexpr int kEpiWarp0 = 4;
-constexpr int kPrepThreads = 64;
+
 constexpr int kAtomBytes = 128 * 128;  // one 128-row x 128-byte swizzled block
 // Registers per thread: the launch gives every thread kRegsLaunch; the
 // producer / MMA / prep warpgroup then hands registers to the two epilogue
@@ -213,23 +217,33 @@ __device__ __forceinline__ Unit make_unit(const FwdArgs& a, int32_t u, uint32_t 
 }
 
 // Walks the tiles of a unit in order: documents j0..j1-1, each cut into tiles
-// of up to kBN of its own tokens; empty documents have no tile.
+// of up to kBN of its own tokens; empty documents have no tile. The offset
+// of the document after next is loaded one document ahead and only clamped
+// when it is promoted, so the load's latency is not waited for at a
+// document boundary.
 struct TileWalk {
-    int32_t j, j1, ds, de, de_next, t0;
+    int32_t j, j1, ds, de, de_next_raw, t0;
+    __device__ __forceinline__ static int32_t raw_start(const FwdArgs& a, int32_t j) {
+        return a.cu_d ? __ldg(a.cu_d + j) : j * a.ld;
+    }
+    __device__ __forceinline__ static int32_t clamp_start(const FwdArgs& a, int32_t v) {
+        // inconsistent offsets (reported separately) stay in bounds
+        return min(max(v, 0), a.total_d);
+    }
     __device__ __forceinline__ void begin(const FwdArgs& a, const Unit& w) {
         j = w.j0;
         j1 = w.j1;
         ds = w.tok0;
         de = j < j1 ? doc_start(a, j + 1) : ds;
-        de_next = j + 1 < j1 ? doc_start(a, j + 2) : de;
+        de_next_raw = raw_start(a, min(j + 2, a.nd));  // promoted only while j + 1 < j1
         t0 = 0;
         skip_empty(a);
     }
     __device__ __forceinline__ void next_doc(const FwdArgs& a) {
         ++j;
         ds = de;
-        de = de_next;
-        de_next = j + 1 < j1 ? doc_start(a, j + 2) : de;
+        de = clamp_start(a, de_next_raw);
+        de_next_raw = raw_start(a, min(j + 2, a.nd));
         t0 = 0;
     }
     __device__ __forceinline__ void skip_empty(const FwdArgs& a) {
@@ -352,6 +366,22 @@ __device__ __forceinline__ void fold_chunk(const float (&y)[32], int32_t col0, f
     }
 }
 
+// Fold one 32-column chunk whose maximum cm is already known (from the TMEM
+// load): only a chunk that beats the running maximum is searched for its
+// lowest column equal to cm.
+__device__ __forceinline__ void fold_chunk_max(const float (&y)[32], float cm, int32_t col0, float& m, int32_t& am) {
+    const bool upd = cm > m;  // false for NaN
+    if (__any_sync(0xFFFFFFFFu, upd)) {
+        int32_t idx = 31;
+#pragma unroll
+        for (int e = 30; e >= 0; --e) idx = (y[e] == cm) ? e : idx;
+        if (upd) {
+            am = col0 + idx;
+            m = cm;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <bool kArg, bool kInt8, bool kPair>
@@ -362,9 +392,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Single CTAs keep the query rows in tensor memory (the MMA's A operand
     // then costs no shared-memory bandwidth) next to two accumulator
     // buffers; CTA pairs keep them in shared memory next to four.
-    constexpr bool kTS = !kPair;
+    constexpr bool kTS = false;
     constexpr int kAccBufs = kTS ? kAccBufsTS : kNAcc;
     constexpr uint32_t kQCol0 = kAccBufs * kBN;    // first TMEM column of Q (TS)
+    // Two MMA warps (1 and 3) share the issue work of a single CTA: M-tiles
+    // k = i, i + 2, ... go to warp i, so that one issues while the other
+    // waits or keeps books. A CTA pair has one issuer and two prep warps.
+    constexpr int kMmaWarps = kPair ? 1 : 2;
+    constexpr int kPrepWarps = 3 - kMmaWarps;
     constexpr int kDRows = kPair ? kBN / 2 : kBN;  // document rows per operand stage in this CTA
     constexpr int kDAtom = kDRows * 128;           // bytes of one 128-byte-wide K block of a stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -404,22 +439,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         const uint32_t ctas = kPair ? 2u : 1u;
         mbar_init(smem_u32(&ctl->q_full), kTS ? kEpiWarps : 1);
-        mbar_init(smem_u32(&ctl->q_empty), 1);
+        mbar_init(smem_u32(&ctl->q_empty), kMmaWarps);
         mbar_init(smem_u32(&ctl->q_ready), ctas);
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(smem_u32(&ctl->d_full[s]), 1);
-            mbar_init(smem_u32(&ctl->d_ready[s]), 2 * ctas);
-            mbar_init(smem_u32(&ctl->d_empty[s]), 1);
+            mbar_init(smem_u32(&ctl->d_ready[s]), kPrepWarps * ctas);
+            mbar_init(smem_u32(&ctl->d_empty[s]), kMmaWarps);
         }
         for (int s = 0; s < a.stages8; ++s) {
             mbar_init(smem_u32(&ctl->d8_full[s]), 1);
-            mbar_init(smem_u32(&ctl->d8_empty[s]), 2);
+            mbar_init(smem_u32(&ctl->d8_empty[s]), kPrepWarps);
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(smem_u32(&ctl->acc_full[b]), 1);
             mbar_init(smem_u32(&ctl->acc_empty[b]), 4 * ctas);
         }
-        mbar_init(smem_u32(&ctl->mma_done), 1);
+        mbar_init(smem_u32(&ctl->mma_done), kMmaWarps);
         mbar_init(smem_u32(&ctl->epi_bar), kEpiWarps);
         ctl->abort = 0;
         fence_barrier_init();
@@ -501,13 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (even CTA of a pair)
-        // The whole warp runs this loop with warp-uniform values; one elected
+    } else if (warp == 1 || (kMmaWarps == 2 && warp == 3)) {
+        // ------------------------------------------------------------ MMA issuers (even CTA of a pair)
+        // Each MMA warp runs this loop with warp-uniform values; one elected
         // lane issues the MMA chains and the commits.
         if (leader) {
-            int32_t stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0, q_phase = 0;
+            const int32_t mi = warp == 1 ? 0 : 1;
+            int32_t stage = 0;
+            int64_t buf = 0;  // global index of the tile's first accumulator buffer use
+            uint32_t phase = 0, q_phase = 0;
             const uint64_t q_desc0 = sdesc_k_sw128(smem_u32(sQ));
             const uint32_t idesc_m = a.idesc | (static_cast<uint32_t>((kPair ? 2 * kBM : kBM) >> 4) << 24);
             constexpr uint32_t kA16 = kAtomBytes >> 4, kB16 = kDAtom >> 4;
@@ -530,7 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t idesc = idesc_m | (static_cast<uint32_t>(mma_n(tw.ntok()) >> 3) << 17);
                     const uint64_t b_desc0 = sdesc_k_sw128(smem_u32(sD + stage * d_stage_bytes));
-                    for (int32_t k = 0; k < w.mt; ++k) {
+                    for (int32_t k = mi; k < w.mt; k += kMmaWarps) {
+                        const int64_t idx = buf + k;
+                        const int32_t acc = static_cast<int32_t>(idx % kAccBufs);
+                        const uint32_t acc_phase = static_cast<uint32_t>((idx / kAccBufs) & 1);
                         if (!wait_bar_warp<kPair>(a, ctl, smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u)) {
                             ok = false;
                             break;
@@ -561,9 +601,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 b_desc0 + (ks >> 2) * kB16 + (ks & 3) * 2, idesc, ks > 0 ? 1u : 0u);
                         }
                         mma_commit_elect<kG>(smem_u32(&ctl->acc_full[acc]));
-                        if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
                     }
                     if (!ok) break;
+                    buf += w.mt;
                     mma_commit_elect<kG>(smem_u32(&ctl->d_empty[stage]));
                     if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 }
@@ -583,7 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // f16/bf16: NaN-fill masked / padding rows in place. INT8: convert the
         // staged INT8 tile to f16 rows (NaN for masked / padding rows). In pair
         // mode each CTA handles its half of the tile's rows.
-        const int pt = threadIdx.x - 64;  // 0..63
+        const int pt = threadIdx.x - 64;  // 0 .. 32 * kPrepWarps - 1
+        constexpr int kPrepThreads = 32 * kPrepWarps;
         int32_t stage = 0, stage8 = 0;
         uint32_t phase = 0, phase8 = 0, q_phase = 0;
         bool ok = true;
@@ -789,23 +830,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the whole row of the buffer in one round, so that it is handed back
                     // to the MMA warp before the reduction
                     float v[4][32];
+                    if constexpr (!kInt8) {
+                        // 16-bit operands: the chunk maxima come out of tensor memory
+                        // with the values (tcgen05.ld.red)
+                        float cm[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c < nfull) {
-                            tmem_ld32(taddr + c * 32, v[c]);
-                        } else if (c == nfull && half) {
-                            tmem_ld16(taddr + c * 32, v[c]);
+                        for (int c = 0; c < 4; ++c) {
+                            cm[c] = kNegInf;
+                            if (c < nfull) {
+                                cm[c] = tmem_ldmax32(taddr + c * 32, v[c]);
+                            } else if (c == nfull && half) {
+                                cm[c] = tmem_ldmax16(taddr + c * 32, v[c]);
 #pragma unroll
-                            for (int x = 16; x < 32; ++x) v[c][x] = kNaN;
+                                for (int x = 16; x < 32; ++x) v[c][x] = kNaN;
+                            }
                         }
-                    }
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) arrive_leader(&ctl->acc_empty[slot]);
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) arrive_leader(&ctl->acc_empty[slot]);
+                        if constexpr (!kArg) {
+                            m[q] = fmax3(m[q], fmax3(cm[0], cm[1], cm[2]), cm[3]);
+                        } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (c < nchunks) fold(v[c], c);
+                            for (int c = 0; c < 4; ++c)
+                                if (c < nchunks) fold_chunk_max(v[c], cm[c], tw.t0 + c * 32, m[q], am[q]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            if (c < nfull) {
+                                tmem_ld32(taddr + c * 32, v[c]);
+                            } else if (c == nfull && half) {
+                                tmem_ld16(taddr + c * 32, v[c]);
+#pragma unroll
+                                for (int x = 16; x < 32; ++x) v[c][x] = kNaN;
+                            }
+                        }
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) arrive_leader(&ctl->acc_empty[slot]);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (c < nchunks) fold(v[c], c);
+                    }
                     if (closes) {
                         const bool has = m[q] > kNegInf;
                         if (kArg && in_rb[q] && row_s[q] < a.lq_out)

@@ -164,7 +164,7 @@ FwdPlan plan_fwd_mode(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varl
     FwdPlan p;
     p.int8 = int8;
     p.pair = pair;
-    p.ts = !pair;
+    p.ts = false;
     p.lq_pad = pad_lq(lq);
     p.k_atoms = static_cast<int32_t>((dim + 63) / 64);
     p.k8_atoms = int8 ? static_cast<int32_t>((dim + 127) / 128) : 0;

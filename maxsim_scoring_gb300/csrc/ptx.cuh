@@ -462,6 +462,38 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[32]) {
         : "r"(taddr));
 }
 
+// 32 (or 16) consecutive fp32 columns of this thread's TMEM lane, and their
+// maximum computed on the way out of tensor memory (tcgen05.ld.red, .max:
+// NaN columns are ignored as by max.f32; all-NaN gives NaN).
+#define MAXSIM_R32 \
+    "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}"
+__device__ __forceinline__ float tmem_ldmax32(uint32_t taddr, float (&v)[32]) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    float m;
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 " MAXSIM_R32 ", %32, [%33];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=f"(m)
+                 : "r"(taddr));
+    return m;
+}
+#undef MAXSIM_R32
+
+__device__ __forceinline__ float tmem_ldmax16(uint32_t taddr, float (&v)[32]) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    float m;
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=f"(m)
+        : "r"(taddr));
+    return m;
+}
+
 // ---------------------------------------------------------------- INT8 -> f16
 
 // Eight signed bytes (w0: elements 0-3, w1: elements 4-7, little-endian) to
