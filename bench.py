@@ -115,8 +115,7 @@ def kernel_source_hash() -> str:
 # profiles/maxsim_fwd_kernel_pair_int8__int8_rerank.md); valid only for the
 # kernel sources whose hash is recorded with it.
 MEASURED_TRAFFIC = {
-    ("colbert_varlen", "ee56a13d550698fe"): 4345643108,  # (428.94 + 3.82) MB x 16,644,526 / 1,657,544 tokens
-    ("int8_rerank", "ee56a13d550698fe"): 1369128960,     # (270.70 + 3.13) MB x 10,000 / 2,000 documents
+    ("colbert_varlen", "2fa4a0496781f598"): 4356116017,  # (429.57 + 4.23) MB x 16,644,526 / 1,657,544 tokens
 }
 
 

@@ -29,10 +29,6 @@
 //    elected lane of an MMA warp issues each K = dim chain from a single asm
 //    block; a single CTA has two MMA warps (M-tiles alternate between them)
 //    so that one issues while the other waits on a barrier.
-//  * The query rows can also sit in tensor memory as the MMA's A operand
-//    (tcgen05.mma with A in TMEM), staged by the epilogue warps; that path
-//    is kept but not selected: it leaves room for only two accumulator
-//    buffers, and the buffer turnaround then bounds the kernel.
 //  * Pair mode (a cluster of two CTAs on two SMs, query rows in shared
 //    memory, four accumulator buffers): the MMA is
 //    tcgen05.mma.cta_group::2 with M = 256, issued by the even CTA. Each CTA
@@ -68,7 +64,6 @@ constexpr int kBN = 128;          // document tokens per tile (largest MMA N)
 constexpr int kBM = 128;          // query rows per M-tile (MMA M)
 constexpr int kMaxMT = 4;         // M-tiles per row block
 constexpr int kNAcc = 4;          // TMEM accumulator buffers (4 x 128 columns)
-constexpr int kAccBufsTS = 2;     // ... when the query rows share TMEM with them (two 128-column slots left for Q)
 constexpr int kEpiGroups = 2;     // epilogue warpgroups; group g owns the M-tiles k with k % 2 == g
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // warp 0 TMA, warp 1 MMA, warps 2-3 prep, then the epilogue
@@ -119,9 +114,7 @@ struct FwdArgs {
     int32_t dim;
     int32_t stages;       // operand ring depth
     int32_t stages8;      // INT8 staging ring depth (INT8 mode)
-    int32_t q_slots;      // M-tiles of Q resident in shared memory (0: Q lives in tensor memory)
-    const uint16_t* q_rows;  // padded 16-bit query rows [R, dim] (read directly when Q lives in TMEM)
-    int32_t q_cols;       // TMEM columns of one M-tile of Q (dim / 2)
+    int32_t q_slots;      // M-tiles of Q resident in shared memory
     int32_t n_pr;         // pair mode: row-block pairs (ceil(n_rb / 2))
     uint32_t idesc;       // tcgen05 instruction descriptor without N
     uint32_t nan_pair;    // two 16-bit NaNs of the operand type
@@ -392,9 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Single CTAs keep the query rows in tensor memory (the MMA's A operand
     // then costs no shared-memory bandwidth) next to two accumulator
     // buffers; CTA pairs keep them in shared memory next to four.
-    constexpr bool kTS = false;
-    constexpr int kAccBufs = kTS ? kAccBufsTS : kNAcc;
-    constexpr uint32_t kQCol0 = kAccBufs * kBN;    // first TMEM column of Q (TS)
+    constexpr int kAccBufs = kNAcc;
     // Two MMA warps (1 and 3) share the issue work of a single CTA: M-tiles
     // k = i, i + 2, ... go to warp i, so that one issues while the other
     // waits or keeps books. A CTA pair has one issuer and two prep warps.
@@ -429,16 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Ring depths index fixed-size barrier arrays: refuse a launch that breaks
     // them (both CTAs of a pair see the same arguments and return together).
     if (a.stages < 1 || a.stages > kMaxStages || (kInt8 && (a.stages8 < 1 || a.stages8 > kMaxStages)) ||
-        (kTS ? (a.q_slots != 0 || a.q_cols < 8 ||
-                kQCol0 + ((a.rb_rows + kBM - 1) / kBM) * a.q_cols > static_cast<uint32_t>(kNAcc * kBN))
-             : (a.q_slots < 1 || a.q_slots > kMaxMT))) {
+        a.q_slots < 1 || a.q_slots > kMaxMT) {
         if (threadIdx.x == 0) record_status(a, kStatusBadInput);
         return;
     }
 
     if (threadIdx.x == 0) {
         const uint32_t ctas = kPair ? 2u : 1u;
-        mbar_init(smem_u32(&ctl->q_full), kTS ? kEpiWarps : 1);
+        mbar_init(smem_u32(&ctl->q_full), 1);
         mbar_init(smem_u32(&ctl->q_empty), kMmaWarps);
         mbar_init(smem_u32(&ctl->q_ready), ctas);
         for (int s = 0; s < a.stages; ++s) {
@@ -495,19 +484,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int32_t u = u0; u < n_units && ok; u += u_step) {
                 const Unit w = make_unit<kPair>(a, u, rank);
-                if constexpr (!kTS) {
-                    if (!first_unit) {
-                        if (!wait_bar(a, ctl, smem_u32(&ctl->q_empty), q_phase)) break;
-                        q_phase ^= 1u;
-                    }
-                    first_unit = false;
-                    const uint32_t qbar = smem_u32(&ctl->q_full);
-                    mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(w.mt * q_tile_bytes));
-                    for (int32_t k = 0; k < w.mt; ++k)
-                        for (int32_t ka = 0; ka < a.k_atoms; ++ka)
-                            tma_load_2d(smem_u32(sQ + k * q_tile_bytes + ka * kAtomBytes), &tm_q, qbar, ka * 64,
-                                        w.rb.row0 + k * kBM);
+                if (!first_unit) {
+                    if (!wait_bar(a, ctl, smem_u32(&ctl->q_empty), q_phase)) break;
+                    q_phase ^= 1u;
                 }
+                first_unit = false;
+                const uint32_t qbar = smem_u32(&ctl->q_full);
+                mbar_arrive_expect_tx(qbar, static_cast<uint32_t>(w.mt * q_tile_bytes));
+                for (int32_t k = 0; k < w.mt; ++k)
+                    for (int32_t ka = 0; ka < a.k_atoms; ++ka)
+                        tma_load_2d(smem_u32(sQ + k * q_tile_bytes + ka * kAtomBytes), &tm_q, qbar, ka * 64,
+                                    w.rb.row0 + k * kBM);
                 TileWalk tw;
                 for (tw.begin(a, w); tw.valid(); tw.advance(a)) {
                     const uint32_t empty = smem_u32(kInt8 ? &ctl->d8_empty[stage] : &ctl->d_empty[stage]);
@@ -553,8 +540,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit w = make_unit<kPair>(a, u, rank);
                 TileWalk tw;
                 tw.begin(a, w);
-                // TS: the epilogue stages query rows only for units with tiles
-                if (kTS && !tw.valid()) continue;
                 if constexpr (kPair) {
                     if (!wait_bar_warp<true>(a, ctl, smem_u32(&ctl->q_ready), q_phase)) break;
                 } else {
@@ -577,16 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-                        if constexpr (kTS) {
-                            const uint32_t a_tmem = tmem_base + kQCol0 + static_cast<uint32_t>(k * a.q_cols);
-                            if (a.k_steps == 8) {  // dim 128: one chain
-                                mma_chain8_ts<kG, kB16>(d_tmem, a_tmem, b_desc0, idesc, 0u);
-                            } else {
-                                for (int32_t ks = 0; ks < a.k_steps; ++ks)
-                                    mma_step_ts<kG>(d_tmem, a_tmem + ks * 8, b_desc0 + (ks >> 2) * kB16 + (ks & 3) * 2,
-                                                    idesc, ks > 0 ? 1u : 0u);
-                            }
-                        } else if (a.k_steps == 8) {  // dim 128: one chain
+                        if (a.k_steps == 8) {  // dim 128: one chain
                             const uint64_t a_desc0 = q_desc0 + static_cast<uint64_t>((k * q_tile_bytes) >> 4);
                             mma_chain8_ss<kG, kA16, kB16>(d_tmem, a_desc0, b_desc0, idesc, 0u);
                         } else {
@@ -608,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (++stage == a.stages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                if constexpr (!kTS) mma_commit_elect<kG>(smem_u32(&ctl->q_empty));
+                mma_commit_elect<kG>(smem_u32(&ctl->q_empty));
             }
             // Drain: wait until every MMA issued above has completed.
             mma_commit_elect<kG>(smem_u32(&ctl->mma_done), 1);
@@ -731,40 +707,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 real[q] = in_rb[q] && (a.q_real == nullptr || a.q_real[r] != 0);
                 active[q] = real[q] && (a.q_active == nullptr || a.q_active[r] != 0);
                 qsc[q] = (kInt8 && in_rb[q]) ? a.q_scale[r] : 1.f;
-            }
-            if constexpr (kTS) {
-                // This warpgroup's M-tiles of the block's query rows into
-                // tensor memory, one row per thread (TMEM lane = row, column c
-                // = elements 2c and 2c + 1). Every MMA that read the previous
-                // unit's rows of these M-tiles completed before the last
-                // accumulator this warpgroup drained, so they can be
-                // overwritten. Units without tiles stage nothing (the MMA
-                // warp skips them the same way).
-                TileWalk probe;
-                probe.begin(a, w);
-                if (probe.valid()) {
-                    const int32_t pieces = a.q_cols >> 3;  // 8 columns = 16 values per store
-#pragma unroll
-                    for (int q = 0; q < kKPer; ++q) {
-                        const int k = g + kEpiGroups * q;
-                        if (k >= w.mt) break;
-                        const int32_t r = rb.row0 + k * kBM + e * 32 + lane;
-                        const bool have = r < rb.row_end;
-                        const uint4* src =
-                            reinterpret_cast<const uint4*>(a.q_rows + static_cast<int64_t>(have ? r : 0) * a.dim);
-                        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(e * 32) << 16) + kQCol0 +
-                                               static_cast<uint32_t>(k * a.q_cols);
-                        for (int32_t pc = 0; pc < pieces; ++pc) {
-                            const uint4 x = have ? __ldg(src + 2 * pc) : make_uint4(0u, 0u, 0u, 0u);
-                            const uint4 y = have ? __ldg(src + 2 * pc + 1) : make_uint4(0u, 0u, 0u, 0u);
-                            tmem_st8(taddr + pc * 8, x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w);
-                        }
-                    }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctl->q_full));
-                }
             }
             // empty documents: score 0 and argmax -1, written up front
             for (int32_t j = w.j0 + et; j < w.j1; j += 32 * kEpiWarps) {

@@ -103,7 +103,6 @@ struct FwdPlan {
     int64_t rows = 0;  // padded query rows
     bool repack = false, int8 = false, ok = false;
     bool pair = false;   // two-CTA clusters (each CTA loads half of every document tile)
-    bool ts = false;     // query rows in tensor memory (single CTAs); else in shared memory
     int64_t n_pr = 0;    // row-block pairs
     size_t smem = 0;
     size_t off_q = 0, off_real = 0, off_active = 0, off_qscale = 0, off_partial = 0, ws_bytes = 0;
@@ -118,10 +117,9 @@ inline int64_t pad_lq(int64_t lq) {
     return (lq + 31) / 32 * 32;
 }
 
-size_t fwd_smem_bytes(int32_t mt, int32_t k_atoms, int32_t stages, int32_t k8_atoms, int32_t stages8, bool pair,
-                      bool ts) {
+size_t fwd_smem_bytes(int32_t mt, int32_t k_atoms, int32_t stages, int32_t k8_atoms, int32_t stages8, bool pair) {
     const size_t d_atom = static_cast<size_t>(pair ? kBN / 2 : kBN) * 128;
-    const size_t q_bytes = ts ? 0 : static_cast<size_t>(mt) * k_atoms * kAtomBytes;
+    const size_t q_bytes = static_cast<size_t>(mt) * k_atoms * kAtomBytes;
     size_t b = 1024 + q_bytes + static_cast<size_t>(stages) * k_atoms * d_atom + sizeof(SmemCtl);
     if (stages8 > 0) b += static_cast<size_t>(stages8) * k8_atoms * d_atom + kDScaleBytes;
     return b;
@@ -132,28 +130,24 @@ size_t fwd_smem_bytes(int32_t mt, int32_t k_atoms, int32_t stages, int32_t k8_at
 // stages when it can; wide INT8 rows fall back to one). Returns false when
 // nothing fits; the entry points then reject the shape.
 bool choose_pipeline(FwdPlan& p) {
-    // TS: the query M-tiles, dim / 2 columns each, share tensor memory with
-    // the accumulator buffers.
-    const int32_t mt_top =
-        p.ts ? std::min<int32_t>(kMaxMT, (kNAcc - kAccBufsTS) * kBN / std::max(8, p.k_steps * 8)) : kMaxMT;
     for (int32_t min_stages = 2; min_stages >= 1; --min_stages) {
-        for (int32_t mt = mt_top; mt >= 1; --mt) {
+        for (int32_t mt = kMaxMT; mt >= 1; --mt) {
             if (!p.int8) {
-                if (min_stages < 2 || fwd_smem_bytes(mt, p.k_atoms, 2, 0, 0, p.pair, p.ts) > kSmemBudget) continue;
+                if (min_stages < 2 || fwd_smem_bytes(mt, p.k_atoms, 2, 0, 0, p.pair) > kSmemBudget) continue;
                 int32_t s = kMaxStages;
-                while (fwd_smem_bytes(mt, p.k_atoms, s, 0, 0, p.pair, p.ts) > kSmemBudget) --s;
+                while (fwd_smem_bytes(mt, p.k_atoms, s, 0, 0, p.pair) > kSmemBudget) --s;
                 p.mt_max = mt;
                 p.stages = s;
                 p.stages8 = 0;
             } else {
-                if (fwd_smem_bytes(mt, p.k_atoms, min_stages, p.k8_atoms, 2, p.pair, p.ts) > kSmemBudget) continue;
+                if (fwd_smem_bytes(mt, p.k_atoms, min_stages, p.k8_atoms, 2, p.pair) > kSmemBudget) continue;
                 int32_t s8 = kMaxStages;
-                while (fwd_smem_bytes(mt, p.k_atoms, min_stages, p.k8_atoms, s8, p.pair, p.ts) > kSmemBudget) --s8;
+                while (fwd_smem_bytes(mt, p.k_atoms, min_stages, p.k8_atoms, s8, p.pair) > kSmemBudget) --s8;
                 p.mt_max = mt;
                 p.stages = min_stages;
                 p.stages8 = s8;
             }
-            p.smem = fwd_smem_bytes(p.mt_max, p.k_atoms, p.stages, p.k8_atoms, p.stages8, p.pair, p.ts);
+            p.smem = fwd_smem_bytes(p.mt_max, p.k_atoms, p.stages, p.k8_atoms, p.stages8, p.pair);
             return true;
         }
     }
@@ -164,7 +158,6 @@ FwdPlan plan_fwd_mode(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varl
     FwdPlan p;
     p.int8 = int8;
     p.pair = pair;
-    p.ts = false;
     p.lq_pad = pad_lq(lq);
     p.k_atoms = static_cast<int32_t>((dim + 63) / 64);
     p.k8_atoms = int8 ? static_cast<int32_t>((dim + 127) / 128) : 0;
@@ -424,9 +417,7 @@ maxsim_status run_fwd(DeviceInfo* dev, const FwdPlan& p, const FwdCall& c, uint8
     a.dim = static_cast<int32_t>(c.dim);
     a.stages = p.stages;
     a.stages8 = p.stages8;
-    a.q_slots = p.ts ? 0 : p.mt_max;
-    a.q_rows = static_cast<const uint16_t*>(c.q_rows);
-    a.q_cols = static_cast<int32_t>(p.k_steps * 8);
+    a.q_slots = p.mt_max;
     a.idesc = idesc_f16_f32(c.ab_format, 0, 0);  // M and N are filled in on the device
     a.nan_pair = c.nan_pair;
     a.status = dev->status;

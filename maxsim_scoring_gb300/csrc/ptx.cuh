@@ -332,62 +332,6 @@ __device__ __forceinline__ void mma_step_ss(uint32_t d, uint64_t a, uint64_t b, 
             : "memory");
 }
 
-// The same chains with A in tensor memory: `a` is the TMEM address of the
-// first K step of A (lane 0, first column); a K = 16 step of f16 / bf16
-// values spans 8 columns. B is the swizzled shared-memory operand as above.
-#define MAXSIM_CHAIN8_TS(GROUP)                                                              \
-    "{\n\t.reg .pred e, p0, pt;\n\t"                                                        \
-    ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t.reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"    \
-    "setp.ne.b32 p0, %4, 0;\n\t"                                                            \
-    "setp.eq.b32 pt, %4, %4;\n\t"                                                           \
-    "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\tadd.u32 a4, %1, 32;\n\t" \
-    "add.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\tadd.u32 a7, %1, 56;\n\t"                 \
-    "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"                    \
-    "add.s64 b4, %2, %5;\n\tadd.s64 b5, %2, %6;\n\tadd.s64 b6, %2, %7;\n\tadd.s64 b7, %2, %8;\n\t" \
-    "elect.sync _|e, 0xffffffff;\n\t"                                                       \
-    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [%1], %2, %3, p0;\n\t"            \
-    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], b1, %3, pt;\n\t"            \
-    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a2], b2, %3, pt;\n\t"            \
-    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a3], b3, %3, pt;\n\t"            \
-    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a4], b4, %3, pt;\n\t"            \
-    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a5], b5, %3, pt;\n\t"            \
-    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a6], b6, %3, pt;\n\t"            \
-    "@e tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a7], b7, %3, pt;\n\t}"
-
-template <int kGroup, uint32_t kBAtom16>
-__device__ __forceinline__ void mma_chain8_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
-                                              uint32_t accumulate) {
-    if constexpr (kGroup == 1)
-        asm volatile(MAXSIM_CHAIN8_TS("1")::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(kBAtom16),
-                     "n"(kBAtom16 + 2), "n"(kBAtom16 + 4), "n"(kBAtom16 + 6)
-                     : "memory");
-    else
-        asm volatile(MAXSIM_CHAIN8_TS("2")::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(kBAtom16),
-                     "n"(kBAtom16 + 2), "n"(kBAtom16 + 4), "n"(kBAtom16 + 6)
-                     : "memory");
-}
-#undef MAXSIM_CHAIN8_TS
-
-template <int kGroup>
-__device__ __forceinline__ void mma_step_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
-    if constexpr (kGroup == 1)
-        asm volatile(
-            "{\n\t.reg .pred e, p0;\n\t"
-            "setp.ne.b32 p0, %4, 0;\n\t"
-            "elect.sync _|e, 0xffffffff;\n\t"
-            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t}" ::"r"(d),
-            "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
-            : "memory");
-    else
-        asm volatile(
-            "{\n\t.reg .pred e, p0;\n\t"
-            "setp.ne.b32 p0, %4, 0;\n\t"
-            "elect.sync _|e, 0xffffffff;\n\t"
-            "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p0;\n\t}" ::"r"(d),
-            "r"(a), "l"(b), "r"(idesc), "r"(accumulate)
-            : "memory");
-}
-
 // tcgen05.commit from the elected lane (the lane that issued the chains).
 template <int kGroup = 1>
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar, uint16_t cta_mask = 3) {
@@ -439,17 +383,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
-
-// Store 8 consecutive 32-bit columns of this thread's TMEM lane (32x32b
-// shape, same lane rule as the loads); complete with tmem_wait_st.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
-                                         uint32_t r4, uint32_t r5, uint32_t r6, uint32_t r7) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-                 "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(r4), "r"(r5), "r"(r6), "r"(r7)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[32]) {
