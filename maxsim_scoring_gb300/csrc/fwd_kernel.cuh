@@ -728,8 +728,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < kKPer; ++q) { m[q] = kNegInf; am[q] = -1; }
 
+            // INT8: this lane's document scales (columns c * 32 + lane) of the
+            // next tile, loaded one tile ahead
+            float sc_next[4];
+            auto load_scales = [&](const TileWalk& t) {
+                const int32_t tn = t.ntok(), trow = t.row();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int32_t col = c * 32 + lane;
+                    sc_next[c] = col < tn ? __ldg(a.d_scale + trow + col) : 0.f;
+                }
+            };
             TileWalk tw;
-            for (tw.begin(a, w); tw.valid() && ok; tw.advance(a)) {
+            tw.begin(a, w);
+            if (kInt8 && tw.valid()) load_scales(tw);
+            for (; tw.valid() && ok; tw.advance(a)) {
                 const int32_t n = tw.ntok(), N = mma_n(n);
                 const int32_t nfull = N >> 5;
                 const bool half = (N & 31) != 0;
@@ -737,11 +750,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool closes = tw.last_of_doc();
                 if constexpr (kInt8) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int32_t t = c * 32 + lane;
-                        dscale[ew * kBN + t] = t < n ? __ldg(a.d_scale + tw.row() + t) : 0.f;
-                    }
+                    for (int c = 0; c < 4; ++c) dscale[ew * kBN + c * 32 + lane] = sc_next[c];
                     __syncwarp();
+                    TileWalk nx = tw;
+                    nx.advance(a);
+                    if (nx.valid()) load_scales(nx);
                 }
 #pragma unroll
                 for (int q = 0; q < kKPer; ++q) {
@@ -761,10 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int x = 0; x < 8; ++x) {
                                 const float4 s4 = sc[x];
-                                vc[4 * x + 0] *= s4.x;
-                                vc[4 * x + 1] *= s4.y;
-                                vc[4 * x + 2] *= s4.z;
-                                vc[4 * x + 3] *= s4.w;
+                                mul2_rn(vc[4 * x + 0], vc[4 * x + 1], s4.x, s4.y);
+                                mul2_rn(vc[4 * x + 2], vc[4 * x + 3], s4.z, s4.w);
                             }
                         }
                         fold_chunk<kArg>(vc, tw.t0 + c * 32, m[q], am[q]);

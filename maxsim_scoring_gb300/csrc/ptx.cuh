@@ -43,6 +43,18 @@ __device__ __forceinline__ void regs_claim() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
+// (x0, x1) *= (s0, s1) with one packed instruction (mul.rn.f32x2: each lane
+// rounded as a plain fp32 multiply).
+__device__ __forceinline__ void mul2_rn(float& x0, float& x1, float s0, float s1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "f"(s0), "f"(s1));
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
