@@ -12,7 +12,8 @@
  * Conventions shared by every entry point
  *  - All tensor pointers are DEVICE pointers owned by the caller. Tensors are
  *    contiguous and row-major with the embedding dimension innermost. Q, D,
- *    and scale pointers must be 16-byte aligned; row strides are dim elements.
+ *    scale and gradient (dQ, dD) pointers must be 16-byte aligned; row
+ *    strides are dim elements.
  *  - Masks are one byte per token, nonzero = active. A masked document token
  *    is set to -inf before the max; a masked query token contributes 0 to the
  *    sum (design notes, "Problem" and "Mask handling").

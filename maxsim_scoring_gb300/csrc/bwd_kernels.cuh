@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(256) csr_count_kernel(const BwdArgs b) {
     const int32_t nsrc = b.nq * b.lq;
     int32_t cnt = 0;
     bool bad = false;
+#pragma unroll 8
     for (int32_t n = threadIdx.x; n < nsrc; n += blockDim.x) {
         int32_t a = b.argmax[src_index(b, j, n)];
         if (a >= 0 && a < b.ld) ++cnt;
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(256) csr_build_kernel(const BwdArgs b, int32_t
     __syncthreads();
     if (warp < nw) {
         const int32_t n0 = warp * per, n1 = min(n0 + per, nsrc);
+#pragma unroll 4
         for (int32_t n = n0 + lane; n < n1; n += 32) {
             int32_t a = b.argmax[src_index(b, j, n)];
             if (a >= 0 && a < b.ld) atomicAdd(&hist[warp * b.ld + a], 1);
@@ -133,17 +135,29 @@ __global__ void __launch_bounds__(256) csr_build_kernel(const BwdArgs b, int32_t
     int32_t local = 0;
     for (int32_t t = t0; t < t1; ++t)
         for (int32_t w = 0; w < nw; ++w) local += hist[w * b.ld + t];
-    part[threadIdx.x] = local;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int32_t run = 0;
-        for (int x = 0; x < static_cast<int>(blockDim.x); ++x) {
-            int32_t v = part[x];
-            part[x] = run;
-            run += v;
+    // exclusive scan of the per-thread totals across the block (warp scans,
+    // then a scan of the warp totals)
+    {
+        int32_t x = local;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
         }
+        __shared__ int32_t wsum[8];
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t w = lane < static_cast<int>(blockDim.x >> 5) ? wsum[lane] : 0;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+                if (lane >= o) w += y;
+            }
+            if (lane < 8) wsum[lane] = w;  // inclusive
+        }
+        __syncthreads();
+        part[threadIdx.x] = (warp > 0 ? wsum[warp - 1] : 0) + x - local;
+        __syncthreads();
     }
-    __syncthreads();
     int32_t run = b.doc_base[j] + part[threadIdx.x];
     for (int32_t t = t0; t < t1; ++t) {
         b.row_ptr[static_cast<int64_t>(j) * b.ld + t] = run;
@@ -179,8 +193,67 @@ __global__ void __launch_bounds__(256) csr_build_kernel(const BwdArgs b, int32_t
     }
 }
 
-// dD: one warp per destination row (j, t); lanes split the embedding.
-template <int kVec>  // floats per lane (dim / 32)
+// One embedding row into this lane's kVec consecutive elements (lane * kVec
+// + v) as fp32; whole-vector loads when the row is exactly 32 * kVec wide.
+template <int kVec>
+__device__ __forceinline__ void load_row(const uint16_t* __restrict__ row, int lane, int32_t dim, int32_t is_bf16,
+                                         float (&x)[kVec]) {
+    const int k0 = lane * kVec;
+    if constexpr (kVec == 2 || kVec == 4 || kVec == 8) {
+        if (dim == 32 * kVec) {
+            uint32_t w[kVec / 2];
+            if constexpr (kVec == 2) {
+                w[0] = __ldg(reinterpret_cast<const uint32_t*>(row + k0));
+            } else if constexpr (kVec == 4) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(row + k0));
+                w[0] = u.x;
+                w[1] = u.y;
+            } else {
+                const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + k0));
+                w[0] = u.x;
+                w[1] = u.y;
+                w[2] = u.z;
+                w[3] = u.w;
+            }
+#pragma unroll
+            for (int h = 0; h < kVec / 2; ++h) {
+                x[2 * h] = bits_to_f32(static_cast<uint16_t>(w[h] & 0xFFFFu), is_bf16);
+                x[2 * h + 1] = bits_to_f32(static_cast<uint16_t>(w[h] >> 16), is_bf16);
+            }
+            return;
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+        const int k = k0 + v;
+        x[v] = k < dim ? bits_to_f32(row[k], is_bf16) : 0.f;
+    }
+}
+
+template <int kVec>
+__device__ __forceinline__ void store_row(float* __restrict__ out, int lane, int32_t dim, const float (&acc)[kVec]) {
+    const int k0 = lane * kVec;
+    if constexpr (kVec == 4) {
+        if (dim == 128) {
+            *reinterpret_cast<float4*>(out + k0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            return;
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+        const int k = k0 + v;
+        if (k < dim) out[k] = acc[v];
+    }
+}
+
+// Rows gathered per batch: their loads are issued together so that their
+// latencies overlap; the accumulation order is unchanged.
+constexpr int kGather = 4;
+
+// dD: one warp per destination row (j, t); lanes split the embedding. The
+// row's sources are taken 32 at a time: each lane decodes one (index, weight),
+// then the warp walks them in CSR order.
+template <int kVec>  // floats per lane (dim / 32, rounded up)
 __global__ void __launch_bounds__(256) dd_kernel(const BwdArgs b) {
     const int lane = threadIdx.x & 31;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -191,28 +264,42 @@ __global__ void __launch_bounds__(256) dd_kernel(const BwdArgs b) {
 #pragma unroll
     for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
     const int32_t e0 = b.row_ptr[r], e1 = b.row_ptr[r + 1];
-    for (int32_t e = e0; e < e1; ++e) {
-        const int32_t p = b.col[e];
-        const int32_t s = p % b.lq;
-        const int32_t i = (p / b.lq) / b.nd;
-        float w = b.g[static_cast<int64_t>(i) * b.nd + j];
-        if (b.q_mask && !b.q_mask[static_cast<int64_t>(i) * b.lq + s]) w = 0.f;
-        const uint16_t* qrow = b.Q + (static_cast<int64_t>(i) * b.lq + s) * b.dim;
+    for (int32_t eb = e0; eb < e1; eb += 32) {
+        const int32_t cnt = min(32, e1 - eb);
+        int64_t off = 0;  // element offset of this lane's source row in Q
+        float wl = 0.f;
+        if (lane < cnt) {
+            const int32_t p = b.col[eb + lane];
+            const int32_t s = p % b.lq;
+            const int32_t i = (p / b.lq) / b.nd;
+            wl = b.g[static_cast<int64_t>(i) * b.nd + j];
+            if (b.q_mask && !b.q_mask[static_cast<int64_t>(i) * b.lq + s]) wl = 0.f;
+            off = (static_cast<int64_t>(i) * b.lq + s) * b.dim;
+        }
+        for (int32_t k = 0; k < cnt; k += kGather) {
+            float x[kGather][kVec];
+            float w[kGather];
 #pragma unroll
-        for (int v = 0; v < kVec; ++v) {
-            const int k = lane * kVec + v;
-            if (k < b.dim) acc[v] = fmaf(w, bits_to_f32(qrow[k], b.is_bf16), acc[v]);
+            for (int u = 0; u < kGather; ++u) {
+                const int32_t src = min(k + u, cnt - 1);
+                w[u] = __shfl_sync(0xFFFFFFFFu, wl, src);
+                const int64_t o = __shfl_sync(0xFFFFFFFFu, off, src);
+                load_row<kVec>(b.Q + o, lane, b.dim, b.is_bf16, x[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kGather; ++u) {
+                if (k + u < cnt) {
+#pragma unroll
+                    for (int v = 0; v < kVec; ++v) acc[v] = fmaf(w[u], x[u][v], acc[v]);
+                }
+            }
         }
     }
-    float* out = b.dD + r * b.dim;
-#pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-        const int k = lane * kVec + v;
-        if (k < b.dim) out[k] = acc[v];
-    }
+    store_row<kVec>(b.dD + r * b.dim, lane, b.dim, acc);
 }
 
-// dQ: one warp per query row (i, s), ascending j.
+// dQ: one warp per query row (i, s), ascending j. The winners and weights of
+// 32 documents are loaded at once, one per lane.
 template <int kVec>
 __global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b) {
     const int lane = threadIdx.x & 31;
@@ -224,24 +311,47 @@ __global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b) {
     float acc[kVec];
 #pragma unroll
     for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
-    for (int32_t j = 0; j < b.nd; ++j) {
-        const int32_t a = b.argmax[(static_cast<int64_t>(i) * b.nd + j) * b.lq + s];
-        if (a < 0 || a >= b.ld) continue;
-        const float w = b.g[static_cast<int64_t>(i) * b.nd + j];
-        const uint16_t* drow = b.D + (static_cast<int64_t>(j) * b.ld + a) * b.dim;
+    for (int32_t jb = 0; jb < b.nd; jb += 32) {
+        const int32_t cnt = min(32, b.nd - jb);
+        int64_t off = 0;
+        float wl = 0.f;  // 0 for a document without a winner (argmax -1)
+        if (lane < cnt) {
+            const int32_t j = jb + lane;
+            const int32_t a = b.argmax[(static_cast<int64_t>(i) * b.nd + j) * b.lq + s];
+            if (a >= 0 && a < b.ld) {
+                wl = b.g[static_cast<int64_t>(i) * b.nd + j];
+                off = (static_cast<int64_t>(j) * b.ld + a) * b.dim;
+            } else {
+                off = -1;
+            }
+        }
+        for (int32_t k = 0; k < cnt; k += kGather) {
+            float x[kGather][kVec];
+            float w[kGather];
+            bool use[kGather];
 #pragma unroll
-        for (int v = 0; v < kVec; ++v) {
-            const int k = lane * kVec + v;
-            if (k < b.dim) acc[v] = fmaf(w, bits_to_f32(drow[k], b.is_bf16), acc[v]);
+            for (int u = 0; u < kGather; ++u) {
+                const int32_t src = min(k + u, cnt - 1);
+                w[u] = __shfl_sync(0xFFFFFFFFu, wl, src);
+                const int64_t o = __shfl_sync(0xFFFFFFFFu, off, src);
+                use[u] = k + u < cnt && o >= 0;
+                load_row<kVec>(b.D + (o >= 0 ? o : 0), lane, b.dim, b.is_bf16, x[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kGather; ++u) {
+                if (use[u]) {
+#pragma unroll
+                    for (int v = 0; v < kVec; ++v) acc[v] = fmaf(w[u], x[u][v], acc[v]);
+                }
+            }
         }
     }
     const bool active = b.q_mask == nullptr || b.q_mask[r] != 0;
-    float* out = b.dQ + r * b.dim;
+    if (!active) {
 #pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-        const int k = lane * kVec + v;
-        if (k < b.dim) out[k] = active ? acc[v] : 0.f;
+        for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
     }
+    store_row<kVec>(b.dQ + r * b.dim, lane, b.dim, acc);
 }
 
 }  // namespace maxsim

@@ -639,8 +639,11 @@ maxsim_status maxsim_bwd(const void* Q, const void* D, maxsim_dtype dtype, int64
     const bool need_csr = dD || csr_row_ptr || csr_col;
     if (need_csr || dQ) {
         if (!argmax || !grad_scores) return MAXSIM_ERR_INVALID_ARG;
-        if ((Nq * Lq > 0 && !Q) || (Nd * Ld > 0 && !D)) return MAXSIM_ERR_INVALID_ARG;
+        if ((Nq * Lq > 0 && (!Q || !aligned16(Q))) || (Nd * Ld > 0 && (!D || !aligned16(D))))
+            return MAXSIM_ERR_INVALID_ARG;
     }
+    // the gradient rows are written as whole vectors
+    if ((dQ && !aligned16(dQ)) || (dD && !aligned16(dD))) return MAXSIM_ERR_INVALID_ARG;
     size_t off = 0;
     const size_t off_cnt = off;
     off = round_up(off + static_cast<size_t>(Nd) * 4, 256);
