@@ -217,6 +217,12 @@ def describe(w, spec):
                 f"Ld~U[{spec['ld_min']},{spec['ld_max']}] (sum Ld={w['total_d']}), d={w['dim']}, f16, "
                 f"l2-normalised Gaussian rows, seed {spec['seed']}")
         d_bytes = w["total_d"] * w["dim"] * 2
+    elif name == "colbert_pairs":
+        text = (f"colbert_pairs: Nq={w['Nq']} queries x Lq={w['Lq']} tokens, {w['num_pairs']} (query, document) "
+                f"pairs ({spec['pairs_per_query']} per query, documents uniform) over Nd={w['Nd']} packed docs, "
+                f"Ld~U[{spec['ld_min']},{spec['ld_max']}], d={w['dim']}, f16, l2-normalised Gaussian rows, "
+                f"seed {spec['seed']}")
+        d_bytes = w["total_d"] * w["dim"] * 2
     elif name == "int8_rerank":
         text = (f"int8_rerank: Q int8 [{w['Nq']},{w['Lq']},{w['dim']}] (query rows in 512-row chunks), "
                 f"D int8 [{w['Nd']},{w['Ld']},{w['dim']}], per-token f32 scales of l2-normalised Gaussian rows, "
@@ -229,7 +235,7 @@ def describe(w, spec):
                 f"{masks} l2-normalised Gaussian rows, seed {spec['seed']}")
         d_bytes = w["Nd"] * w["Ld"] * w["dim"] * 2
     cfg = {"workload": text}
-    for k in ("Nq", "Lq", "Nd", "Ld", "total_d", "dim"):
+    for k in ("Nq", "Lq", "Nd", "Ld", "total_d", "num_pairs", "dim"):
         if k in w:
             cfg[k] = w[k]
     cfg["l2"] = ("inputs larger than L2 (D alone is %.2f GB); no flush needed" % (d_bytes / 1e9)
@@ -240,13 +246,26 @@ def describe(w, spec):
 
 # ---------------------------------------------------------------- the oracle arm
 
+def units_of(w) -> int:
+    """Documents scored per step: every (query, document) pair of a pair list."""
+    return w["num_pairs"] if "num_pairs" in w else w["Nd"]
+
+
 def time_oracle(w, n_docs: int, threads: int = 0):
-    """Oracle docs/s on the first n_docs documents (a bounded sample)."""
+    """Oracle docs/s on the first n_docs documents (pairs, for a pair list) -
+    a bounded sample."""
     import oracle
     docs = np.arange(n_docs, dtype=np.int64)
     t0 = time.perf_counter()
     name = w["name"]
-    if name == "colbert_varlen":
+    if name == "colbert_pairs":
+        pr = w["pairs"][:n_docs]
+        for i in np.unique(pr[:, 0]):
+            rows = w["Q"][i].reshape(-1, w["dim"])
+            oracle.fwd_packed(rows, np.array([0, w["Lq"]], dtype=np.int64), w["D"],
+                              w["cu_seqlens_d"].astype(np.int64), "f16", docs=pr[pr[:, 0] == i, 1].astype(np.int64),
+                              threads=threads)
+    elif name == "colbert_varlen":
         q_off = np.arange(w["Nq"] + 1, dtype=np.int64) * w["Lq"]
         oracle.fwd_packed(w["Q"].reshape(-1, w["dim"]), q_off, w["D"], w["cu_seqlens_d"].astype(np.int64), "f16",
                           docs=docs, threads=threads)
@@ -262,9 +281,9 @@ def time_oracle(w, n_docs: int, threads: int = 0):
 
 
 def calibrated_sample(w, target_s: float):
-    probe = min(8, w["Nd"])
+    probe = min(8, units_of(w))
     rate, _ = time_oracle(w, probe)
-    return int(max(probe, min(w["Nd"], rate * target_s)))
+    return int(max(probe, min(units_of(w), rate * target_s)))
 
 
 def run_reference(args, rank, world):
@@ -281,7 +300,8 @@ def run_reference(args, rank, world):
         _, dt = time_oracle(w, n)
         times.append(dt)
     value = n * args.steps / sum(times)
-    sample = f"first {n} of {w['Nd']} documents per step, all {w['Nq']} queries"
+    sample = (f"first {n} of {w['num_pairs']} pairs per step" if "num_pairs" in w else
+              f"first {n} of {w['Nd']} documents per step, all {w['Nq']} queries")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
@@ -320,16 +340,17 @@ class Case:
         else:
             dt = t.float16 if w["dtype"] == "f16" else t.bfloat16
             self.h_in["Q"], self.h_in["D"] = pinned_half(w["Q"], dt), pinned_half(w["D"], dt)
-            for k in ("cu_seqlens_d", "q_mask", "d_mask", "grad"):
+            for k in ("cu_seqlens_d", "q_mask", "d_mask", "grad", "pairs"):
                 if w.get(k) is not None:
                     self.h_in[k] = pinned(w[k])
         for k, v in self.h_in.items():
             self.d_in[k] = v.to(device)
         self.e2e_in = {k: t.empty_like(v) for k, v in self.d_in.items()}
         Nq, Nd, dim = w["Nq"], w["Nd"], w["dim"]
-        self.scores = t.empty((Nq, Nd), dtype=t.float32, device=device)
-        self.h_scores = t.empty((Nq, Nd), dtype=t.float32).pin_memory()
-        self.units = Nd
+        out_shape = (w["num_pairs"],) if name == "colbert_pairs" else (Nq, Nd)
+        self.scores = t.empty(out_shape, dtype=t.float32, device=device)
+        self.h_scores = t.empty(out_shape, dtype=t.float32).pin_memory()
+        self.units = units_of(w)
         self.argmax = None
         if name == "colbert_varlen":
             Lq, T = w["Lq"], w["total_d"]
@@ -337,6 +358,15 @@ class Case:
             self.flops = maxsim_flops(Nq * Lq, dim, T)
             self.bytes = varlen_algorithmic_bytes(Nq, Lq, dim, T, Nd)
             self.bound, self.dtype, self.launches = "tensor", "f16", 3
+        elif name == "colbert_pairs":
+            Lq, T, n = w["Lq"], w["total_d"], w["num_pairs"]
+            ws = ops.workspace_size(_native.OP_SCORE_PAIRS, Nq, Lq, Nd, n, dim)
+            lens = np.diff(w["cu_seqlens_d"].astype(np.int64))
+            tokens = int(lens[w["pairs"][:, 1]].sum())  # every pair streams its document
+            self.flops = maxsim_flops(Lq, dim, tokens)
+            # per pair: its document's rows, the pair, two offsets, the score; plus Q
+            self.bytes = tokens * dim * 2 + n * (8 + 8 + 4) + Nq * Lq * dim * 2
+            self.bound, self.dtype, self.launches = "hbm", "f16", 6
         elif name == "int8_rerank":
             Lq, Ld = w["Lq"], w["Ld"]
             ws = ops.workspace_size(_native.OP_FWD_INT8, Nq, Lq, Nd, Ld, dim)
@@ -375,6 +405,9 @@ class Case:
         if name == "colbert_varlen":
             ops.maxsim_fwd_varlen(d["Q"], None, w["Lq"], d["D"], d["cu_seqlens_d"], scores=self.scores,
                                   workspace=self.ws)
+        elif name == "colbert_pairs":
+            ops.maxsim_score_pairs_packed(d["Q"], None, w["Lq"], d["D"], d["cu_seqlens_d"], d["pairs"],
+                                          scores=self.scores, workspace=self.ws)
         elif name == "int8_rerank":
             ops.maxsim_fwd_int8(d["Q"], d["q_scale"], d["D"], d["d_scale"], scores=self.scores, workspace=self.ws)
         elif name == "contrastive_bwd":
@@ -511,8 +544,10 @@ def run_ours(args, rank, world, local_rank):
         import oracle
         n = calibrated_sample(w, target_s=args.cpu_seconds)
         rate, dt = time_oracle(w, n)
+        what = (f"first {n} of {w['num_pairs']} pairs" if "num_pairs" in w else
+                f"first {n} of {w['Nd']} documents, all {w['Nq']} queries")
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-                                "sample": f"first {n} of {w['Nd']} documents, all {w['Nq']} queries ({dt:.1f} s)"}
+                                "sample": f"{what} ({dt:.1f} s)"}
     print(json.dumps(line), flush=True)
 
 

@@ -15,13 +15,16 @@ generators in this package.
                   N(0,1), seed 4
  int8_rerank      Q int8 [1,1024,128] + scales, D int8 [10000,1024,128] + scales,
                   seed 5
+ colbert_pairs    the colbert_varlen corpus and queries with 10,000 (query,
+                  document) pairs per query, documents uniform over the corpus
+                  (a reranker's candidate lists), seed 2
 Every row is an l2-normalised Gaussian vector rounded once to its storage type.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import (TID_D, TID_DMASK, TID_GRAD, TID_LEN_D, TID_Q, TID_QMASK, gaussian_rows, int8_rows,
+from . import (TID_D, TID_DMASK, TID_GRAD, TID_LEN_D, TID_PAIR_D, TID_Q, TID_QMASK, gaussian_rows, int8_rows,
                mask_drop_tail, mask_random_subset, normal_f32, uniform_int)
 
 SPECS = {
@@ -31,6 +34,8 @@ SPECS = {
                           q_drop_max=40, d_hide_max=200),
     "contrastive_bwd": dict(Nq=64, Lq=128, Nd=64, Ld=1024, dim=128, dtype="bf16", seed=4),
     "int8_rerank": dict(Nq=1, Lq=1024, Nd=10_000, Ld=1024, dim=128, seed=5),
+    "colbert_pairs": dict(Nq=32, Lq=32, Nd=100_000, ld_min=32, ld_max=300, dim=128, dtype="f16", seed=2,
+                          pairs_per_query=10_000),
 }
 
 
@@ -61,6 +66,17 @@ def varlen(Nq, Lq, Nd, ld_min, ld_max, dim, dtype, seed):
     return w
 
 
+def pairs(Nq, Lq, Nd, ld_min, ld_max, dim, dtype, seed, pairs_per_query):
+    """The varlen corpus plus int32 pairs [Nq * pairs_per_query, 2]: query i
+    owns rows i * pairs_per_query ..., each naming a uniform random document."""
+    w = varlen(Nq, Lq, Nd, ld_min, ld_max, dim, dtype, seed)
+    n = Nq * pairs_per_query
+    docs = uniform_int(seed, TID_PAIR_D, n, 0, Nd - 1) if n else np.zeros(0, np.int32)
+    w["pairs"] = np.stack([np.repeat(np.arange(Nq, dtype=np.int32), pairs_per_query), docs], axis=1)
+    w["num_pairs"] = n
+    return w
+
+
 def int8(Nq, Lq, Nd, Ld, dim, seed):
     """INT8 Q/D with one float32 scale per token (per-token symmetric)."""
     w = dict(Nq=Nq, Lq=Lq, Nd=Nd, Ld=Ld, dim=dim, seed=seed)
@@ -77,6 +93,8 @@ def make(name: str, **overrides):
     spec.update(overrides)
     if name == "colbert_varlen":
         return varlen(**spec)
+    if name == "colbert_pairs":
+        return pairs(**spec)
     if name == "int8_rerank":
         return int8(**spec)
     grad = name == "contrastive_bwd"

@@ -57,7 +57,8 @@ typedef enum {
 typedef enum { MAXSIM_F16 = 0, MAXSIM_BF16 = 1 } maxsim_dtype;
 
 /* Operation codes for maxsim_workspace_size(). */
-enum { MAXSIM_OP_FWD = 0, MAXSIM_OP_FWD_VARLEN = 1, MAXSIM_OP_BWD = 2, MAXSIM_OP_FWD_INT8 = 3 };
+enum { MAXSIM_OP_FWD = 0, MAXSIM_OP_FWD_VARLEN = 1, MAXSIM_OP_BWD = 2, MAXSIM_OP_FWD_INT8 = 3,
+       MAXSIM_OP_SCORE_PAIRS = 4 };
 
 /*
  * Dense forward.
@@ -104,6 +105,33 @@ maxsim_status maxsim_fwd_varlen(const void *Q, const int32_t *cu_seqlens_q, int6
                                 const uint8_t *q_mask, const uint8_t *d_mask,
                                 float *scores, int32_t *argmax,
                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Forward for an arbitrary list of (query, document) pairs of the packed
+ * batches of maxsim_fwd_varlen, output [num_pairs] instead of [Nq, Nd]
+ * (design notes, "Varlen / packed path": score_pairs_packed; for pair lists
+ * sparse relative to Nq x Nd, as in reranker scheduling).
+ *   Q, cu_seqlens_q, max_lq, D, cu_seqlens_d, total_d, dtype, Nq, Nd, dim,
+ *   q_mask, d_mask   as for maxsim_fwd_varlen
+ *   pairs      [num_pairs, 2] i32, pairs[p] = (query index, document index)
+ *   scores     [num_pairs] f32 (out): the score of pair p
+ *   argmax     [num_pairs, max_lq] i32 (out, optional), layout as a row of
+ *              maxsim_fwd_varlen's argmax
+ * The pairs are grouped by query on the device; every pair streams its own
+ * document, so a document named by several pairs is read once per pair.
+ * Results per pair equal maxsim_fwd_varlen's entry (i, j). A pair with an
+ * index outside [0, Nq) x [0, Nd) scores 0 (argmax row -1) and is reported as
+ * MAXSIM_ERR_DEVICE_INPUT by maxsim_device_status(). Queries up to 512 tokens
+ * (at dim <= 128; MAXSIM_ERR_UNSUPPORTED beyond). Workspace:
+ * maxsim_workspace_size(MAXSIM_OP_SCORE_PAIRS, Nq, max_lq, Nd, num_pairs, dim).
+ */
+maxsim_status maxsim_score_pairs_packed(const void *Q, const int32_t *cu_seqlens_q, int64_t max_lq,
+                                        const void *D, const int32_t *cu_seqlens_d, int64_t total_d,
+                                        maxsim_dtype dtype, int64_t Nq, int64_t Nd, int64_t dim,
+                                        const uint8_t *q_mask, const uint8_t *d_mask,
+                                        const int32_t *pairs, int64_t num_pairs,
+                                        float *scores, int32_t *argmax,
+                                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Backward through the saved argmax ("Flash-MaxSim" Sec. 4.2, Eqs. (2)-(3);
@@ -162,6 +190,7 @@ maxsim_status maxsim_fwd_int8(const int8_t *Q, const float *q_scale,
  *                                      packed Q (an upper bound for dense Q)
  *   MAXSIM_OP_BWD:                     (Nq, Lq, Nd, Ld, dim); assumes the CSR
  *                                      outputs are NULL (an upper bound)
+ *   MAXSIM_OP_SCORE_PAIRS:             (Nq, max_lq, Nd, num_pairs, dim)
  * Returns (size_t)-1 for an invalid shape.
  */
 size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim);

@@ -25,7 +25,7 @@ STATUS = {
     6: "MAXSIM_ERR_DEVICE_INPUT",
 }
 
-OP_FWD, OP_FWD_VARLEN, OP_BWD, OP_FWD_INT8 = 0, 1, 2, 3
+OP_FWD, OP_FWD_VARLEN, OP_BWD, OP_FWD_INT8, OP_SCORE_PAIRS = 0, 1, 2, 3, 4
 F16, BF16 = 0, 1
 
 # Every symbol the header declares, with its ctypes signature.
@@ -40,6 +40,8 @@ SIGNATURES = {
                              _VP]),
     "maxsim_fwd_varlen_noalloc": (_I, [_VP, _VP, _I64, _VP, _VP, _I64, _I, _I64, _I64, _I64, _VP, _VP, _VP, _VP,
                                        _VP]),
+    "maxsim_score_pairs_packed": (_I, [_VP, _VP, _I64, _VP, _VP, _I64, _I, _I64, _I64, _I64, _VP, _VP, _VP, _I64,
+                                       _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_workspace_size": (_SZ, [_I, _I64, _I64, _I64, _I64, _I64]),
     "maxsim_status_string": (ctypes.c_char_p, [_I]),
     "maxsim_device_status": (_I, [_VP]),

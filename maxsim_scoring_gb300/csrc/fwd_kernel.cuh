@@ -103,6 +103,13 @@ struct FwdArgs {
     const float* d_scale;    // [total_d] INT8 mode: per-token document scale
     int32_t n_dr;         // document ranges
     int32_t n_units;      // n_rb * n_dr
+    // pair-list mode (score_pairs_packed): a unit is one query and a run of
+    // its (query, document) pairs; NULL pr_sorted = the [Nq, Nd] grid
+    const int32_t* pr_pairs;   // [num_pairs, 2] (query index, document index)
+    const int32_t* pr_sorted;  // [num_pairs] pair indices grouped by query
+    const int32_t* pr_qptr;    // [nq + 1] first grouped position of each query's pairs
+    const int32_t* pr_uptr;    // [nq + 1] first unit of each query; pr_uptr[nq] = number of units
+    int32_t pr_chunk;          // pairs per unit
     // outputs
     float* scores;        // [nq, nd]
     float* partial;       // [n_chunks, nq, nd] when n_chunks > 1
@@ -199,6 +206,27 @@ __device__ __forceinline__ Unit make_unit(const FwdArgs& a, int32_t u, uint32_t 
         w.rb = row_block(a, 2 * pr + static_cast<int32_t>(rank));
         w.mt = max(w.rb.mt, row_block(a, 2 * pr + 1 - static_cast<int32_t>(rank)).mt);
     } else {
+        if (a.pr_sorted) {
+            // query i owns units pr_uptr[i] .. pr_uptr[i+1]-1: the last i with pr_uptr[i] <= u
+            int32_t lo = 0, hi = a.nq - 1;
+            while (lo < hi) {
+                const int32_t mid = (lo + hi + 1) >> 1;
+                if (__ldg(a.pr_uptr + mid) <= u) lo = mid; else hi = mid - 1;
+            }
+            const int32_t i = lo;
+            const int32_t k0 = __ldg(a.pr_qptr + i) + (u - __ldg(a.pr_uptr + i)) * a.pr_chunk;
+            w.rb.q0 = i;
+            w.rb.nqb = 1;
+            w.rb.chunk = 0;
+            w.rb.row0 = i * a.lq_pad;
+            w.rb.row_end = w.rb.row0 + a.lq_pad;
+            w.rb.mt = (a.lq_pad + kBM - 1) / kBM;
+            w.mt = w.rb.mt;
+            w.j0 = k0;
+            w.j1 = min(k0 + a.pr_chunk, __ldg(a.pr_qptr + i + 1));
+            w.tok0 = 0;
+            return w;
+        }
         w.rb = row_block(a, u % a.n_rb);
         w.mt = w.rb.mt;
         dr = u / a.n_rb;
@@ -209,13 +237,21 @@ __device__ __forceinline__ Unit make_unit(const FwdArgs& a, int32_t u, uint32_t 
     return w;
 }
 
-// Walks the tiles of a unit in order: documents j0..j1-1, each cut into tiles
-// of up to kBN of its own tokens; empty documents have no tile. The offset
-// of the document after next is loaded one document ahead and only clamped
-// when it is promoted, so the load's latency is not waited for at a
-// document boundary.
+// Output index of (query i, document position oj): the [Nq, Nd] grid, or in
+// pair-list mode the pair index itself.
+__device__ __forceinline__ int64_t out_index(const FwdArgs& a, int32_t i, int32_t oj) {
+    return a.pr_sorted ? static_cast<int64_t>(oj) : static_cast<int64_t>(i) * a.nd + oj;
+}
+
+// Walks the tiles of a unit in order: documents j0..j1-1 (in pair-list mode
+// the documents of grouped pairs j0..j1-1), each cut into tiles of up to kBN
+// of its own tokens; empty documents have no tile. The bounds of the next
+// document are loaded one document ahead and only clamped when they are
+// used, so the loads' latency is not waited for at a document boundary.
 struct TileWalk {
-    int32_t j, j1, ds, de, de_next_raw, t0;
+    int32_t j, j1, ds, de, t0;
+    int32_t oj;                    // output column of document j (pair index in pair-list mode)
+    int32_t nx_oj, nx_s, nx_e;     // raw bounds of the next document (nx_s unused on the grid)
     __device__ __forceinline__ static int32_t raw_start(const FwdArgs& a, int32_t j) {
         return a.cu_d ? __ldg(a.cu_d + j) : j * a.ld;
     }
@@ -223,21 +259,48 @@ struct TileWalk {
         // inconsistent offsets (reported separately) stay in bounds
         return min(max(v, 0), a.total_d);
     }
+    // pair-list mode: pair, and raw token range of its document, at grouped position k
+    __device__ __forceinline__ void load_pair(const FwdArgs& a, int32_t k, int32_t& p, int32_t& s0, int32_t& e0) const {
+        p = __ldg(a.pr_sorted + k);
+        const int32_t doc = __ldg(a.pr_pairs + 2 * p + 1);
+        s0 = __ldg(a.cu_d + doc);
+        e0 = __ldg(a.cu_d + doc + 1);
+    }
     __device__ __forceinline__ void begin(const FwdArgs& a, const Unit& w) {
         j = w.j0;
         j1 = w.j1;
-        ds = w.tok0;
-        de = j < j1 ? doc_start(a, j + 1) : ds;
-        de_next_raw = raw_start(a, min(j + 2, a.nd));  // promoted only while j + 1 < j1
         t0 = 0;
+        if (!a.pr_sorted) {
+            ds = w.tok0;
+            de = j < j1 ? doc_start(a, j + 1) : ds;
+            oj = j;
+            nx_e = raw_start(a, min(j + 2, a.nd));  // promoted only while j + 1 < j1
+        } else if (j < j1) {
+            int32_t s0, e0;
+            load_pair(a, j, oj, s0, e0);
+            ds = clamp_start(a, s0);
+            de = max(ds, clamp_start(a, e0));
+            load_pair(a, min(j + 1, j1 - 1), nx_oj, nx_s, nx_e);
+        } else {
+            ds = de = 0;
+            oj = 0;
+        }
         skip_empty(a);
     }
     __device__ __forceinline__ void next_doc(const FwdArgs& a) {
         ++j;
-        ds = de;
-        de = clamp_start(a, de_next_raw);
-        de_next_raw = raw_start(a, min(j + 2, a.nd));
         t0 = 0;
+        if (!a.pr_sorted) {
+            ds = de;
+            de = clamp_start(a, nx_e);
+            oj = j;
+            nx_e = raw_start(a, min(j + 2, a.nd));
+        } else {
+            oj = nx_oj;
+            ds = clamp_start(a, nx_s);
+            de = max(ds, clamp_start(a, nx_e));
+            load_pair(a, min(j + 1, j1 - 1), nx_oj, nx_s, nx_e);
+        }
     }
     __device__ __forceinline__ void skip_empty(const FwdArgs& a) {
         while (j < j1 && de <= ds) next_doc(a);
@@ -459,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (kPair) cluster_sync_all();  // barriers of both CTAs exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
-    const int32_t n_units = a.n_units;
+    const int32_t n_units = a.pr_sorted ? __ldg(a.pr_uptr + a.nq) : a.n_units;
     const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
     const int32_t u_step = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
 
@@ -709,7 +772,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 qsc[q] = (kInt8 && in_rb[q]) ? a.q_scale[r] : 1.f;
             }
             // empty documents: score 0 and argmax -1, written up front
-            for (int32_t j = w.j0 + et; j < w.j1; j += 32 * kEpiWarps) {
+            for (int32_t j = w.j0 + et; j < w.j1 && a.pr_sorted; j += 32 * kEpiWarps) {
+                const int32_t p = __ldg(a.pr_sorted + j);
+                const int32_t doc = __ldg(a.pr_pairs + 2 * p + 1);
+                if (__ldg(a.cu_d + doc + 1) > __ldg(a.cu_d + doc)) continue;
+                a.scores[p] = 0.f;
+                if (kArg)
+                    for (int32_t s = 0; s < a.lq_out; ++s) a.argmax[static_cast<int64_t>(p) * a.lq_out + s] = -1;
+            }
+            for (int32_t j = w.j0 + et; j < w.j1 && !a.pr_sorted; j += 32 * kEpiWarps) {
                 if (doc_start(a, j + 1) > doc_start(a, j)) continue;
                 for (int32_t q = 0; q < rb.nqb; ++q) {
                     const int32_t i = rb.q0 + q;
@@ -831,21 +902,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (closes) {
                         const bool has = m[q] > kNegInf;
                         if (kArg && in_rb[q] && row_s[q] < a.lq_out)
-                            a.argmax[(static_cast<int64_t>(row_i[q]) * a.nd + tw.j) * a.lq_out + row_s[q]] =
+                            a.argmax[out_index(a, row_i[q], tw.oj) * a.lq_out + row_s[q]] =
                                 (real[q] && has) ? am[q] : -1;
                         float val = (active[q] && has) ? m[q] * qsc[q] : 0.f;
                         if (a.lq_pad >= 32) {
 #pragma unroll
                             for (int o = 16; o > 0; o >>= 1) val += __shfl_xor_sync(0xFFFFFFFFu, val, o);
                             if (a.lq_pad == 32 && !chunked) {
-                                if (lane == 0 && in_rb[q]) a.scores[static_cast<int64_t>(row_i[q]) * a.nd + tw.j] = val;
+                                if (lane == 0 && in_rb[q]) a.scores[out_index(a, row_i[q], tw.oj)] = val;
                             } else if (lane == 0) {
                                 ctl->wslot[k * 4 + e] = val;
                             }
                         } else {
                             for (int o = a.lq_pad >> 1; o > 0; o >>= 1) val += __shfl_xor_sync(0xFFFFFFFFu, val, o);
                             if (in_rb[q] && (lane & (a.lq_pad - 1)) == 0)
-                                a.scores[static_cast<int64_t>(row_i[q]) * a.nd + tw.j] = val;
+                                a.scores[out_index(a, row_i[q], tw.oj)] = val;
                         }
                         m[q] = kNegInf;
                         am[q] = -1;
@@ -862,8 +933,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float sum = 0.f;
                         for (int32_t ww = wb; ww < we; ++ww) sum += ctl->wslot[ww];
                         const int32_t i = rb.q0 + et;
-                        if (chunked) a.partial[(static_cast<int64_t>(rb.chunk) * a.nq + i) * a.nd + tw.j] = sum;
-                        else a.scores[static_cast<int64_t>(i) * a.nd + tw.j] = sum;
+                        if (chunked) a.partial[(static_cast<int64_t>(rb.chunk) * a.nq + i) * a.nd + tw.oj] = sum;
+                        else a.scores[out_index(a, i, tw.oj)] = sum;
                     }
                     if (!epi_sync(a, ctl, epi_phase)) { ok = false; break; }
                 }

@@ -363,6 +363,12 @@ struct FwdCall {
     const uint8_t* d_mask;
     float* scores;
     int32_t* argmax;
+    // pair-list mode (score_pairs_packed), else all NULL / 0
+    const int32_t* pr_pairs;
+    const int32_t* pr_sorted;
+    const int32_t* pr_qptr;
+    const int32_t* pr_uptr;
+    int32_t pr_chunk;
 };
 
 maxsim_status run_fwd(DeviceInfo* dev, const FwdPlan& p, const FwdCall& c, uint8_t* ws, cudaStream_t st) {
@@ -424,7 +430,15 @@ maxsim_status run_fwd(DeviceInfo* dev, const FwdPlan& p, const FwdCall& c, uint8
     a.timeout_ns = kTimeoutNs;
     // One CTA per SM: the request always exceeds half of an SM's shared memory.
     const size_t smem = std::max<size_t>(p.smem, kSmemBudget / 2 + 1024);
-    const int grid = p.pair ? 2 * static_cast<int>(std::min<int64_t>(a.n_units, workers))
+    a.pr_pairs = c.pr_pairs;
+    a.pr_sorted = c.pr_sorted;
+    a.pr_qptr = c.pr_qptr;
+    a.pr_uptr = c.pr_uptr;
+    a.pr_chunk = c.pr_chunk;
+    if (c.pr_sorted && p.pair) return MAXSIM_ERR_UNSUPPORTED;
+    // pair-list mode: the unit count is known on the device only; every SM runs
+    const int grid = c.pr_sorted ? workers
+                   : p.pair ? 2 * static_cast<int>(std::min<int64_t>(a.n_units, workers))
                             : static_cast<int>(std::min<int64_t>(a.n_units, workers));
 
     maxsim_status rc;
@@ -446,6 +460,117 @@ maxsim_status run_fwd(DeviceInfo* dev, const FwdPlan& p, const FwdCall& c, uint8
         if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
     }
     return MAXSIM_OK;
+}
+
+// ---------------------------------------------------------------- pair lists
+
+// Valid pairs counted per query; a pair outside [0, Nq) x [0, Nd) scores 0,
+// its argmax row is -1, and it is reported on the device status word.
+__global__ void pairs_count_kernel(const int32_t* __restrict__ pairs, int64_t np, int64_t nq, int64_t nd,
+                                   int32_t* __restrict__ qcnt, float* __restrict__ scores, int32_t* __restrict__ argmax,
+                                   int64_t lq_out, int* status) {
+    for (int64_t p = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; p < np;
+         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int32_t q = pairs[2 * p], d = pairs[2 * p + 1];
+        if (q >= 0 && q < nq && d >= 0 && d < nd) {
+            atomicAdd(qcnt + q, 1);
+        } else {
+            scores[p] = 0.f;
+            if (argmax)
+                for (int64_t s = 0; s < lq_out; ++s) argmax[p * lq_out + s] = -1;
+            atomicCAS(status, 0, kStatusBadInput);
+        }
+    }
+}
+
+// One block: exclusive prefix sums over the queries of their pair counts
+// (qptr, also copied to the placement cursors) and of their unit counts
+// ceil(count / chunk) (uptr); qptr[nq] and uptr[nq] hold the totals.
+__global__ void __launch_bounds__(1024) pairs_scan_kernel(const int32_t* __restrict__ qcnt, int64_t nq, int32_t chunk,
+                                                          int32_t* __restrict__ qptr, int32_t* __restrict__ uptr,
+                                                          int32_t* __restrict__ cursor) {
+    __shared__ int32_t wsum[2][32];
+    __shared__ int32_t carry[2];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry[0] = carry[1] = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < nq; base += blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        const int32_t c = i < nq ? qcnt[i] : 0;
+        int32_t v[2] = {c, (c + chunk - 1) / chunk};
+        int32_t x[2] = {v[0], v[1]};
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x[h], o);
+                if (lane >= o) x[h] += y;
+            }
+        if (lane == 31) { wsum[0][warp] = x[0]; wsum[1][warp] = x[1]; }
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                int32_t w = lane < static_cast<int>(blockDim.x >> 5) ? wsum[h][lane] : 0;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+                    if (lane >= o) w += y;
+                }
+                wsum[h][lane] = w;  // inclusive
+            }
+        }
+        __syncthreads();
+        int32_t ex[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) ex[h] = carry[h] + (warp > 0 ? wsum[h][warp - 1] : 0) + x[h] - v[h];
+        if (i < nq) {
+            qptr[i] = ex[0];
+            cursor[i] = ex[0];
+            uptr[i] = ex[1];
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) {
+            carry[0] = ex[0] + v[0];
+            carry[1] = ex[1] + v[1];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        qptr[nq] = carry[0];
+        uptr[nq] = carry[1];
+    }
+}
+
+// Each valid pair to the next free slot of its query. The order inside a
+// query's group is free: every pair is scored on its own.
+__global__ void pairs_place_kernel(const int32_t* __restrict__ pairs, int64_t np, int64_t nq, int64_t nd,
+                                   int32_t* __restrict__ cursor, int32_t* __restrict__ sorted) {
+    for (int64_t p = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; p < np;
+         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int32_t q = pairs[2 * p], d = pairs[2 * p + 1];
+        if (q >= 0 && q < nq && d >= 0 && d < nd) sorted[atomicAdd(cursor + q, 1)] = static_cast<int32_t>(p);
+    }
+}
+
+// Workspace of the pair-list forward: the varlen plan's, then the grouping.
+struct PairsWs {
+    size_t off_qcnt = 0, off_qptr = 0, off_uptr = 0, off_cursor = 0, off_sorted = 0, bytes = 0;
+};
+
+PairsWs pairs_ws(size_t base, int64_t nq, int64_t np) {
+    PairsWs w;
+    size_t off = round_up(base, 256);
+    w.off_qcnt = off;
+    off = round_up(off + static_cast<size_t>(nq) * 4, 256);
+    w.off_qptr = off;
+    off = round_up(off + static_cast<size_t>(nq + 1) * 4, 256);
+    w.off_uptr = off;
+    off = round_up(off + static_cast<size_t>(nq + 1) * 4, 256);
+    w.off_cursor = off;
+    off = round_up(off + static_cast<size_t>(nq) * 4, 256);
+    w.off_sorted = off;
+    off = round_up(off + static_cast<size_t>(np) * 4, 256);
+    w.bytes = off;
+    return w;
 }
 
 maxsim_status check_dim(int64_t dim, int64_t multiple) {
@@ -504,6 +629,8 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
         return plan_fwd(Nq, Lq, Nd, dim, false, false).ws_bytes;
     case MAXSIM_OP_FWD_VARLEN:
         return plan_fwd(Nq, Lq, Nd, dim, true, false).ws_bytes;
+    case MAXSIM_OP_SCORE_PAIRS:  // Ld carries the number of pairs
+        return pairs_ws(plan_fwd(Nq, Lq, Nd, dim, true, false).ws_bytes, Nq, Ld).bytes;
     case MAXSIM_OP_FWD_INT8:
         return plan_fwd(Nq, Lq, Nd, dim, false, true).ws_bytes;
     case MAXSIM_OP_BWD: {
@@ -622,6 +749,85 @@ maxsim_status maxsim_fwd_varlen(const void* Q, const int32_t* cu_seqlens_q, int6
     c.d_mask = d_mask;
     c.scores = scores;
     c.argmax = argmax;
+    return run_fwd(dev, p, c, ws, st);
+}
+
+maxsim_status maxsim_score_pairs_packed(const void* Q, const int32_t* cu_seqlens_q, int64_t max_lq, const void* D,
+                                        const int32_t* cu_seqlens_d, int64_t total_d, maxsim_dtype dtype, int64_t Nq,
+                                        int64_t Nd, int64_t dim, const uint8_t* q_mask, const uint8_t* d_mask,
+                                        const int32_t* pairs, int64_t num_pairs, float* scores, int32_t* argmax,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (dtype != MAXSIM_F16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_INVALID_ARG;
+    if (Nq < 0 || Nd < 0 || max_lq < 0 || total_d < 0 || num_pairs < 0) return MAXSIM_ERR_INVALID_ARG;
+    maxsim_status rc = check_dim(dim, 16);
+    if (rc != MAXSIM_OK) return rc;
+    if (num_pairs == 0) return MAXSIM_OK;
+    if (!scores || !pairs || !aligned(pairs, 4) || !cu_seqlens_d) return MAXSIM_ERR_INVALID_ARG;
+    if ((max_lq > 0 && (!Q || !aligned16(Q))) || (total_d > 0 && (!D || !aligned16(D))))
+        return MAXSIM_ERR_INVALID_ARG;
+    if (total_d > kI32Max || Nq * pad_lq(max_lq) > kI32Max || num_pairs > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
+    const FwdPlan p = plan_fwd(Nq, max_lq, Nd, dim, true, false);
+    if (!p.ok || p.n_chunks > 1) return MAXSIM_ERR_UNSUPPORTED;  // one query per unit: up to 4 M-tiles
+    const PairsWs pw = pairs_ws(p.ws_bytes, Nq, num_pairs);
+    if (workspace_bytes < pw.bytes || !workspace) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* qcnt = reinterpret_cast<int32_t*>(ws + pw.off_qcnt);
+    int32_t* qptr = reinterpret_cast<int32_t*>(ws + pw.off_qptr);
+    int32_t* uptr = reinterpret_cast<int32_t*>(ws + pw.off_uptr);
+    int32_t* cursor = reinterpret_cast<int32_t*>(ws + pw.off_cursor);
+    int32_t* sorted = reinterpret_cast<int32_t*>(ws + pw.off_sorted);
+    const int gp = grid_for(num_pairs, 256, dev->num_sms);
+    if (Nq * Nd == 0 || max_lq == 0) {
+        // no pair can be valid (reported), or every query is empty (score 0)
+        if (Nq * Nd == 0) {
+            pairs_count_kernel<<<gp, 256, 0, st>>>(pairs, num_pairs, Nq, Nd, nullptr, scores, argmax, max_lq,
+                                                   dev->status);
+        } else {
+            fill_kernel<<<gp, 256, 0, st>>>(scores, num_pairs, nullptr, 0);
+        }
+        return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+    }
+    check_cu_kernel<<<grid_for(Nd + 1, 256, dev->num_sms), 256, 0, st>>>(cu_seqlens_d, Nd, total_d, dev->status);
+    if (cu_seqlens_q)
+        check_cu_kernel<<<grid_for(Nq + 1, 256, dev->num_sms), 256, 0, st>>>(cu_seqlens_q, Nq, -1, dev->status);
+    // group the pairs by query: count, scan (pairs and units), place
+    const int32_t chunk =
+        static_cast<int32_t>(std::max<int64_t>(1, (num_pairs + 4 * dev->num_sms - 1) / (4 * dev->num_sms)));
+    if (cudaMemsetAsync(qcnt, 0, static_cast<size_t>(Nq) * 4, st) != cudaSuccess) return MAXSIM_ERR_CUDA;
+    pairs_count_kernel<<<gp, 256, 0, st>>>(pairs, num_pairs, Nq, Nd, qcnt, scores, argmax, max_lq, dev->status);
+    pairs_scan_kernel<<<1, 1024, 0, st>>>(qcnt, Nq, chunk, qptr, uptr, cursor);
+    pairs_place_kernel<<<gp, 256, 0, st>>>(pairs, num_pairs, Nq, Nd, cursor, sorted);
+    uint16_t* qp = reinterpret_cast<uint16_t*>(ws + p.off_q);
+    dim3 blk(32, 8);
+    repack_q_kernel<false><<<grid_for(p.rows, 8, dev->num_sms), blk, 0, st>>>(
+        Q, cu_seqlens_q, max_lq, p.lq_pad, Nq, dim, q_mask, nullptr, qp, ws + p.off_real, ws + p.off_active, nullptr);
+    if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+    FwdCall c{};
+    c.q_rows = qp;
+    c.q_real = ws + p.off_real;
+    c.q_active = ws + p.off_active;
+    c.d_rows = D;
+    c.q_dt = c.d_dt = half_map(dtype);
+    c.ab_format = dtype == MAXSIM_BF16 ? 1u : 0u;
+    c.nan_pair = dtype == MAXSIM_BF16 ? kNaNPairBF16 : kNaNPairF16;
+    c.nq = Nq;
+    c.lq_out = max_lq;
+    c.nd = Nd;
+    c.ld = 0;
+    c.total_d = total_d;
+    c.dim = dim;
+    c.cu_d = cu_seqlens_d;
+    c.d_mask = d_mask;
+    c.scores = scores;
+    c.argmax = argmax;
+    c.pr_pairs = pairs;
+    c.pr_sorted = sorted;
+    c.pr_qptr = qptr;
+    c.pr_uptr = uptr;
+    c.pr_chunk = chunk;
     return run_fwd(dev, p, c, ws, st);
 }
 

@@ -127,6 +127,43 @@ def maxsim_fwd_varlen(Q: torch.Tensor, cu_seqlens_q: Optional[torch.Tensor], max
     return scores, argmax
 
 
+def maxsim_score_pairs_packed(Q: torch.Tensor, cu_seqlens_q: Optional[torch.Tensor], max_lq: int, D: torch.Tensor,
+                              cu_seqlens_d: torch.Tensor, pairs: torch.Tensor, q_mask=None, d_mask=None, *,
+                              want_argmax: bool = False, scores: Optional[torch.Tensor] = None,
+                              argmax: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Scores of the (query, document) pairs `pairs` [num_pairs, 2] (int32)
+    over the packed batches of maxsim_fwd_varlen. Returns scores [num_pairs]
+    (and argmax [num_pairs, max_lq])."""
+    if Q.dtype not in _DT or D.dtype != Q.dtype:
+        raise TypeError("Q and D must both be float16 or both bfloat16")
+    dev = Q.device
+    Q, D = _contig(Q, "Q"), _contig(D, "D", device=dev)
+    cu_d = _contig(cu_seqlens_d, "cu_seqlens_d", torch.int32, dev)
+    cu_q = _contig(cu_seqlens_q, "cu_seqlens_q", torch.int32, dev)
+    pr = _contig(pairs, "pairs", torch.int32, dev)
+    if pr.dim() != 2 or pr.shape[1] != 2:
+        raise ValueError("pairs must be [num_pairs, 2]")
+    dim = Q.shape[-1]
+    if D.dim() != 2 or D.shape[1] != dim:
+        raise ValueError("D must be packed [total_d, dim]")
+    Nd = cu_d.numel() - 1
+    Nq = (cu_q.numel() - 1) if cu_q is not None else Q.shape[0]
+    if cu_q is None and (Q.dim() != 3 or Q.shape[1] != max_lq):
+        raise ValueError("dense Q must be [Nq, max_lq, dim]")
+    total_d, n = D.shape[0], pr.shape[0]
+    qm, dm = _mask(q_mask, "q_mask", dev), _mask(d_mask, "d_mask", dev)
+    if scores is None:
+        scores = torch.empty((n,), dtype=torch.float32, device=dev)
+    if want_argmax and argmax is None:
+        argmax = torch.empty((n, max_lq), dtype=torch.int32, device=dev)
+    ws, nbytes = _workspace(workspace_size(_native.OP_SCORE_PAIRS, Nq, max_lq, Nd, n, dim), dev, workspace)
+    rc = _native.lib().maxsim_score_pairs_packed(_ptr(Q), _ptr(cu_q), max_lq, _ptr(D), _ptr(cu_d), total_d,
+                                                 _DT[Q.dtype], Nq, Nd, dim, _ptr(qm), _ptr(dm), _ptr(pr), n,
+                                                 _ptr(scores), _ptr(argmax), _ptr(ws), nbytes, _stream(dev))
+    _native.check(rc, "maxsim_score_pairs_packed")
+    return scores, argmax
+
+
 def maxsim_bwd(Q: torch.Tensor, D: torch.Tensor, argmax: torch.Tensor, grad_scores: torch.Tensor, q_mask=None, *,
                want_dq: bool = True, want_dd: bool = True, want_csr: bool = False,
                dQ: Optional[torch.Tensor] = None, dD: Optional[torch.Tensor] = None,

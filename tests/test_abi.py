@@ -73,6 +73,18 @@ def test_varlen_and_bwd_host_validation(lib):
     assert b(FAKE, FAKE, 3, 2, 8, 3, 10, 128, None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 20, None) == 1
 
 
+def test_score_pairs_host_validation(lib):
+    sp = lib.maxsim_score_pairs_packed
+    # Q, cu_q, max_lq, D, cu_d, total_d, dtype, Nq, Nd, dim, q_mask, d_mask, pairs, n, scores, argmax, ws, bytes, stream
+    assert sp(FAKE, None, 32, FAKE, FAKE, 100, 0, 2, 3, 128, None, None, FAKE, 0, FAKE, None, None, 0, None) == 0
+    assert sp(FAKE, None, 32, FAKE, FAKE, 100, 0, 2, 3, 128, None, None, None, 5, FAKE, None, FAKE, 1 << 20, None) == 1
+    assert sp(FAKE, None, 32, FAKE, None, 100, 0, 2, 3, 128, None, None, FAKE, 5, FAKE, None, FAKE, 1 << 20, None) == 1
+    assert sp(FAKE, None, 32, FAKE, FAKE, 100, 2, 2, 3, 128, None, None, FAKE, 5, FAKE, None, FAKE, 1 << 20, None) == 1
+    assert sp(FAKE, None, 32, FAKE, FAKE, 100, 0, 2, 3, 128, None, None, FAKE, 5, FAKE, None, None, 0, None) == 5
+    assert sp(FAKE, None, 600, FAKE, FAKE, 100, 0, 2, 3, 128, None, None, FAKE, 5, FAKE, None, FAKE, 1 << 30,
+              None) == 2                                            # one query per unit: at most 512 rows
+
+
 def test_workspace_sizes(lib):
     ws = lib.maxsim_workspace_size
     assert ws(0, 32, 32, 100, 180, 128) == 0                      # aligned query length, no chunks
@@ -80,5 +92,6 @@ def test_workspace_sizes(lib):
     assert ws(0, 1, 1024, 10, 1024, 128) >= 2 * 1 * 10 * 4        # two 512-row chunks of partial scores
     assert ws(1, 32, 32, 1000, 50000, 128) > 0                    # varlen always repacks the queries
     assert ws(2, 4, 8, 3, 10, 128) >= 4 * (3 + 4 + 31 + 96)      # counts, bases, row_ptr, col
+    assert ws(4, 32, 32, 1000, 5000, 128) >= ws(1, 32, 32, 1000, 50000, 128) + 4 * (32 * 4 + 5000)  # + grouping
     assert ws(9, 1, 1, 1, 1, 16) == ctypes.c_size_t(-1).value
     assert ws(0, -1, 1, 1, 1, 16) == ctypes.c_size_t(-1).value
