@@ -33,10 +33,12 @@ DTYPES = {"f16": 0, "bf16": 1, "f64": 2}
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle (gcc -O2 -fopenmp) next to its source."""
+    """Compile the oracle (gcc -O2 -ffp-contract=off -fopenmp) next to its source."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        # no fused multiply-add contraction: the same rounding on every host
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC,
+                               "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -53,7 +55,10 @@ def _load():
                                             vp, ci]
             lib.oracle_csr.argtypes = [vp, i64, i64, i64, i64, vp, vp]
             lib.oracle_bwd.argtypes = [vp, vp, ci, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, ci]
-            for f in (lib.oracle_fwd, lib.oracle_fwd_int8, lib.oracle_csr, lib.oracle_bwd, lib.oracle_max_threads):
+            lib.oracle_chamfer_fwd.argtypes = [vp, vp, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, ci]
+            lib.oracle_chamfer_bwd.argtypes = [vp, vp, i64, i64, i64, i64, vp, vp, vp, vp, vp]
+            for f in (lib.oracle_fwd, lib.oracle_fwd_int8, lib.oracle_csr, lib.oracle_bwd, lib.oracle_max_threads,
+                      lib.oracle_chamfer_fwd, lib.oracle_chamfer_bwd):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -178,3 +183,43 @@ def bwd(Q, D, dtype, argmax, grad, q_mask=None, threads=0):
     if rc:
         raise ValueError(f"oracle_bwd failed ({rc})")
     return dQ, dD, row_ptr, col[: row_ptr[-1]].copy()
+
+
+def chamfer_fwd(P, Q, threads=0):
+    """Chamfer distance (Sec. 4.2.4) of B pairs of point sets P [B, N, dim],
+    Q [B, M, dim] (float32). Returns (dist_p [B,N], idx_p [B,N], gap_p [B,N],
+    dist_q [B,M], idx_q [B,M], gap_q [B,M], loss [B]), distances in float64."""
+    P = np.ascontiguousarray(P, dtype=np.float32)
+    Q = np.ascontiguousarray(Q, dtype=np.float32)
+    B, N, dim = P.shape
+    M = Q.shape[1]
+    assert Q.shape[0] == B and Q.shape[2] == dim
+    dp, gp = np.zeros((B, N)), np.zeros((B, N))
+    dq, gq = np.zeros((B, M)), np.zeros((B, M))
+    ip = np.zeros((B, N), dtype=np.int32)
+    iq = np.zeros((B, M), dtype=np.int32)
+    loss = np.zeros(B)
+    rc = _load().oracle_chamfer_fwd(_p(P), _p(Q), B, N, M, dim, _p(dp), _p(ip), _p(gp), _p(dq), _p(iq), _p(gq),
+                                    _p(loss), threads)
+    if rc:
+        raise ValueError(f"oracle_chamfer_fwd failed ({rc})")
+    return dp, ip, gp, dq, iq, gq, loss
+
+
+def chamfer_bwd(P, Q, idx_p, idx_q, grad):
+    """dP [B,N,dim], dQ [B,M,dim] (float64) of sum_b grad[b] * CD(P_b, Q_b)."""
+    P = np.ascontiguousarray(P, dtype=np.float32)
+    Q = np.ascontiguousarray(Q, dtype=np.float32)
+    B, N, dim = P.shape
+    M = Q.shape[1]
+    ip = np.ascontiguousarray(idx_p, dtype=np.int32)
+    iq = np.ascontiguousarray(idx_q, dtype=np.int32)
+    g = np.ascontiguousarray(grad, dtype=np.float32).reshape(-1)
+    dP = np.zeros((B, N, dim))
+    dQ = np.zeros((B, M, dim))
+    rc = _load().oracle_chamfer_bwd(_p(P), _p(Q), B, N, M, dim, _p(ip), _p(iq), _p(g), _p(dP), _p(dQ))
+    if rc == 3:
+        raise ValueError("nearest index outside [-1, set size)")
+    if rc:
+        raise ValueError(f"oracle_chamfer_bwd failed ({rc})")
+    return dP, dQ

@@ -34,6 +34,8 @@
  *  - INT8: the max is taken over dequantised values dot * d_scale[t]; the
  *    positive q_scale[s] multiplies the row maximum.
  *  - Masked query rows still enter the CSR (their weight is 0).
+ *  - Chamfer: with an empty point set both terms are 0 and every point
+ *    reports nearest index -1 (distance 0).
  */
 #include <math.h>
 #include <stdint.h>
@@ -329,6 +331,119 @@ int oracle_bwd(const void *Q, const void *D, int dtype, int64_t Nq, int64_t Lq, 
     if (!row_ptr_out) free(row_ptr);
     if (!col_out) free(col);
     return rc;
+}
+
+/*
+ * Chamfer distance ("Flash-MaxSim" paper, Sec. 4.2.4): for B independent
+ * pairs of point sets P [B, N, dim] and Q [B, M, dim],
+ *   CD(P, Q) = (1/N) sum_p min_q ||p - q||^2 + (1/M) sum_q min_p ||q - p||^2.
+ * float32 inputs, double arithmetic. Per point: the squared distance to its
+ * nearest point of the other set, that point's index (lowest index among
+ * ties) and the gap to the second-nearest distance (+inf if there is none).
+ * Reading where the page is silent: with an empty set (N or M = 0) both
+ * terms are 0 and every point reports index -1 and distance 0.
+ */
+static void chamfer_dir(const float *X, int64_t nx, const float *Y, int64_t ny, int64_t dim, double *dist,
+                        int32_t *idx, double *gap) {
+    for (int64_t x = 0; x < nx; ++x) {
+        double best = INFINITY, second = INFINITY;
+        int32_t arg = -1;
+        for (int64_t y = 0; y < ny; ++y) {
+            double d2 = 0.0;
+            for (int64_t k = 0; k < dim; ++k) {
+                double diff = (double)X[x * dim + k] - (double)Y[y * dim + k];
+                d2 += diff * diff;
+            }
+            if (d2 < best) { second = best; best = d2; arg = (int32_t)y; }
+            else if (d2 < second) { second = d2; }
+        }
+        dist[x] = arg < 0 ? 0.0 : best;
+        idx[x] = arg;
+        gap[x] = second - best;
+    }
+}
+
+int oracle_chamfer_fwd(const float *P, const float *Q, int64_t B, int64_t N, int64_t M, int64_t dim,
+                       double *dist_p, int32_t *idx_p, double *gap_p, double *dist_q, int32_t *idx_q,
+                       double *gap_q, double *loss, int nthreads) {
+    if (B < 0 || N < 0 || M < 0 || dim <= 0) return 1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t b = 0; b < B; ++b) {
+        const float *Pb = P + b * N * dim, *Qb = Q + b * M * dim;
+        chamfer_dir(Pb, N, Qb, M, dim, dist_p + b * N, idx_p + b * N, gap_p + b * N);
+        chamfer_dir(Qb, M, Pb, N, dim, dist_q + b * M, idx_q + b * M, gap_q + b * M);
+        double sp = 0.0, sq = 0.0;
+        for (int64_t x = 0; x < N; ++x) sp += dist_p[b * N + x];
+        for (int64_t y = 0; y < M; ++y) sq += dist_q[b * M + y];
+        loss[b] = (N > 0 && M > 0) ? sp / (double)N + sq / (double)M : 0.0;
+    }
+    return 0;
+}
+
+/*
+ * Gradient of sum_b g[b] * CD(P_b, Q_b) through the saved nearest indices
+ * a = idx_p (P -> Q) and c = idx_q (Q -> P) (Sec. 4.2.4 with the inverse
+ * index of Sec. 4.2.2-4.2.3):
+ *   dP[p] = g (2/N) (p - Q[a_p]) - g (2/M) sum over q with c_q = p of (q - p)
+ *   dQ[q] = g (2/M) (q - P[c_q]) - g (2/N) sum over p with a_p = q of (p - q)
+ * The sums over an inverse index run in ascending source order (a CSR by
+ * counting sort). Points with index -1 contribute nothing. Returns 3 for an
+ * index outside [-1, size of the other set).
+ */
+int oracle_chamfer_bwd(const float *P, const float *Q, int64_t B, int64_t N, int64_t M, int64_t dim,
+                       const int32_t *idx_p, const int32_t *idx_q, const float *g, double *dP, double *dQ) {
+    if (B < 0 || N < 0 || M < 0 || dim <= 0) return 1;
+    for (int64_t b = 0; b < B; ++b) {
+        const float *Pb = P + b * N * dim, *Qb = Q + b * M * dim;
+        const int32_t *a = idx_p + b * N, *c = idx_q + b * M;
+        double *dPb = dP + b * N * dim, *dQb = dQ + b * M * dim;
+        const double gb = (double)g[b];
+        const double wn = N > 0 ? 2.0 * gb / (double)N : 0.0, wm = M > 0 ? 2.0 * gb / (double)M : 0.0;
+        for (int64_t x = 0; x < N; ++x)
+            if (a[x] < -1 || a[x] >= M) return 3;
+        for (int64_t y = 0; y < M; ++y)
+            if (c[y] < -1 || c[y] >= N) return 3;
+        /* inverse of a (destinations = Q points) and of c (destinations = P points) as CSRs */
+        int64_t *cnt_q = (int64_t *)calloc((size_t)M + 1, sizeof(int64_t));
+        int64_t *cnt_p = (int64_t *)calloc((size_t)N + 1, sizeof(int64_t));
+        int64_t *col_q = (int64_t *)malloc(((size_t)N + 1) * sizeof(int64_t));
+        int64_t *col_p = (int64_t *)malloc(((size_t)M + 1) * sizeof(int64_t));
+        int64_t *fill_q = (int64_t *)calloc((size_t)M + 1, sizeof(int64_t));
+        int64_t *fill_p = (int64_t *)calloc((size_t)N + 1, sizeof(int64_t));
+        if (!cnt_q || !cnt_p || !col_q || !col_p || !fill_q || !fill_p) {
+            free(cnt_q); free(cnt_p); free(col_q); free(col_p); free(fill_q); free(fill_p);
+            return 4;
+        }
+        for (int64_t x = 0; x < N; ++x) if (a[x] >= 0) cnt_q[a[x] + 1] += 1;
+        for (int64_t y = 0; y < M; ++y) if (c[y] >= 0) cnt_p[c[y] + 1] += 1;
+        for (int64_t y = 0; y < M; ++y) cnt_q[y + 1] += cnt_q[y];
+        for (int64_t x = 0; x < N; ++x) cnt_p[x + 1] += cnt_p[x];
+        for (int64_t x = 0; x < N; ++x)
+            if (a[x] >= 0) { col_q[cnt_q[a[x]] + fill_q[a[x]]] = x; fill_q[a[x]] += 1; }
+        for (int64_t y = 0; y < M; ++y)
+            if (c[y] >= 0) { col_p[cnt_p[c[y]] + fill_p[c[y]]] = y; fill_p[c[y]] += 1; }
+        for (int64_t x = 0; x < N; ++x) {
+            for (int64_t k = 0; k < dim; ++k) {
+                const double px = (double)Pb[x * dim + k];
+                double v = a[x] >= 0 ? wn * (px - (double)Qb[(int64_t)a[x] * dim + k]) : 0.0;
+                double inv = 0.0;
+                for (int64_t e = cnt_p[x]; e < cnt_p[x + 1]; ++e) inv += (double)Qb[col_p[e] * dim + k] - px;
+                dPb[x * dim + k] = v - wm * inv;
+            }
+        }
+        for (int64_t y = 0; y < M; ++y) {
+            for (int64_t k = 0; k < dim; ++k) {
+                const double qy = (double)Qb[y * dim + k];
+                double v = c[y] >= 0 ? wm * (qy - (double)Pb[(int64_t)c[y] * dim + k]) : 0.0;
+                double inv = 0.0;
+                for (int64_t e = cnt_q[y]; e < cnt_q[y + 1]; ++e) inv += (double)Pb[col_q[e] * dim + k] - qy;
+                dQb[y * dim + k] = v - wn * inv;
+            }
+        }
+        free(cnt_q); free(cnt_p); free(col_q); free(col_p); free(fill_q); free(fill_p);
+    }
+    return 0;
 }
 
 int oracle_version(void) { return 1; }

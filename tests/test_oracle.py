@@ -323,3 +323,116 @@ def test_backward_column_sums_and_csr():
 def test_csr_rejects_out_of_range():
     with pytest.raises(ValueError):
         oracle.csr(np.array([[0, 7]], np.int32), 1, 2, 1, 3)
+
+
+# ---------------------------------------------------------------- Chamfer distance
+
+def test_chamfer_hand_example(golden):
+    ex = golden["chamfer_two_points"]
+    P = np.array([ex["P"]], np.float32)
+    Q = np.array([ex["Q"]], np.float32)
+    dp, ip, _, dq, iq, _, loss = oracle.chamfer_fwd(P, Q)
+    assert dp[0].tolist() == ex["dist_p"] and ip[0].tolist() == ex["idx_p"]
+    assert dq[0].tolist() == ex["dist_q"] and iq[0].tolist() == ex["idx_q"]
+    assert loss[0] == ex["loss"]
+    dP, dQ = oracle.chamfer_bwd(P, Q, ip, iq, np.array([ex["grad_loss"]], np.float32))
+    assert dP[0].tolist() == ex["dP"] and dQ[0].tolist() == ex["dQ"]
+
+
+def _clouds(seed, B, N, M, dim=3, scale=1.0, integer=False):
+    rng = np.random.default_rng(seed)
+    if integer:
+        return (rng.integers(-20, 21, (B, N, dim)).astype(np.float32), rng.integers(-20, 21, (B, M, dim)).astype(np.float32))
+    return ((rng.standard_normal((B, N, dim)) * scale).astype(np.float32),
+            (rng.standard_normal((B, M, dim)) * scale).astype(np.float32))
+
+
+def _sq_dist(p, q):
+    """Squared distance summed left to right in double (the built-in sum() of
+    floats compensates, which would round differently)."""
+    d = 0.0
+    for x, y in zip(p, q):
+        t = float(x) - float(y)
+        d += t * t
+    return d
+
+
+def test_chamfer_brute_force_tiny():
+    # nearest neighbours by exhaustive search over an explicit distance table
+    for seed in range(5):
+        P, Q = _clouds(seed, 2, 7, 5, dim=1 + seed % 4)
+        dp, ip, gp, dq, iq, gq, loss = oracle.chamfer_fwd(P, Q)
+        for b in range(2):
+            table = np.array([[_sq_dist(p, q) for q in Q[b]] for p in P[b]])
+            assert np.array_equal(ip[b], table.argmin(axis=1)) and np.array_equal(iq[b], table.argmin(axis=0))
+            assert np.array_equal(dp[b], table.min(axis=1)) and np.array_equal(dq[b], table.min(axis=0))
+            assert np.array_equal(gp[b], np.sort(table, axis=1)[:, 1] - table.min(axis=1))
+            # sums in a different order: equal to rounding
+            assert np.isclose(loss[b], table.min(axis=1).mean() + table.min(axis=0).mean(), rtol=1e-14, atol=0)
+
+
+def test_chamfer_invariants():
+    P, Q = _clouds(11, 3, 40, 33, integer=True)
+    _, _, _, _, _, _, loss = oracle.chamfer_fwd(P, Q)
+    # symmetric in its arguments
+    assert np.array_equal(oracle.chamfer_fwd(Q, P)[6], loss)
+    # translation invariant (integer shifts keep every value exact)
+    t = np.array([3, -7, 11], np.float32)
+    assert np.array_equal(oracle.chamfer_fwd(P + t, Q + t)[6], loss)
+    # a set against itself: zero, every point its own nearest neighbour
+    dp, ip, _, dq, iq, _, l0 = oracle.chamfer_fwd(P, P)
+    assert (l0 == 0).all() and (dp == 0).all() and (dq == 0).all()
+    # scaling by 2 scales every squared distance by 4
+    assert np.array_equal(oracle.chamfer_fwd(2 * P, 2 * Q)[6], 4 * loss)
+
+
+def test_chamfer_single_target_closed_form():
+    P, Q = _clouds(13, 2, 9, 1)
+    dp, ip, _, dq, iq, _, loss = oracle.chamfer_fwd(P, Q)
+    d = ((P.astype(np.float64) - Q.astype(np.float64)) ** 2).sum(-1)
+    assert np.allclose(dp, d, rtol=1e-15, atol=0) and (ip == 0).all()
+    assert np.allclose(dq[:, 0], d.min(axis=1), rtol=1e-15, atol=0)
+    assert np.allclose(loss, d.mean(axis=1) + d.min(axis=1), rtol=1e-14, atol=0)
+
+
+def test_chamfer_ties_take_lowest_index_and_empty_sets():
+    P = np.zeros((1, 3, 3), np.float32)
+    Q = np.array([[[1, 0, 0], [0, 1, 0], [0, 0, 1]]], np.float32)
+    dp, ip, gp, dq, iq, _, _ = oracle.chamfer_fwd(P, Q)
+    assert (ip == 0).all() and (gp == 0).all() and (iq == 0).all()
+    dp, ip, _, dq, iq, _, loss = oracle.chamfer_fwd(np.zeros((1, 0, 3), np.float32), Q)
+    assert loss[0] == 0 and (iq == -1).all() and (dq == 0).all()
+    dP, dQ = oracle.chamfer_bwd(np.zeros((1, 0, 3), np.float32), Q, ip, iq, np.ones(1, np.float32))
+    assert (dQ == 0).all()
+
+
+def test_chamfer_gradient_finite_differences():
+    P, Q = _clouds(17, 1, 12, 10)
+    _, ip, gp, _, iq, gq, _ = oracle.chamfer_fwd(P, Q)
+    assert gp.min() > 1e-3 and gq.min() > 1e-3  # nearest neighbours stable under the probe
+    g = np.array([0.7], np.float32)
+    dP, dQ = oracle.chamfer_bwd(P, Q, ip, iq, g)
+    h = 1e-3
+
+    def loss_at(P2, Q2):  # the loss at perturbed points, evaluated in double through the oracle's indices
+        Pd, Qd = P2.astype(np.float64)[0], Q2.astype(np.float64)[0]
+        return 0.7 * (((Pd - Qd[ip[0]]) ** 2).sum(-1).mean() + ((Qd - Pd[iq[0]]) ** 2).sum(-1).mean())
+
+    for which, X, dX in (("P", P, dP), ("Q", Q, dQ)):
+        for n, k in [(0, 0), (3, 1), (7, 2)]:
+            Xp, Xm = X.astype(np.float64).copy(), X.astype(np.float64).copy()
+            Xp[0, n, k] += h
+            Xm[0, n, k] -= h
+            if which == "P":
+                fd = (loss_at(Xp, Q) - loss_at(Xm, Q)) / (2 * h)
+            else:
+                fd = (loss_at(P, Xp) - loss_at(P, Xm)) / (2 * h)
+            assert abs(fd - dX[0, n, k]) < 1e-6 * max(1.0, abs(fd))
+
+
+def test_chamfer_gradient_sums():
+    # translation invariance of the loss: every gradient sums to zero over both sets
+    P, Q = _clouds(19, 2, 30, 25)
+    _, ip, _, _, iq, _, _ = oracle.chamfer_fwd(P, Q)
+    dP, dQ = oracle.chamfer_bwd(P, Q, ip, iq, np.array([1.3, -0.4], np.float32))
+    assert np.allclose(dP.sum(axis=1) + dQ.sum(axis=1), 0, atol=1e-12)
