@@ -11,6 +11,8 @@ document against every query.
                   [--workload NAME] [--shard weak|global]
 
 Other workloads (measured the same way, for the design notes):
+  chamfer_100k     Chamfer distance, forward + backward, of two 100,000-point
+                   3-D clouds (float32): cloud pairs/s, fp32 ALU roofline
   tiny_rerank      1 x 32 tokens vs 1,000 x 180 (f16), scores + argmax
   colpali_cross    128 x 128 vs 128 x 1024 (bf16), masks, scores + argmax
   contrastive_bwd  the backward of 64 x 128 vs 64 x 1024 (bf16)
@@ -45,6 +47,19 @@ if ROOT not in sys.path:
 
 METRIC = "MaxSim docs scored/s at 1 GB300 + % of roofline (HBM GB/s or tensor-pipe)"
 UNIT = "docs/s"
+CHAMFER_METRIC = "Chamfer distance forward + backward of 100K-point cloud pairs/s at 1 GB300 + % of fp32 FMA peak"
+CHAMFER_UNIT = "cloud pairs/s"
+FP32_LANES_PER_SM = 128  # fp32 FMA lanes per SM (4 sub-partitions x 32)
+
+
+def metric_of(workload: str):
+    return (CHAMFER_METRIC, CHAMFER_UNIT) if workload.startswith("chamfer") else (METRIC, UNIT)
+
+
+def chamfer_fma(B: int, N: int, M: int, dim: int) -> int:
+    """FMAs of the nearest-point search: dim per (source, target) pair, both
+    directions (the min of each pair is extra)."""
+    return 2 * B * N * M * dim
 L2_BYTES = 129 * 1024 * 1024
 
 # ---------------------------------------------------------------- byte / flop accounting
@@ -101,9 +116,11 @@ def shard_documents(lens: np.ndarray, rank: int, world: int):
 
 # ---------------------------------------------------------------- helpers
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(workload: str) -> str:
+    """Hash of the device sources of the workload's dominant kernel."""
+    files = ("chamfer_kernels.cuh",) if workload.startswith("chamfer") else ("fwd_kernel.cuh", "ptx.cuh")
     h = hashlib.sha256()
-    for f in ("fwd_kernel.cuh", "ptx.cuh", "maxsim_api.cu"):
+    for f in files:
         with open(os.path.join(ROOT, "maxsim_scoring_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -115,7 +132,6 @@ def kernel_source_hash() -> str:
 # profiles/maxsim_fwd_kernel_pair_int8__int8_rerank.md); valid only for the
 # kernel sources whose hash is recorded with it.
 MEASURED_TRAFFIC = {
-    ("colbert_varlen", "2fa4a0496781f598"): 4356116017,  # (429.57 + 4.23) MB x 16,644,526 / 1,657,544 tokens
 }
 
 
@@ -212,6 +228,13 @@ def make_workload(name: str, rank: int, world: int, shard: str, nd: int = 0):
 
 def describe(w, spec):
     name = w["name"]
+    if name == "chamfer_100k":
+        text = (f"chamfer_100k: B={w['B']} pair of point clouds, P [{w['N']},{w['dim']}] and Q [{w['M']},{w['dim']}] "
+                f"float32 with N(0,1) coordinates, upstream gradient N(0,1), seed {spec['seed']}; a step is the "
+                f"loss forward (nearest points both ways) and the backward through the saved indices")
+        cfg = {"workload": text, "B": w["B"], "N": w["N"], "M": w["M"], "dim": w["dim"],
+               "l2": "inputs (2.4 MB) stay in L2 by design: the step is ALU-bound; no flush"}
+        return cfg
     if name == "colbert_varlen":
         text = (f"colbert_varlen: Nq={w['Nq']} queries x Lq={w['Lq']} tokens vs Nd={w['Nd']} packed docs, "
                 f"Ld~U[{spec['ld_min']},{spec['ld_max']}] (sum Ld={w['total_d']}), d={w['dim']}, f16, "
@@ -247,7 +270,10 @@ def describe(w, spec):
 # ---------------------------------------------------------------- the oracle arm
 
 def units_of(w) -> int:
-    """Documents scored per step: every (query, document) pair of a pair list."""
+    """Documents scored per step: every (query, document) pair of a pair list;
+    for Chamfer, pairs of point clouds."""
+    if w["name"].startswith("chamfer"):
+        return w["B"]
     return w["num_pairs"] if "num_pairs" in w else w["Nd"]
 
 
@@ -280,10 +306,49 @@ def time_oracle(w, n_docs: int, threads: int = 0):
     return n_docs / dt, dt
 
 
+def time_chamfer_oracle(w, k: int):
+    """Oracle cloud pairs/s from the first k points of P against all of Q (both
+    directions: 2 k M distance evaluations) plus the backward of that pair,
+    scaled by the 2 N M evaluations of a full pair."""
+    import oracle
+    P, Q = w["P"][:, :k], w["Q"]
+    t0 = time.perf_counter()
+    _, ip, _, _, iq, _, _ = oracle.chamfer_fwd(P, Q)
+    oracle.chamfer_bwd(P, Q, ip, iq, w["grad"])
+    dt = time.perf_counter() - t0
+    frac = (2.0 * k * w["M"]) / (2.0 * w["N"] * w["M"])
+    return w["B"] * frac / dt, dt
+
+
 def calibrated_sample(w, target_s: float):
+    if w["name"].startswith("chamfer"):
+        probe = 64
+        _, dt = time_chamfer_oracle(w, probe)
+        return int(max(probe, min(w["N"], probe * target_s / max(dt, 1e-9))))
     probe = min(8, units_of(w))
     rate, _ = time_oracle(w, probe)
     return int(max(probe, min(units_of(w), rate * target_s)))
+
+
+def oracle_sample(w, n: int):
+    """(rate, seconds, description) of the oracle on a bounded sample."""
+    if w["name"].startswith("chamfer"):
+        rate, dt = time_chamfer_oracle(w, n)
+        return rate, dt, (f"first {n} of {w['N']} points of P against all {w['M']} of Q, both directions, "
+                          f"plus that pair's backward, scaled by the distance evaluations of a full pair")
+    rate, dt = time_oracle(w, n)
+    what = (f"first {n} of {w['num_pairs']} pairs" if "num_pairs" in w else
+            f"first {n} of {w['Nd']} documents, all {w['Nq']} queries")
+    return rate, dt, what
+
+
+def oracle_cores(w) -> int:
+    """Threads the oracle actually runs: the Chamfer oracle parallelises over
+    the B pairs of clouds only."""
+    import oracle
+    if w["name"].startswith("chamfer"):
+        return max(1, min(oracle.max_threads(), w["B"]))
+    return oracle.max_threads()
 
 
 def run_reference(args, rank, world):
@@ -291,24 +356,25 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     w, spec = make_workload(args.workload, 0, 1, "weak", args.nd)
-    cores = oracle.max_threads()
+    cores = oracle_cores(w)
+    metric, unit = metric_of(args.workload)
     n = calibrated_sample(w, target_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        time_oracle(w, n)
-    times = []
+        oracle_sample(w, n)
+    rates, times = [], []
     for _ in range(args.steps):
-        _, dt = time_oracle(w, n)
+        rate, dt, what = oracle_sample(w, n)
+        rates.append(rate)
         times.append(dt)
-    value = n * args.steps / sum(times)
-    sample = (f"first {n} of {w['num_pairs']} pairs per step" if "num_pairs" in w else
-              f"first {n} of {w['Nd']} documents per step, all {w['Nq']} queries")
+    value = args.steps / sum(1.0 / r for r in rates)
+    sample = f"{what}, per step"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": describe(w, spec),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -441,6 +507,81 @@ class Case:
             self.flush_buf.add_(1.0)
 
 
+class ChamferCase:
+    """Chamfer distance of one pair of 100K-point clouds: a step is the
+    forward (nearest points both ways, loss) and the backward through the
+    saved indices. The forward call is also timed on its own: its nearest-
+    point kernel dominates the step and carries the roofline."""
+
+    def __init__(self, w, device):
+        import torch as t
+
+        from maxsim_scoring_gb300 import _native, ops
+        self.w, self.device, self.ops, self.t = w, device, ops, t
+        self.name = w["name"]
+        B, N, M, dim = w["B"], w["N"], w["M"], w["dim"]
+        self.h_in = {k: t.from_numpy(np.ascontiguousarray(w[k])).pin_memory() for k in ("P", "Q", "grad")}
+        self.d_in = {k: v.to(device) for k, v in self.h_in.items()}
+        self.e2e_in = {k: t.empty_like(v) for k, v in self.d_in.items()}
+        self.ws_f = t.empty(ops.workspace_size(_native.OP_CHAMFER_FWD, B, N, M, 0, dim), dtype=t.uint8, device=device)
+        self.ws_b = t.empty(max(1, ops.workspace_size(_native.OP_CHAMFER_BWD, B, N, M, 0, dim)), dtype=t.uint8,
+                            device=device)
+        self.dP = t.empty((B, N, dim), dtype=t.float32, device=device)
+        self.dQ = t.empty((B, M, dim), dtype=t.float32, device=device)
+        self.h_out = {"loss": t.empty(B, dtype=t.float32).pin_memory(),
+                      "dP": t.empty((B, N, dim), dtype=t.float32).pin_memory(),
+                      "dQ": t.empty((B, M, dim), dtype=t.float32).pin_memory()}
+        self.units = B
+        self.fma = chamfer_fma(B, N, M, dim)
+        self.flops = 2 * self.fma
+        self.bytes = (B * (N + M) * dim * 4) * 2 + B * (N + M) * 8
+        self.bound, self.dtype = "alu", "f32"
+        K = B * (N + M)
+        passes = max(1, -(-int(K).bit_length() // 8))
+        self.launches = 3 + 1 + 3 * passes + 2  # nn, merge, loss | keys, radix passes, row_ptr, grad
+        self.events = None
+        self.loss = None
+
+    def call(self, d):
+        ops = self.ops
+        stream = self.t.cuda.current_stream(self.device)
+        if self.events is not None:
+            e0, e1 = self.t.cuda.Event(enable_timing=True), self.t.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        self.loss, _, ip, _, iq = ops.chamfer_fwd(d["P"], d["Q"], workspace=self.ws_f)
+        if self.events is not None:
+            e1.record(stream)
+            self.events.append((e0, e1))
+        ops.chamfer_bwd(d["P"], d["Q"], ip, iq, d["grad"], dP=self.dP, dQ=self.dQ, workspace=self.ws_b)
+
+    def step(self):
+        self.call(self.d_in)
+
+    def e2e_step(self):
+        for k, v in self.h_in.items():
+            self.e2e_in[k].copy_(v, non_blocking=True)
+        self.call(self.e2e_in)
+        self.h_out["loss"].copy_(self.loss, non_blocking=True)
+        self.h_out["dP"].copy_(self.dP, non_blocking=True)
+        self.h_out["dQ"].copy_(self.dQ, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.h_in.values())
+
+    def d2h_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.h_out.values())
+
+    def flush(self):
+        pass
+
+    def start_kernel_timing(self):
+        self.events = []
+
+    def kernel_ms(self):
+        ev, self.events = self.events, None
+        return sum(a.elapsed_time(b) for a, b in ev) / max(1, len(ev))
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -451,7 +592,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     _native.lib()  # fail loudly without the extension
     w, spec = make_workload(args.workload, rank, world, args.shard, args.nd)
-    case = Case(w, device)
+    case = ChamferCase(w, device) if args.workload.startswith("chamfer") else Case(w, device)
+    metric, unit_name = metric_of(args.workload)
     stream = torch.cuda.current_stream(device)
 
     def barrier():
@@ -471,6 +613,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(device)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if hasattr(case, "start_kernel_timing"):
+        case.start_kernel_timing()
     for k in range(args.steps):
         case.flush()  # outside the events (no-op for inputs larger than L2)
         starts[k].record(stream)
@@ -481,6 +625,7 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     per_step_ms = [starts[k].elapsed_time(ends[k]) for k in range(args.steps)]
     total_ms = sum(per_step_ms)
+    kernel_ms = case.kernel_ms() if hasattr(case, "kernel_ms") else None
     if ops.device_status(device) != 0:
         raise SystemExit("device status after the timed steps is not OK")
 
@@ -511,7 +656,16 @@ def run_ours(args, rank, world, local_rank):
     ms = total_ms / args.steps
     value = all_units / (ms / 1e3)
     peaks, peak_src = load_peaks()
-    if case.bound == "tensor":
+    if case.bound == "alu":
+        # fp32 FMA peak: lanes x SMs x 2 FLOP x the maximum SM clock
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        max_mhz = clk.get("sm_max_mhz") or 2070.0
+        peak = round(FP32_LANES_PER_SM * sms * 2 * max_mhz * 1e6 / 1e12, 2)
+        achieved = case.flops / (kernel_ms / 1e3) / 1e12
+        unit = "TFLOP/s"
+        src = (f"fp32 FMA peak derived from {FP32_LANES_PER_SM} lanes/SM x {sms} SMs x 2 FLOP x {max_mhz:.0f} MHz "
+               f"(maximum SM clock)")
+    elif case.bound == "tensor":
         achieved = case.flops / (ms / 1e3) / 1e12
         sustained = total_ms > 1000.0
         peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
@@ -521,32 +675,31 @@ def run_ours(args, rank, world, local_rank):
         achieved = case.bytes / (ms / 1e3) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
         src = f"{peak_src} HBM copy bandwidth"
-    traffic = (MEASURED_TRAFFIC.get((case.name, kernel_source_hash())) if args.nd is None and world == 1 else None)
+    traffic = MEASURED_TRAFFIC.get((case.name, kernel_source_hash(case.name))) if not args.nd and world == 1 else None
     roofline = {
         "bound": case.bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": src,
-        "kernel": ("maxsim_fwd_kernel (duration = whole entry-point call, which also runs small helper kernels)"
+        "kernel": ("chamfer_nn_kernel (duration = the whole maxsim_chamfer_fwd call, CUDA events per step: "
+                   f"{kernel_ms:.4f} ms; it also runs the merge and loss kernels)" if case.bound == "alu" else
+                   "maxsim_fwd_kernel (duration = whole entry-point call, which also runs small helper kernels)"
                    if case.name != "contrastive_bwd" else "backward kernels (whole maxsim_bwd call)"),
         "algorithmic_flops_per_launch": case.flops,
         "algorithmic_bytes_per_launch": case.bytes,
     }
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "metric": metric, "value": value, "unit": unit_name, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "strong" if args.shard == "global" else "weak",
         "vs_baseline": None, "dtype": case.dtype, "data": "synthetic", "config": describe(w, spec), "clocks": clk,
         "roofline": roofline,
-        "e2e": {"value": all_units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": case.h2d_bytes(),
+        "e2e": {"value": all_units / (e2e_ms / 1e3), "unit": unit_name, "h2d_bytes_per_step": case.h2d_bytes(),
                 "d2h_bytes_per_step": case.d2h_bytes()},
         "gpu_launches": case.launches * args.steps,
         "step_ms_min_median_max": [min(per_step_ms), statistics.median(per_step_ms), max(per_step_ms)],
     }
     if world == 1 and not args.no_cpu_baseline and case.name != "contrastive_bwd":
-        import oracle
         n = calibrated_sample(w, target_s=args.cpu_seconds)
-        rate, dt = time_oracle(w, n)
-        what = (f"first {n} of {w['num_pairs']} pairs" if "num_pairs" in w else
-                f"first {n} of {w['Nd']} documents, all {w['Nq']} queries")
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+        rate, dt, what = oracle_sample(w, n)
+        line["cpu_baseline"] = {"value": rate, "unit": unit_name, "cores": oracle_cores(w), "kind": "oracle",
                                 "sample": f"{what} ({dt:.1f} s)"}
     print(json.dumps(line), flush=True)
 

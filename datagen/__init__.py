@@ -23,6 +23,7 @@ _lib = None
 # tensor ids: each tensor of a workload draws from its own family of streams
 TID_Q, TID_D, TID_LEN_D, TID_QMASK, TID_DMASK, TID_GRAD, TID_LEN_Q = 1, 2, 3, 4, 5, 6, 7
 TID_PAIR_D = 8  # document index of each (query, document) pair
+TID_CLOUD_P, TID_CLOUD_Q, TID_CLOUD_GRAD = 9, 10, 11  # Chamfer point clouds and upstream gradient
 
 DTYPE_CODES = {"f16": 0, "bf16": 1, "f64": 2, "f32": 3}
 

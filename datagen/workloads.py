@@ -19,13 +19,18 @@ generators in this package.
                   document) pairs per query, documents uniform over the corpus
                   (a reranker's candidate lists), seed 2
 Every row is an l2-normalised Gaussian vector rounded once to its storage type.
+
+ chamfer_100k     one pair of 3-D point clouds of 100,000 points each
+                  (standard normal coordinates, float32) and an upstream
+                  gradient N(0,1) per pair, seed 6: the Chamfer-distance
+                  workload at the cloud size the pages run
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import (TID_D, TID_DMASK, TID_GRAD, TID_LEN_D, TID_PAIR_D, TID_Q, TID_QMASK, gaussian_rows, int8_rows,
-               mask_drop_tail, mask_random_subset, normal_f32, uniform_int)
+from . import (TID_CLOUD_GRAD, TID_CLOUD_P, TID_CLOUD_Q, TID_D, TID_DMASK, TID_GRAD, TID_LEN_D, TID_PAIR_D, TID_Q,
+               TID_QMASK, gaussian_rows, int8_rows, mask_drop_tail, mask_random_subset, normal_f32, uniform_int)
 
 SPECS = {
     "tiny_rerank": dict(Nq=1, Lq=32, Nd=1000, Ld=180, dim=128, dtype="f16", seed=0),
@@ -36,6 +41,7 @@ SPECS = {
     "int8_rerank": dict(Nq=1, Lq=1024, Nd=10_000, Ld=1024, dim=128, seed=5),
     "colbert_pairs": dict(Nq=32, Lq=32, Nd=100_000, ld_min=32, ld_max=300, dim=128, dtype="f16", seed=2,
                           pairs_per_query=10_000),
+    "chamfer_100k": dict(B=1, N=100_000, M=100_000, dim=3, seed=6),
 }
 
 
@@ -87,6 +93,16 @@ def int8(Nq, Lq, Nd, Ld, dim, seed):
     return w
 
 
+def clouds(B, N, M, dim, seed):
+    """Point clouds P [B,N,dim], Q [B,M,dim] (float32, standard normal
+    coordinates) and an upstream gradient grad [B] (float32, N(0,1))."""
+    w = dict(B=B, N=N, M=M, dim=dim, seed=seed)
+    w["P"] = gaussian_rows(seed, TID_CLOUD_P, B * N, dim, "f32", normalize=False).reshape(B, N, dim)
+    w["Q"] = gaussian_rows(seed, TID_CLOUD_Q, B * M, dim, "f32", normalize=False).reshape(B, M, dim)
+    w["grad"] = normal_f32(seed, TID_CLOUD_GRAD, B)
+    return w
+
+
 def make(name: str, **overrides):
     """Build a named workload; keyword overrides shrink it for quick tests."""
     spec = dict(SPECS[name])
@@ -97,5 +113,7 @@ def make(name: str, **overrides):
         return pairs(**spec)
     if name == "int8_rerank":
         return int8(**spec)
+    if name == "chamfer_100k":
+        return clouds(**spec)
     grad = name == "contrastive_bwd"
     return dense(**spec, grad=grad)

@@ -58,7 +58,7 @@ typedef enum { MAXSIM_F16 = 0, MAXSIM_BF16 = 1 } maxsim_dtype;
 
 /* Operation codes for maxsim_workspace_size(). */
 enum { MAXSIM_OP_FWD = 0, MAXSIM_OP_FWD_VARLEN = 1, MAXSIM_OP_BWD = 2, MAXSIM_OP_FWD_INT8 = 3,
-       MAXSIM_OP_SCORE_PAIRS = 4 };
+       MAXSIM_OP_SCORE_PAIRS = 4, MAXSIM_OP_CHAMFER_FWD = 5, MAXSIM_OP_CHAMFER_BWD = 6 };
 
 /*
  * Dense forward.
@@ -184,6 +184,50 @@ maxsim_status maxsim_fwd_int8(const int8_t *Q, const float *q_scale,
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Chamfer distance ("Flash-MaxSim" paper, Sec. 4.2.4, the generalisation of
+ * the hard-selection pattern to a min over squared Euclidean distances) of B
+ * independent pairs of point sets:
+ *   CD(P_b, Q_b) = (1/N) sum_p min_q ||p - q||^2 + (1/M) sum_q min_p ||q - p||^2
+ *   P       [B, N, dim] f32        Q [B, M, dim] f32        1 <= dim <= 8
+ *   dist_p  [B, N] f32 (out): squared distance from each p to its nearest q
+ *   idx_p   [B, N] i32 (out): the index in [0, M) of that q
+ *   dist_q, idx_q [B, M] (out): the same from Q to P
+ *   loss    [B] f32 (out): CD(P_b, Q_b)
+ * The [N, M] distance table is never formed (online min over streamed
+ * tiles). The nearest point is searched in fp32 on ||y||^2 - 2 <x, y>; among
+ * candidates whose fp32 values are equal the lowest index wins; dist is then
+ * computed directly as sum_k (x_k - y_k)^2 in fp32 and the loss sums it in
+ * double. With an empty set (N or M = 0) the loss is 0 and every point of the
+ * other set reports index -1 and distance 0. Coordinates must be finite and
+ * their squared norms representable in fp32. P, Q and the outputs need 4-byte
+ * alignment, the workspace 256-byte alignment. Workspace:
+ * maxsim_workspace_size(MAXSIM_OP_CHAMFER_FWD, B, N, M, 0, dim).
+ */
+maxsim_status maxsim_chamfer_fwd(const float *P, const float *Q, int64_t B, int64_t N, int64_t M, int64_t dim,
+                                 float *dist_p, int32_t *idx_p, float *dist_q, int32_t *idx_q, float *loss,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Gradient of sum_b grad_loss[b] * CD(P_b, Q_b) through the saved nearest
+ * indices a = idx_p, c = idx_q of maxsim_chamfer_fwd (Sec. 4.2.4 with the
+ * inverse index of Sec. 4.2.2 and the destination-owned reduction of 4.2.3):
+ *   dP[p] = g (2/N) (p - Q[a_p]) - g (2/M) sum over q with c_q = p of (q - p)
+ *   dQ[q] = g (2/M) (q - P[c_q]) - g (2/N) sum over p with a_p = q of (p - q)
+ *   idx_p [B, N] i32, idx_q [B, M] i32 (values in [-1, size of the other set))
+ *   grad_loss [B] f32;  dP [B, N, dim] f32 (out);  dQ [B, M, dim] f32 (out)
+ * The inverse maps are built on the device as a CSR by a stable sort of the
+ * flattened destinations; every gradient row is written by one thread that
+ * sums its inverse row in ascending source order: no atomics, bitwise
+ * reproducible. fp32 arithmetic. An index of -1 contributes nothing; an index
+ * outside [-1, size) is skipped and reported as MAXSIM_ERR_DEVICE_INPUT by
+ * maxsim_device_status(). Workspace:
+ * maxsim_workspace_size(MAXSIM_OP_CHAMFER_BWD, B, N, M, 0, dim).
+ */
+maxsim_status maxsim_chamfer_bwd(const float *P, const float *Q, int64_t B, int64_t N, int64_t M, int64_t dim,
+                                 const int32_t *idx_p, const int32_t *idx_q, const float *grad_loss, float *dP,
+                                 float *dQ, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace an operation needs for a shape (0 if none).
  *   MAXSIM_OP_FWD / MAXSIM_OP_FWD_INT8: (Nq, Lq, Nd, Ld, dim)
  *   MAXSIM_OP_FWD_VARLEN:              (Nq, max_lq, Nd, total_d, dim); assumes
@@ -191,6 +235,7 @@ maxsim_status maxsim_fwd_int8(const int8_t *Q, const float *q_scale,
  *   MAXSIM_OP_BWD:                     (Nq, Lq, Nd, Ld, dim); assumes the CSR
  *                                      outputs are NULL (an upper bound)
  *   MAXSIM_OP_SCORE_PAIRS:             (Nq, max_lq, Nd, num_pairs, dim)
+ *   MAXSIM_OP_CHAMFER_FWD / _BWD:      (B, N, M, 0, dim)
  * Returns (size_t)-1 for an invalid shape.
  */
 size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim);

@@ -30,3 +30,24 @@ class _MaxSim(torch.autograd.Function):
 def maxsim(Q: torch.Tensor, D: torch.Tensor, q_mask=None, d_mask=None) -> torch.Tensor:
     """Differentiable MaxSim scores [Nq, Nd] for Q [Nq,Lq,d], D [Nd,Ld,d]."""
     return _MaxSim.apply(Q, D, q_mask, d_mask)
+
+
+class _Chamfer(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, P, Q):
+        loss, _, idx_p, _, idx_q = ops.chamfer_fwd(P, Q)
+        ctx.save_for_backward(P, Q, idx_p, idx_q)
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad_loss):
+        P, Q, idx_p, idx_q = ctx.saved_tensors
+        dP, dQ = ops.chamfer_bwd(P, Q, idx_p, idx_q, grad_loss.float().contiguous())
+        return dP, dQ
+
+
+def chamfer_distance(P: torch.Tensor, Q: torch.Tensor) -> torch.Tensor:
+    """Differentiable Chamfer distance [B] of point sets P [B,N,dim], Q [B,M,dim]
+    (float32): the forward saves the nearest indices, the backward routes the
+    gradient through their inverse ("Flash-MaxSim" Sec. 4.2.4)."""
+    return _Chamfer.apply(P, Q)

@@ -12,6 +12,7 @@
 
 #include "maxsim.h"
 #include "bwd_kernels.cuh"
+#include "chamfer_kernels.cuh"
 #include "fwd_kernel.cuh"
 
 namespace maxsim {
@@ -587,6 +588,94 @@ inline CUtensorMapDataType half_map(maxsim_dtype dt) {
     return dt == MAXSIM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
+
+// ---------------------------------------------------------------- Chamfer planning
+
+struct ChamferFwdPlan {
+    int64_t n_sb[2] = {0, 0}, n_span[2] = {0, 0}, n_mblk[2] = {0, 0};
+    int64_t items0 = 0, items = 0;
+    size_t off_counter = 0, off_best[2] = {0, 0}, off_sub[2] = {0, 0}, off_loss[2] = {0, 0}, ws_bytes = 0;
+    int kd = 3;
+};
+
+ChamferFwdPlan plan_chamfer_fwd(int64_t B, int64_t N, int64_t M, int64_t dim) {
+    ChamferFwdPlan p;
+    p.kd = dim <= 3 ? 3 : kChMaxDim;
+    const int64_t per_item = p.kd == 3 ? ChamferShape<3>::kSources : ChamferShape<kChMaxDim>::kSources;
+    const int64_t nx[2] = {N, M}, ny[2] = {M, N};
+    size_t off = 256;  // the work counter
+    for (int d = 0; d < 2; ++d) {
+        p.n_sb[d] = (nx[d] + per_item - 1) / per_item;
+        p.n_span[d] = (ny[d] + kChSpan - 1) / kChSpan;
+        p.n_mblk[d] = (nx[d] + kChMergeThreads - 1) / kChMergeThreads;
+        const size_t n_part = static_cast<size_t>(p.n_span[d]) * static_cast<size_t>(B * nx[d]);
+        p.off_best[d] = off;
+        off = round_up(off + n_part * 4, 256);
+        p.off_sub[d] = off;
+        off = round_up(off + n_part * 4, 256);
+        p.off_loss[d] = off;
+        off = round_up(off + static_cast<size_t>(B * p.n_mblk[d]) * 8, 256);
+    }
+    p.items0 = B * p.n_sb[0] * p.n_span[0];
+    p.items = p.items0 + B * p.n_sb[1] * p.n_span[1];
+    p.ws_bytes = off;
+    return p;
+}
+
+struct ChamferBwdPlan {
+    int64_t K = 0, nblocks = 0, hist_n = 0;
+    int passes = 0;
+    size_t off_keys[2] = {0, 0}, off_vals[2] = {0, 0}, off_hist = 0, off_row = 0, ws_bytes = 0;
+};
+
+ChamferBwdPlan plan_chamfer_bwd(int64_t B, int64_t N, int64_t M) {
+    ChamferBwdPlan p;
+    p.K = B * (N + M);
+    p.nblocks = (p.K + kRadixBlock - 1) / kRadixBlock;
+    p.hist_n = p.nblocks * kRadixBins;
+    int bits = 0;
+    while (bits < 32 && (int64_t(1) << bits) <= p.K) ++bits;  // keys are in [0, K]
+    p.passes = (bits + kRadixBits - 1) / kRadixBits;
+    size_t off = 0;
+    for (int i = 0; i < 2; ++i) {
+        p.off_keys[i] = off;
+        off = round_up(off + static_cast<size_t>(p.K) * 4, 256);
+        p.off_vals[i] = off;
+        off = round_up(off + static_cast<size_t>(p.K) * 4, 256);
+    }
+    p.off_hist = off;
+    off = round_up(off + static_cast<size_t>(p.hist_n) * 4, 256);
+    p.off_row = off;
+    off = round_up(off + static_cast<size_t>(p.K + 1) * 4, 256);
+    p.ws_bytes = p.K > 0 ? off : 0;
+    return p;
+}
+
+maxsim_status check_chamfer_shape(int64_t B, int64_t N, int64_t M, int64_t dim) {
+    if (B < 0 || N < 0 || M < 0 || dim <= 0) return MAXSIM_ERR_INVALID_ARG;
+    if (dim > kChMaxDim) return MAXSIM_ERR_UNSUPPORTED;
+    if (B * (N + M) >= kI32Max || B * (N + M) * dim >= (int64_t(1) << 40)) return MAXSIM_ERR_UNSUPPORTED;
+    return MAXSIM_OK;
+}
+
+template <int kD>
+maxsim_status launch_chamfer_nn(DeviceInfo* dev, int slot, const ChamferFwdArgs& a, int64_t items, cudaStream_t st) {
+    auto kern = chamfer_nn_kernel<kD>;
+    const size_t smem = ChamferShape<kD>::kSmem;
+    if (!dev->attrs_set[slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        dev->attrs_set[slot] = true;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kChThreads, smem) != cudaSuccess || per_sm < 1)
+        return MAXSIM_ERR_CUDA;
+    const int64_t grid = std::min<int64_t>(items, static_cast<int64_t>(dev->num_sms) * per_sm);
+    kern<<<static_cast<unsigned>(grid), kChThreads, smem, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace maxsim
 
@@ -641,6 +730,12 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
         off = round_up(off + static_cast<size_t>(Nq * Nd * Lq) * 4, 256);  // col
         return off;
     }
+    case MAXSIM_OP_CHAMFER_FWD:  // (B, N, M, unused, dim)
+        if (check_chamfer_shape(Nq, Lq, Nd, dim) == MAXSIM_ERR_INVALID_ARG) return static_cast<size_t>(-1);
+        return plan_chamfer_fwd(Nq, Lq, Nd, dim).ws_bytes;
+    case MAXSIM_OP_CHAMFER_BWD:
+        if (check_chamfer_shape(Nq, Lq, Nd, dim) == MAXSIM_ERR_INVALID_ARG) return static_cast<size_t>(-1);
+        return plan_chamfer_bwd(Nq, Lq, Nd).ws_bytes;
     default: return static_cast<size_t>(-1);
     }
 }
@@ -987,6 +1082,105 @@ maxsim_status maxsim_fwd_int8(const int8_t* Q, const float* q_scale, const int8_
         if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
     }
     return MAXSIM_OK;
+}
+
+maxsim_status maxsim_chamfer_fwd(const float* P, const float* Q, int64_t B, int64_t N, int64_t M, int64_t dim,
+                                 float* dist_p, int32_t* idx_p, float* dist_q, int32_t* idx_q, float* loss,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    maxsim_status rc = check_chamfer_shape(B, N, M, dim);
+    if (rc != MAXSIM_OK) return rc;
+    if (B == 0) return MAXSIM_OK;
+    if (B > 65535) return MAXSIM_ERR_UNSUPPORTED;  // grid.y of the merge
+    if (!loss || !aligned(loss, 4)) return MAXSIM_ERR_INVALID_ARG;
+    if (N > 0 && (!P || !aligned(P, 4) || !dist_p || !idx_p || !aligned(dist_p, 4) || !aligned(idx_p, 4)))
+        return MAXSIM_ERR_INVALID_ARG;
+    if (M > 0 && (!Q || !aligned(Q, 4) || !dist_q || !idx_q || !aligned(dist_q, 4) || !aligned(idx_q, 4)))
+        return MAXSIM_ERR_INVALID_ARG;
+    const ChamferFwdPlan p = plan_chamfer_fwd(B, N, M, dim);
+    if (workspace_bytes < p.ws_bytes || !workspace || !aligned(workspace, 256)) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    ChamferFwdArgs a{};
+    a.X[0] = P; a.Y[0] = Q; a.X[1] = Q; a.Y[1] = P;
+    a.nx[0] = N; a.ny[0] = M; a.nx[1] = M; a.ny[1] = N;
+    a.B = B;
+    a.dim = static_cast<int32_t>(dim);
+    a.items0 = p.items0;
+    a.items = p.items;
+    a.counter = reinterpret_cast<unsigned long long*>(ws + p.off_counter);
+    a.dist[0] = dist_p; a.idx[0] = idx_p; a.dist[1] = dist_q; a.idx[1] = idx_q;
+    for (int d = 0; d < 2; ++d) {
+        a.n_sb[d] = p.n_sb[d];
+        a.n_span[d] = p.n_span[d];
+        a.n_mblk[d] = p.n_mblk[d];
+        a.part_best[d] = reinterpret_cast<float*>(ws + p.off_best[d]);
+        a.part_sub[d] = reinterpret_cast<int32_t*>(ws + p.off_sub[d]);
+        a.loss_part[d] = reinterpret_cast<double*>(ws + p.off_loss[d]);
+    }
+    a.loss = loss;
+    a.status = dev->status;
+    if (p.items > 0) {
+        if (cudaMemsetAsync(a.counter, 0, sizeof(unsigned long long), st) != cudaSuccess) return MAXSIM_ERR_CUDA;
+        rc = p.kd == 3 ? launch_chamfer_nn<3>(dev, 12, a, p.items, st)
+                       : launch_chamfer_nn<kChMaxDim>(dev, 13, a, p.items, st);
+        if (rc != MAXSIM_OK) return rc;
+    }
+    const int64_t mblk = std::max(p.n_mblk[0], p.n_mblk[1]);
+    if (mblk > 0) {
+        chamfer_merge_kernel<<<dim3(static_cast<unsigned>(mblk), static_cast<unsigned>(B), 2), kChMergeThreads, 0,
+                               st>>>(a);
+    }
+    chamfer_loss_kernel<<<static_cast<unsigned>((B + 127) / 128), 128, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
+maxsim_status maxsim_chamfer_bwd(const float* P, const float* Q, int64_t B, int64_t N, int64_t M, int64_t dim,
+                                 const int32_t* idx_p, const int32_t* idx_q, const float* grad_loss, float* dP,
+                                 float* dQ, void* workspace, size_t workspace_bytes, void* stream) {
+    maxsim_status rc = check_chamfer_shape(B, N, M, dim);
+    if (rc != MAXSIM_OK) return rc;
+    if (B * (N + M) == 0) return MAXSIM_OK;
+    if (!grad_loss || !aligned(grad_loss, 4)) return MAXSIM_ERR_INVALID_ARG;
+    if (N > 0 && (!P || !aligned(P, 4) || !idx_p || !aligned(idx_p, 4) || !dP || !aligned(dP, 4)))
+        return MAXSIM_ERR_INVALID_ARG;
+    if (M > 0 && (!Q || !aligned(Q, 4) || !idx_q || !aligned(idx_q, 4) || !dQ || !aligned(dQ, 4)))
+        return MAXSIM_ERR_INVALID_ARG;
+    const ChamferBwdPlan p = plan_chamfer_bwd(B, N, M);
+    if (workspace_bytes < p.ws_bytes || !workspace || !aligned(workspace, 256)) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint32_t* keys[2] = {reinterpret_cast<uint32_t*>(ws + p.off_keys[0]), reinterpret_cast<uint32_t*>(ws + p.off_keys[1])};
+    int32_t* vals[2] = {reinterpret_cast<int32_t*>(ws + p.off_vals[0]), reinterpret_cast<int32_t*>(ws + p.off_vals[1])};
+    int32_t* hist = reinterpret_cast<int32_t*>(ws + p.off_hist);
+    int32_t* row_ptr = reinterpret_cast<int32_t*>(ws + p.off_row);
+    ch_keys_kernel<<<grid_for(p.K, 256, dev->num_sms), 256, 0, st>>>(idx_p, idx_q, B, N, M, keys[0], vals[0],
+                                                                     dev->status);
+    int cur = 0;
+    for (int pass = 0; pass < p.passes; ++pass) {
+        const int shift = pass * kRadixBits;
+        radix_hist_kernel<<<static_cast<unsigned>(p.nblocks), kRadixThreads, 0, st>>>(keys[cur], p.K, shift, hist,
+                                                                                     p.nblocks);
+        scan_exclusive_kernel<<<1, kScanThreads, 0, st>>>(hist, p.hist_n);
+        radix_scatter_kernel<<<static_cast<unsigned>(p.nblocks), kRadixThreads, 0, st>>>(
+            keys[cur], vals[cur], p.K, shift, hist, p.nblocks, keys[cur ^ 1], vals[cur ^ 1]);
+        cur ^= 1;
+    }
+    ch_row_ptr_kernel<<<grid_for(p.K + 1, 256, dev->num_sms), 256, 0, st>>>(keys[cur], p.K, p.K, row_ptr);
+    ChamferBwdArgs g{};
+    g.P = P; g.Q = Q; g.B = B; g.N = N; g.M = M;
+    g.dim = static_cast<int32_t>(dim);
+    g.idx_p = idx_p; g.idx_q = idx_q; g.g = grad_loss;
+    g.dP = dP; g.dQ = dQ;
+    g.row_ptr = row_ptr;
+    g.col = vals[cur];
+    const int grid = grid_for(p.K, 256, dev->num_sms);
+    if (dim <= 3) chamfer_grad_kernel<3><<<grid, 256, 0, st>>>(g);
+    else chamfer_grad_kernel<kChMaxDim><<<grid, 256, 0, st>>>(g);
+    return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -219,6 +219,59 @@ def maxsim_fwd_int8(Q: torch.Tensor, q_scale: torch.Tensor, D: torch.Tensor, d_s
     return scores, argmax, win
 
 
+def _points(P: torch.Tensor, Q: torch.Tensor):
+    if P.dim() != 3 or Q.dim() != 3 or P.shape[0] != Q.shape[0] or P.shape[2] != Q.shape[2]:
+        raise ValueError("P must be [B, N, dim] and Q [B, M, dim]")
+    dev = P.device
+    return _contig(P, "P", torch.float32), _contig(Q, "Q", torch.float32, dev), dev
+
+
+def chamfer_fwd(P: torch.Tensor, Q: torch.Tensor, *, workspace: Optional[torch.Tensor] = None):
+    """Chamfer distance of B pairs of point sets P [B,N,dim], Q [B,M,dim] (f32).
+
+    Returns (loss [B], dist_p [B,N], idx_p [B,N] i32, dist_q [B,M], idx_q [B,M] i32).
+    """
+    P, Q, dev = _points(P, Q)
+    B, N, dim = P.shape
+    M = Q.shape[1]
+    loss = torch.empty(B, dtype=torch.float32, device=dev)
+    dist_p = torch.empty((B, N), dtype=torch.float32, device=dev)
+    idx_p = torch.empty((B, N), dtype=torch.int32, device=dev)
+    dist_q = torch.empty((B, M), dtype=torch.float32, device=dev)
+    idx_q = torch.empty((B, M), dtype=torch.int32, device=dev)
+    ws, nbytes = _workspace(workspace_size(_native.OP_CHAMFER_FWD, B, N, M, 0, dim), dev, workspace)
+    rc = _native.lib().maxsim_chamfer_fwd(_ptr(P), _ptr(Q), B, N, M, dim, _ptr(dist_p), _ptr(idx_p), _ptr(dist_q),
+                                          _ptr(idx_q), _ptr(loss), _ptr(ws), nbytes, _stream(dev))
+    _native.check(rc, "maxsim_chamfer_fwd")
+    return loss, dist_p, idx_p, dist_q, idx_q
+
+
+def chamfer_bwd(P: torch.Tensor, Q: torch.Tensor, idx_p: torch.Tensor, idx_q: torch.Tensor, grad_loss: torch.Tensor,
+                *, dP: Optional[torch.Tensor] = None, dQ: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None):
+    """(dP [B,N,dim], dQ [B,M,dim]) f32 of sum_b grad_loss[b] * CD(P_b, Q_b)."""
+    P, Q, dev = _points(P, Q)
+    B, N, dim = P.shape
+    M = Q.shape[1]
+    ip = _contig(idx_p, "idx_p", torch.int32, dev)
+    iq = _contig(idx_q, "idx_q", torch.int32, dev)
+    g = _contig(grad_loss, "grad_loss", torch.float32, dev)
+    if ip.numel() != B * N or iq.numel() != B * M or g.numel() != B:
+        raise ValueError("idx_p must be [B, N], idx_q [B, M] and grad_loss [B]")
+    if dP is None:
+        dP = torch.empty((B, N, dim), dtype=torch.float32, device=dev)
+    if dQ is None:
+        dQ = torch.empty((B, M, dim), dtype=torch.float32, device=dev)
+    for t, shape, name in ((dP, (B, N, dim), "dP"), (dQ, (B, M, dim), "dQ")):
+        if tuple(t.shape) != shape or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 tensor of shape {shape}")
+    ws, nbytes = _workspace(workspace_size(_native.OP_CHAMFER_BWD, B, N, M, 0, dim), dev, workspace)
+    rc = _native.lib().maxsim_chamfer_bwd(_ptr(P), _ptr(Q), B, N, M, dim, _ptr(ip), _ptr(iq), _ptr(g), _ptr(dP),
+                                          _ptr(dQ), _ptr(ws), nbytes, _stream(dev))
+    _native.check(rc, "maxsim_chamfer_bwd")
+    return dP, dQ
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device status word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)

@@ -95,3 +95,37 @@ def test_workspace_sizes(lib):
     assert ws(4, 32, 32, 1000, 5000, 128) >= ws(1, 32, 32, 1000, 50000, 128) + 4 * (32 * 4 + 5000)  # + grouping
     assert ws(9, 1, 1, 1, 1, 16) == ctypes.c_size_t(-1).value
     assert ws(0, -1, 1, 1, 1, 16) == ctypes.c_size_t(-1).value
+
+
+def test_chamfer_host_validation(lib):
+    f, b = lib.maxsim_chamfer_fwd, lib.maxsim_chamfer_bwd
+    # P, Q, B, N, M, dim, dist_p, idx_p, dist_q, idx_q, loss, ws, bytes, stream
+    need = lib.maxsim_workspace_size(5, 2, 100, 70, 0, 3)
+    assert f(FAKE, FAKE, 0, 100, 70, 3, None, None, None, None, None, None, 0, None) == 0   # nothing to do
+    assert f(FAKE, FAKE, 2, 100, 70, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 1  # dim 0
+    assert f(FAKE, FAKE, 2, 100, 70, 9, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 2  # dim > 8
+    assert f(FAKE, FAKE, 2, -1, 70, 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 1
+    assert f(FAKE, FAKE, 2, 100, 70, 3, FAKE, FAKE, FAKE, FAKE, None, FAKE, need, None) == 1  # no loss
+    assert f(FAKE, None, 2, 100, 70, 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 1  # no Q
+    assert f(FAKE + 2, FAKE, 2, 100, 70, 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 1  # misaligned
+    assert f(FAKE, FAKE, 2, 100, 70, 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need - 1, None) == 5
+    assert f(FAKE, FAKE, 2, 100, 70, 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 16, need, None) == 5  # ws alignment
+    # P, Q, B, N, M, dim, idx_p, idx_q, grad, dP, dQ, ws, bytes, stream
+    nb = lib.maxsim_workspace_size(6, 2, 100, 70, 0, 3)
+    assert b(FAKE, FAKE, 2, 0, 0, 3, None, None, None, None, None, None, 0, None) == 0
+    assert b(FAKE, FAKE, 2, 100, 70, 3, FAKE, FAKE, None, FAKE, FAKE, FAKE, nb, None) == 1  # no grad
+    assert b(FAKE, FAKE, 2, 100, 70, 3, FAKE, None, FAKE, FAKE, FAKE, FAKE, nb, None) == 1  # no idx_q
+    assert b(FAKE, FAKE, 2, 100, 70, 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, nb - 1, None) == 5
+
+
+def test_chamfer_workspace_sizes(lib):
+    ws = lib.maxsim_workspace_size
+    B, N, M = 2, 5000, 9000
+    # per direction: one (min, sub-tile) pair per source and 4096-target span
+    spans_p, spans_q = -(-M // 4096), -(-N // 4096)
+    assert ws(5, B, N, M, 0, 3) >= 8 * B * (N * spans_p + M * spans_q)
+    assert ws(5, B, N, M, 0, 8) == ws(5, B, N, M, 0, 3)
+    # two key / value buffers, the row pointers
+    assert ws(6, B, N, M, 0, 3) >= 16 * B * (N + M) + 4 * (B * (N + M) + 1)
+    assert ws(6, 0, 0, 0, 0, 3) == 0
+    assert ws(5, 1, 1, 1, 0, 0) == ctypes.c_size_t(-1).value
