@@ -128,10 +128,11 @@ def kernel_source_hash(workload: str) -> str:
 
 # DRAM traffic (read + write bytes) of the forward kernel per launch on a
 # workload's default size, scaled by the document tokens from one ncu capture
-# of a smaller instance (profiles/maxsim_fwd_kernel__colbert_varlen.md,
-# profiles/maxsim_fwd_kernel_pair_int8__int8_rerank.md); valid only for the
-# kernel sources whose hash is recorded with it.
+# of a smaller instance (profiles/maxsim_fwd_kernel__colbert_varlen.md); valid
+# only for the kernel sources whose hash is recorded with it.
 MEASURED_TRAFFIC = {
+    # (429,040,896 + 3,935,744) B at 1,657,544 tokens, x 16,644,526 / 1,657,544
+    ("colbert_varlen", "c2e4f8f82dea2e36"): 4347812753,
 }
 
 
@@ -211,7 +212,10 @@ def make_workload(name: str, rank: int, world: int, shard: str, nd: int = 0):
     if shard == "weak":
         spec["seed"] = spec["seed"] + 1000 * rank  # every rank scores its own documents
     if nd:
-        spec["Nd"] = nd  # smaller instance for profiler captures only
+        if name.startswith("chamfer"):
+            spec["N"] = spec["M"] = nd  # smaller clouds for profiler captures only
+        else:
+            spec["Nd"] = nd  # smaller instance for profiler captures only
     w = workloads.make(name, **spec)
     w["name"] = name
     if shard == "global" and world > 1:
@@ -537,7 +541,7 @@ class ChamferCase:
         self.bytes = (B * (N + M) * dim * 4) * 2 + B * (N + M) * 8
         self.bound, self.dtype = "alu", "f32"
         K = B * (N + M)
-        passes = max(1, -(-int(K).bit_length() // 8))
+        passes = max(1, -(-int(K).bit_length() // 9))  # 9-bit digits
         self.launches = 3 + 1 + 3 * passes + 2  # nn, merge, loss | keys, radix passes, row_ptr, grad
         self.events = None
         self.loss = None
@@ -714,7 +718,8 @@ def main():
     ap.add_argument("--shard", choices=["weak", "global"], default="weak")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--nd", type=int, default=0, help="override the document count (profiler captures only)")
+    ap.add_argument("--nd", type=int, default=0,
+                    help="override the document count, or the cloud size for Chamfer (profiler captures only)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

@@ -11,9 +11,11 @@
 //  * min_t ||x - y_t||^2 = ||x||^2 + min_t (||y_t||^2 - 2 <x, y_t>): the
 //    search runs on the shifted value d'(x, y) = fma chain of x_k * (-2 y_k)
 //    starting from ||y||^2, which shared memory holds precomputed per target;
-//  * two targets go through one fma.rn.f32x2 (each lane a single-rounded fma,
-//    the same value as scalar fmaf), and a three-input min folds both into
-//    the running minimum;
+//  * targets sit in shared memory in pairs, coordinate-interleaved, so two
+//    16-byte broadcast loads feed 2 x kD FMAs per source, and a three-input
+//    min folds both targets into the source's running minimum (the packed
+//    fma.rn.f32x2 form was measured slower: it occupies the FMA pipe as long
+//    as two scalar FMAs and stalls on dispatch);
 //  * the argmin is not tracked per pair: every 32 targets (a sub-tile) each
 //    source records the sub-tile in which its minimum last dropped; once the
 //    search is over, a second kernel recomputes d' bit for bit over that one
@@ -75,16 +77,6 @@ struct ChamferFwdArgs {
     int* status;
 };
 
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
-}
-
-__device__ __forceinline__ uint64_t fma2_rn(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
 __device__ __forceinline__ float min3f(float a, float b, float c) {
     float d;
     asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -99,7 +91,7 @@ __device__ __forceinline__ float ch_norm2(const float* y, int dim) {
 }
 
 template <int kD>
-__global__ void __launch_bounds__(kChThreads, 1) chamfer_nn_kernel(ChamferFwdArgs a) {
+__global__ void __launch_bounds__(kChThreads, 2) chamfer_nn_kernel(ChamferFwdArgs a) {
     using S = ChamferShape<kD>;
     constexpr int kSrc = S::kSrc;
     constexpr int kV = S::kPairFloats / 4;  // 16-byte vectors per target pair
@@ -126,8 +118,7 @@ __global__ void __launch_bounds__(kChThreads, 1) chamfer_nn_kernel(ChamferFwdArg
         const float* Xb = (dir ? a.X[1] : a.X[0]) + b * nx * dim;
         const float* Yb = (dir ? a.Y[1] : a.Y[0]) + b * ny * dim;
 
-        // sources: (x_k, x_k) pairs in registers
-        uint64_t xx[kSrc][kD];
+        float xx[kSrc][kD];
         float m[kSrc], best[kSrc];
         int32_t sub_of[kSrc];
 #pragma unroll
@@ -135,8 +126,7 @@ __global__ void __launch_bounds__(kChThreads, 1) chamfer_nn_kernel(ChamferFwdArg
             const int64_t src = sb * S::kSources + s * kChThreads + tid;
 #pragma unroll
             for (int k = 0; k < kD; ++k) {
-                const float v = (src < nx && k < dim) ? Xb[src * dim + k] : 0.f;
-                xx[s][k] = f2_pack(v, v);
+                xx[s][k] = (src < nx && k < dim) ? Xb[src * dim + k] : 0.f;
             }
             m[s] = __int_as_float(0x7f800000);
             best[s] = m[s];
@@ -170,24 +160,27 @@ __global__ void __launch_bounds__(kChThreads, 1) chamfer_nn_kernel(ChamferFwdArg
             __syncthreads();
             const int64_t sub0 = t0 / kChSub;
             for (int st = 0; st < n_sub; ++st) {
-                const ulonglong2* tp = reinterpret_cast<const ulonglong2*>(ch_tile) +
-                                       static_cast<int64_t>(st) * (kChSub / 2) * kV;
+                const float4* tp = reinterpret_cast<const float4*>(ch_tile) + static_cast<int64_t>(st) * (kChSub / 2) * kV;
 #pragma unroll S::kUnroll
                 for (int j = 0; j < kChSub / 2; ++j) {
-                    uint64_t c[2 * kV];
+                    float c[4 * kV];  // (-2 y_k of the two targets) for each k, then the two norms
 #pragma unroll
                     for (int v = 0; v < kV; ++v) {
-                        const ulonglong2 q = tp[j * kV + v];
-                        c[2 * v] = q.x;
-                        c[2 * v + 1] = q.y;
+                        const float4 q = tp[j * kV + v];
+                        c[4 * v] = q.x;
+                        c[4 * v + 1] = q.y;
+                        c[4 * v + 2] = q.z;
+                        c[4 * v + 3] = q.w;
                     }
 #pragma unroll
                     for (int s = 0; s < kSrc; ++s) {
-                        uint64_t acc = c[kD];  // (||y_t||^2, ||y_t+1||^2)
+                        float d0 = c[2 * kD], d1 = c[2 * kD + 1];
 #pragma unroll
-                        for (int k = 0; k < kD; ++k) acc = fma2_rn(xx[s][k], c[k], acc);
-                        m[s] = min3f(m[s], __uint_as_float(static_cast<uint32_t>(acc)),
-                                     __uint_as_float(static_cast<uint32_t>(acc >> 32)));
+                        for (int k = 0; k < kD; ++k) {
+                            d0 = __fmaf_rn(xx[s][k], c[2 * k], d0);
+                            d1 = __fmaf_rn(xx[s][k], c[2 * k + 1], d1);
+                        }
+                        m[s] = min3f(m[s], d0, d1);
                     }
                 }
 #pragma unroll
@@ -212,7 +205,15 @@ __global__ void __launch_bounds__(kChThreads, 1) chamfer_nn_kernel(ChamferFwdArg
 }
 
 // Merge of the spans, exact argmin inside the winning sub-tile, distance of
-// the winner, and the block's share of the loss. Grid (blocks, B, 2).
+// the winner, and the block's share of the loss. Grid (blocks, B, 2); a
+// block covers kChMergeThreads sources, a warp 32 of them:
+//  * lane l merges the spans of source l in span order (strict <: the
+//    earliest span keeps a tie);
+//  * then, four sources at a time, lane t recomputes d' for target t of each
+//    winning sub-tile (the operations of the search, in its order), and the
+//    first lane whose value equals the minimum holds the argmin; that lane
+//    computes the distance sum_k (x_k - y_k)^2 directly.
+constexpr int kChMergeGroup = 4;
 __global__ void __launch_bounds__(kChMergeThreads) chamfer_merge_kernel(ChamferFwdArgs a) {
     const int dir = blockIdx.z;
     const int64_t b = blockIdx.y;
@@ -220,79 +221,127 @@ __global__ void __launch_bounds__(kChMergeThreads) chamfer_merge_kernel(ChamferF
     const int64_t n_mblk = dir ? a.n_mblk[1] : a.n_mblk[0], n_span = dir ? a.n_span[1] : a.n_span[0];
     const float* part_best = dir ? a.part_best[1] : a.part_best[0];
     const int32_t* part_sub = dir ? a.part_sub[1] : a.part_sub[0];
+    const float* X = (dir ? a.X[1] : a.X[0]) + b * nx * a.dim;
+    const float* Yb = (dir ? a.Y[1] : a.Y[0]) + b * ny * a.dim;
     const int dim = a.dim;
     if (static_cast<int64_t>(blockIdx.x) >= n_mblk) return;
-    const int64_t src = static_cast<int64_t>(blockIdx.x) * kChMergeThreads + threadIdx.x;
-    float d2 = 0.f;
-    if (src < nx) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t src0 = static_cast<int64_t>(blockIdx.x) * kChMergeThreads + warp * 32;
+    const int64_t my_src = src0 + lane;
+    const bool mine = my_src < nx;
+    // this lane's source: merge its spans
+    float best = __int_as_float(0x7f800000);
+    int32_t sub = -1;
+    if (mine) {
         const int64_t stride = a.B * nx;
-        float best = __int_as_float(0x7f800000);
-        int32_t sub = -1;
-        for (int64_t s = 0; s < n_span; ++s) {
-            const float v = part_best[s * stride + b * nx + src];
+        for (int64_t sp = 0; sp < n_span; ++sp) {
+            const float v = part_best[sp * stride + b * nx + my_src];
             if (v < best) {
                 best = v;
-                sub = part_sub[s * stride + b * nx + src];
+                sub = part_sub[sp * stride + b * nx + my_src];
             }
         }
-        const float* x = (dir ? a.X[1] : a.X[0]) + (b * nx + src) * dim;
-        const float* Yb = (dir ? a.Y[1] : a.Y[0]) + b * ny * dim;
-        float xv[kChMaxDim];
-#pragma unroll
-        for (int k = 0; k < kChMaxDim; ++k) xv[k] = k < dim ? x[k] : 0.f;
-        int32_t arg = -1;
-        if (sub >= 0) {
-            const int64_t t_lo = static_cast<int64_t>(sub) * kChSub;
-            const int64_t t_hi = t_lo + kChSub < ny ? t_lo + kChSub : ny;
-            for (int64_t t = t_lo; t < t_hi; ++t) {
-                const float* y = Yb + t * dim;
-                float acc = ch_norm2(y, dim);
-#pragma unroll
-                for (int k = 0; k < kChMaxDim; ++k)
-                    if (k < dim) acc = __fmaf_rn(xv[k], __fmul_rn(-2.f, y[k]), acc);
-                if (acc == best) {
-                    arg = static_cast<int32_t>(t);
-                    break;
-                }
-            }
-            if (arg < 0 && a.status) atomicCAS(a.status, 0, 6);  // a recomputation that disagrees
-        }
-        if (arg >= 0) {
-            const float* y = Yb + static_cast<int64_t>(arg) * dim;
-            const float e0 = __fsub_rn(xv[0], y[0]);
-            d2 = __fmul_rn(e0, e0);
-#pragma unroll
-            for (int k = 1; k < kChMaxDim; ++k) {
-                if (k < dim) {
-                    const float e = __fsub_rn(xv[k], y[k]);
-                    d2 = __fmaf_rn(e, e, d2);
-                }
-            }
-        }
-        (dir ? a.dist[1] : a.dist[0])[b * nx + src] = d2;
-        (dir ? a.idx[1] : a.idx[0])[b * nx + src] = arg;
     }
-    // the block's share of sum(dist): a fixed-order tree in double
-    __shared__ double part[kChMergeThreads];
-    part[threadIdx.x] = static_cast<double>(d2);
+    float my_x[kChMaxDim];
+#pragma unroll
+    for (int k = 0; k < kChMaxDim; ++k) my_x[k] = (mine && k < dim) ? X[my_src * dim + k] : 0.f;
+    float my_d2 = 0.f;
+    int32_t my_arg = -1;
+    for (int i0 = 0; i0 < 32; i0 += kChMergeGroup) {
+        float yv[kChMergeGroup][kChMaxDim];
+        int32_t sb[kChMergeGroup];
+        float bv[kChMergeGroup];
+#pragma unroll
+        for (int g = 0; g < kChMergeGroup; ++g) {
+            sb[g] = __shfl_sync(0xFFFFFFFFu, sub, i0 + g);
+            bv[g] = __shfl_sync(0xFFFFFFFFu, best, i0 + g);
+            const int64_t t = static_cast<int64_t>(sb[g]) * kChSub + lane;
+            const bool ok = sb[g] >= 0 && t < ny;
+#pragma unroll
+            for (int k = 0; k < kChMaxDim; ++k) yv[g][k] = (ok && k < dim) ? Yb[t * dim + k] : 0.f;
+        }
+#pragma unroll
+        for (int g = 0; g < kChMergeGroup; ++g) {
+            if (sb[g] < 0) continue;  // warp-uniform
+            float xv[kChMaxDim];
+#pragma unroll
+            for (int k = 0; k < kChMaxDim; ++k) xv[k] = __shfl_sync(0xFFFFFFFFu, my_x[k], i0 + g);
+            const int64_t t = static_cast<int64_t>(sb[g]) * kChSub + lane;
+            float acc = __fmul_rn(yv[g][0], yv[g][0]);
+#pragma unroll
+            for (int k = 1; k < kChMaxDim; ++k)
+                if (k < dim) acc = __fmaf_rn(yv[g][k], yv[g][k], acc);
+#pragma unroll
+            for (int k = 0; k < kChMaxDim; ++k)
+                if (k < dim) acc = __fmaf_rn(xv[k], __fmul_rn(-2.f, yv[g][k]), acc);
+            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, t < ny && acc == bv[g]);
+            if (hit == 0u) {
+                if (lane == 0 && a.status) atomicCAS(a.status, 0, 6);  // a recomputation that disagrees
+                continue;
+            }
+            const int w = __ffs(hit) - 1;
+            float d2 = 0.f;
+            if (lane == w) {
+                const float e0 = __fsub_rn(xv[0], yv[g][0]);
+                d2 = __fmul_rn(e0, e0);
+#pragma unroll
+                for (int k = 1; k < kChMaxDim; ++k) {
+                    if (k < dim) {
+                        const float e = __fsub_rn(xv[k], yv[g][k]);
+                        d2 = __fmaf_rn(e, e, d2);
+                    }
+                }
+            }
+            d2 = __shfl_sync(0xFFFFFFFFu, d2, w);
+            if (lane == i0 + g) {
+                my_d2 = d2;
+                my_arg = static_cast<int32_t>(static_cast<int64_t>(sb[g]) * kChSub + w);
+            }
+        }
+    }
+    if (mine) {
+        (dir ? a.dist[1] : a.dist[0])[b * nx + my_src] = my_d2;
+        (dir ? a.idx[1] : a.idx[0])[b * nx + my_src] = my_arg;
+    }
+    // the block's share of sum(dist): fixed-order trees in double
+    double sum = static_cast<double>(my_d2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    __shared__ double wsum[kChMergeThreads / 32];
+    if (lane == 0) wsum[warp] = sum;
     __syncthreads();
-    for (int w = kChMergeThreads / 2; w > 0; w >>= 1) {
-        if (static_cast<int>(threadIdx.x) < w) part[threadIdx.x] += part[threadIdx.x + w];
-        __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < kChMergeThreads / 32; ++w) t += wsum[w];
+        (dir ? a.loss_part[1] : a.loss_part[0])[b * n_mblk + blockIdx.x] = t;
     }
-    if (threadIdx.x == 0) (dir ? a.loss_part[1] : a.loss_part[0])[b * n_mblk + blockIdx.x] = part[0];
 }
 
-// loss[b] = sum(dist_p[b]) / N + sum(dist_q[b]) / M (0 if N or M is 0).
-__global__ void chamfer_loss_kernel(ChamferFwdArgs a) {
-    const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (b >= a.B) return;
-    double sp = 0.0, sq = 0.0;
-    for (int64_t k = 0; k < a.n_mblk[0]; ++k) sp += a.loss_part[0][b * a.n_mblk[0] + k];
-    for (int64_t k = 0; k < a.n_mblk[1]; ++k) sq += a.loss_part[1][b * a.n_mblk[1] + k];
-    const int64_t N = a.nx[0], M = a.nx[1];
-    a.loss[b] = (N > 0 && M > 0) ? static_cast<float>(sp / static_cast<double>(N) + sq / static_cast<double>(M))
-                                 : 0.f;
+// loss[b] = sum(dist_p[b]) / N + sum(dist_q[b]) / M (0 if N or M is 0); one
+// block per pair of sets, the partial sums added in a fixed order.
+constexpr int kChLossThreads = 256;
+__global__ void __launch_bounds__(kChLossThreads) chamfer_loss_kernel(ChamferFwdArgs a) {
+    const int64_t b = blockIdx.x;
+    __shared__ double red[2][kChLossThreads];
+    double s0 = 0.0, s1 = 0.0;
+    for (int64_t k = threadIdx.x; k < a.n_mblk[0]; k += kChLossThreads) s0 += a.loss_part[0][b * a.n_mblk[0] + k];
+    for (int64_t k = threadIdx.x; k < a.n_mblk[1]; k += kChLossThreads) s1 += a.loss_part[1][b * a.n_mblk[1] + k];
+    red[0][threadIdx.x] = s0;
+    red[1][threadIdx.x] = s1;
+    __syncthreads();
+    for (int w = kChLossThreads / 2; w > 0; w >>= 1) {
+        if (static_cast<int>(threadIdx.x) < w) {
+            red[0][threadIdx.x] += red[0][threadIdx.x + w];
+            red[1][threadIdx.x] += red[1][threadIdx.x + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const int64_t N = a.nx[0], M = a.nx[1];
+        a.loss[b] = (N > 0 && M > 0) ? static_cast<float>(red[0][0] / static_cast<double>(N) +
+                                                           red[1][0] / static_cast<double>(M))
+                                     : 0.f;
+    }
 }
 
 // ---------------------------------------------------------------- backward
@@ -320,57 +369,64 @@ __global__ void ch_keys_kernel(const int32_t* __restrict__ idx_p, const int32_t*
     }
 }
 
-constexpr int kRadixBits = 8;
+constexpr int kRadixBits = 9;
 constexpr int kRadixBins = 1 << kRadixBits;
 constexpr int kRadixThreads = 256;
-constexpr int kRadixPerThread = 4;
+constexpr int kRadixPerThread = 16;
 constexpr int kRadixBlock = kRadixThreads * kRadixPerThread;  // keys per block
-static_assert(kRadixBins == kRadixThreads, "one bin per thread");
+static_assert(kRadixBins % kRadixThreads == 0, "bins per thread");
 
-// Per-block counts of one 8-bit digit, stored bin-major: hist[bin * blocks + block].
+// Per-block counts of one digit, stored bin-major: hist[bin * blocks + block].
 __global__ void __launch_bounds__(kRadixThreads) radix_hist_kernel(const uint32_t* __restrict__ keys, int64_t n,
                                                                    int shift, int32_t* __restrict__ hist,
                                                                    int64_t nblocks) {
     __shared__ int32_t h[kRadixBins];
-    h[threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < kRadixBins; i += kRadixThreads) h[i] = 0;
     __syncthreads();
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kRadixBlock;
-#pragma unroll
+#pragma unroll 4
     for (int e = 0; e < kRadixPerThread; ++e) {
         const int64_t i = base + e * kRadixThreads + threadIdx.x;
         if (i < n) atomicAdd(&h[(keys[i] >> shift) & (kRadixBins - 1)], 1);
     }
     __syncthreads();
-    hist[static_cast<int64_t>(threadIdx.x) * nblocks + blockIdx.x] = h[threadIdx.x];
+    for (int i = threadIdx.x; i < kRadixBins; i += kRadixThreads)
+        hist[static_cast<int64_t>(i) * nblocks + blockIdx.x] = h[i];
 }
 
-// Exclusive prefix sum in place over n int32 by one block of 1024 threads:
-// each thread scans 16 consecutive values per pass, then the threads' totals
-// are scanned with warp shuffles.
+// Exclusive prefix sum in place over n int32 by one block of 1024 threads,
+// 8192 values per pass: warp w scans its 256 consecutive values as 8 rows
+// of 32 (coalesced loads, shuffle scans, a running carry), then the 32 warp
+// totals are scanned and added.
 constexpr int kScanThreads = 1024;
-constexpr int kScanPer = 16;
+constexpr int kScanRows = 8;
 __global__ void __launch_bounds__(kScanThreads) scan_exclusive_kernel(int32_t* __restrict__ a, int64_t n) {
     __shared__ int32_t wsum[32];
     __shared__ int32_t carry;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
-    for (int64_t base = 0; base < n; base += static_cast<int64_t>(kScanThreads) * kScanPer) {
-        const int64_t i0 = base + static_cast<int64_t>(threadIdx.x) * kScanPer;
-        int32_t v[kScanPer];
-        int32_t tot = 0;
+    for (int64_t base = 0; base < n; base += static_cast<int64_t>(kScanThreads) * kScanRows) {
+        const int64_t w0 = base + static_cast<int64_t>(warp) * 32 * kScanRows;
+        int32_t v[kScanRows], incl[kScanRows];
 #pragma unroll
-        for (int e = 0; e < kScanPer; ++e) {
-            v[e] = i0 + e < n ? a[i0 + e] : 0;
-            tot += v[e];
+        for (int r = 0; r < kScanRows; ++r) {
+            const int64_t i = w0 + r * 32 + lane;
+            v[r] = i < n ? a[i] : 0;
         }
-        int32_t x = tot;
+        int32_t run = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-            if (lane >= o) x += y;
+        for (int r = 0; r < kScanRows; ++r) {
+            int32_t x = v[r];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            incl[r] = run + x;
+            run += __shfl_sync(0xFFFFFFFFu, x, 31);
         }
-        if (lane == 31) wsum[warp] = x;
+        if (lane == 0) wsum[warp] = run;
         __syncthreads();
         if (warp == 0) {
             int32_t w = wsum[lane];
@@ -382,14 +438,14 @@ __global__ void __launch_bounds__(kScanThreads) scan_exclusive_kernel(int32_t* _
             wsum[lane] = w;
         }
         __syncthreads();
-        int32_t run = carry + (warp > 0 ? wsum[warp - 1] : 0) + x - tot;
+        const int32_t prefix = carry + (warp > 0 ? wsum[warp - 1] : 0);
 #pragma unroll
-        for (int e = 0; e < kScanPer; ++e) {
-            if (i0 + e < n) a[i0 + e] = run;
-            run += v[e];
+        for (int r = 0; r < kScanRows; ++r) {
+            const int64_t i = w0 + r * 32 + lane;
+            if (i < n) a[i] = prefix + incl[r] - v[r];
         }
         __syncthreads();
-        if (threadIdx.x == kScanThreads - 1) carry = run;
+        if (threadIdx.x == 0) carry += wsum[31];
         __syncthreads();
     }
 }
@@ -403,7 +459,8 @@ __global__ void __launch_bounds__(kRadixThreads) radix_scatter_kernel(
     int32_t* __restrict__ vals_out) {
     __shared__ int32_t run[kRadixBins];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    run[threadIdx.x] = offs[static_cast<int64_t>(threadIdx.x) * nblocks + blockIdx.x];
+    for (int i = threadIdx.x; i < kRadixBins; i += kRadixThreads)
+        run[i] = offs[static_cast<int64_t>(i) * nblocks + blockIdx.x];
     __syncthreads();
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kRadixBlock;
     for (int e = 0; e < kRadixPerThread; ++e) {

@@ -1132,7 +1132,7 @@ maxsim_status maxsim_chamfer_fwd(const float* P, const float* Q, int64_t B, int6
         chamfer_merge_kernel<<<dim3(static_cast<unsigned>(mblk), static_cast<unsigned>(B), 2), kChMergeThreads, 0,
                                st>>>(a);
     }
-    chamfer_loss_kernel<<<static_cast<unsigned>((B + 127) / 128), 128, 0, st>>>(a);
+    chamfer_loss_kernel<<<static_cast<unsigned>(B), kChLossThreads, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
 }
 

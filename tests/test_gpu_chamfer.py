@@ -175,6 +175,27 @@ def test_backward_is_bitwise_reproducible_and_hubs():
     assert np.allclose(a[0], rP, rtol=1e-5, atol=1e-7) and np.allclose(a[1], rQ, rtol=1e-4, atol=1e-6)
 
 
+def test_backward_matches_an_fp32_model_bit_for_bit():
+    # the kernel's own fp32 operations, in ascending source order along every
+    # inverse row: equal to the last bit only if the inverse index is stable
+    # and the formula is the stated one
+    P, Q = clouds(37, 2, 300, 220, 3)
+    _, ip, iq = check_fwd(P, Q)
+    g = np.array([0.3, -1.7], np.float32)
+    dP, dQ = bwd(P, Q, ip, iq, g)
+    f = np.float32
+    for b in range(2):
+        for X, Y, near, inv_src, got in ((P[b], Q[b], ip[b], iq[b], dP[b]), (Q[b], P[b], iq[b], ip[b], dQ[b])):
+            wx = f(f(2) * g[b]) / f(len(X))
+            wy = f(f(2) * g[b]) / f(len(Y))
+            for x in range(len(X)):
+                inv = np.zeros(X.shape[1], np.float32)
+                for y in np.nonzero(inv_src == x)[0]:  # ascending
+                    inv = inv + (Y[y] - X[x])
+                own = wx * (X[x] - Y[near[x]])
+                assert np.array_equal(got[x], own - wy * inv), (b, x)
+
+
 def test_backward_bad_index_is_reported_and_skipped():
     P, Q = clouds(23, 1, 200, 300, 3)
     _, ip, iq = check_fwd(P, Q)
