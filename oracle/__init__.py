@@ -12,6 +12,11 @@ Functions
                            and the int32 dot product at the argmax
   csr                    : inverse-argmax CSR (row_ptr, col)
   bwd                    : dQ, dD through the saved argmax (+ the CSR)
+  chamfer_fwd / _bwd     : Chamfer distance of point sets and its gradient
+  topk                   : the k largest values of every row (descending,
+                           lower index first among equal values)
+  two_stage_topk         : INT8 scores over the whole corpus, top-k1
+                           candidates, f16 / bf16 rescoring, top-k
 See the C source for the page sections each one follows.
 """
 from __future__ import annotations
@@ -223,3 +228,42 @@ def chamfer_bwd(P, Q, idx_p, idx_q, grad):
     if rc:
         raise ValueError(f"oracle_chamfer_bwd failed ({rc})")
     return dP, dQ
+
+
+def topk(scores, k):
+    """The k largest values of every row of scores [R, n] ("Flash-MaxSim"
+    Sec. 4 lists a top-K scan among the forward variants; TileMaxSim's
+    retrieval pipeline takes the top-k of the scores). Order: descending
+    value, the lower index first among equal values (-0.0 equals +0.0).
+    Returns (indices [R, k] int32, values [R, k] float64)."""
+    s = np.asarray(scores, dtype=np.float64)
+    R, n = s.shape
+    if not 0 < k <= n:
+        raise ValueError("need 0 < k <= n")
+    idx = np.empty((R, k), dtype=np.int32)
+    for r in range(R):
+        order = np.lexsort((np.arange(n), -s[r]))  # primary: -value, then index
+        idx[r] = order[:k]
+    return idx, np.take_along_axis(s, idx.astype(np.int64), axis=1)
+
+
+def two_stage_topk(Q8, q_scale, D8, d_scale, Q16, D16, dtype, k1, k, threads=0):
+    """Two-stage INT8 -> f16 / bf16 top-k ("Flash-MaxSim" Sec. 4: the
+    two-stage INT8 -> FP16 top-K scan among the forward variants):
+      1. INT8 x INT8 scores s8 of every (query, document) (fwd_int8);
+      2. the k1 best documents of each query by s8 (topk);
+      3. those documents rescored from the f16 / bf16 embeddings (fwd_dense);
+      4. the k best of the rescored candidates (topk).
+    Q8 / D8 int8 [Nq,Lq,dim] / [Nd,Ld,dim] with per-token scales; Q16 / D16 the
+    same shapes as uint16 bits of dtype. Returns (top_idx [Nq,k] int32 document
+    indices, top_scores [Nq,k], s8 [Nq,Nd], candidates [Nq,k1], s16 [Nq,k1])."""
+    Nq = Q8.shape[0]
+    s8, _, _, _ = fwd_int8(Q8, q_scale, D8, d_scale, threads=threads)
+    cand, _ = topk(s8, k1)
+    s16 = np.empty((Nq, k1), dtype=np.float64)
+    for i in range(Nq):
+        si, _, _ = fwd_dense(Q16[i:i + 1], D16, dtype, docs=cand[i].astype(np.int64), threads=threads)
+        s16[i] = si[0]
+    pos, top_scores = topk(s16, k)
+    top_idx = np.take_along_axis(cand, pos.astype(np.int64), axis=1)
+    return top_idx, top_scores, s8, cand, s16

@@ -436,3 +436,84 @@ def test_chamfer_gradient_sums():
     _, ip, _, _, iq, _, _ = oracle.chamfer_fwd(P, Q)
     dP, dQ = oracle.chamfer_bwd(P, Q, ip, iq, np.array([1.3, -0.4], np.float32))
     assert np.allclose(dP.sum(axis=1) + dQ.sum(axis=1), 0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- top-k and the two-stage scan
+
+def _f16_bits(x):
+    return datagen.float_to_bits(np.asarray(x, dtype=np.float64), "f16")
+
+
+def test_two_stage_hand_example(golden):
+    ex = golden["two_stage_topk"]
+    Q8 = np.array(ex["Q8"], np.int8)
+    D8 = np.array(ex["D8"], np.int8)
+    qs = np.array(ex["q_scale"], np.float32)
+    ds = np.array(ex["d_scale"], np.float32)
+    Q16, D16 = _f16_bits(ex["Q16"]), _f16_bits(ex["D16"])
+    top_idx, top_scores, s8, cand, s16 = oracle.two_stage_topk(Q8, qs, D8, ds, Q16, D16, "f16", ex["k1"], ex["k"])
+    assert s8.tolist() == ex["s8"] and cand.tolist() == ex["candidates"] and s16.tolist() == ex["s16"]
+    assert top_idx.tolist() == ex["top_idx"] and top_scores.tolist() == ex["top_scores"]
+
+
+def test_topk_brute_force_with_ties_and_signed_zeros():
+    rng = np.random.default_rng(71)
+    for trial in range(20):
+        n = int(rng.integers(1, 60))
+        v = rng.integers(-4, 5, size=(3, n)).astype(np.float64) * 0.5
+        v[:, ::7] = -0.0
+        v[:, 1::9] = 0.0
+        k = int(rng.integers(1, n + 1))
+        idx, vals = oracle.topk(v, k)
+        for r in range(3):
+            want = sorted(range(n), key=lambda j: (-v[r, j], j))[:k]
+            assert idx[r].tolist() == want
+            assert vals[r].tolist() == [v[r, j] for j in want]
+    # k = n: a permutation, descending
+    v = rng.standard_normal((2, 50))
+    idx, vals = oracle.topk(v, 50)
+    assert all(sorted(row) == list(range(50)) for row in idx.tolist()) and (np.diff(vals, axis=1) <= 0).all()
+
+
+def _two_stage_inputs(seed, Nq, Lq, Nd, Ld, dim, integer=False):
+    rng = np.random.default_rng(seed)
+    if integer:
+        q = rng.integers(-3, 4, size=(Nq, Lq, dim))
+        d = rng.integers(-3, 4, size=(Nd, Ld, dim))
+        Q8, D8 = q.astype(np.int8), d.astype(np.int8)
+        qs, ds = np.ones((Nq, Lq), np.float32), np.ones((Nd, Ld), np.float32)
+        return Q8, qs, D8, ds, _f16_bits(q), _f16_bits(d)
+    Q8, qs = datagen.int8_rows(seed, datagen.TID_Q, Nq * Lq, dim)
+    D8, ds = datagen.int8_rows(seed, datagen.TID_D, Nd * Ld, dim)
+    Q16 = datagen.gaussian_rows(seed, datagen.TID_Q, Nq * Lq, dim, "f16")
+    D16 = datagen.gaussian_rows(seed, datagen.TID_D, Nd * Ld, dim, "f16")
+    return (Q8.reshape(Nq, Lq, dim), qs.reshape(Nq, Lq), D8.reshape(Nd, Ld, dim), ds.reshape(Nd, Ld),
+            Q16.reshape(Nq, Lq, dim), D16.reshape(Nd, Ld, dim))
+
+
+def test_two_stage_with_every_candidate_is_the_exact_topk():
+    Q8, qs, D8, ds, Q16, D16 = _two_stage_inputs(73, 3, 5, 40, 7, 32)
+    top_idx, top_scores, s8, cand, s16 = oracle.two_stage_topk(Q8, qs, D8, ds, Q16, D16, "f16", 40, 6)
+    exact, _, _ = oracle.fwd_dense(Q16, D16, "f16")
+    want_idx, want_scores = oracle.topk(exact, 6)
+    assert np.array_equal(top_idx, want_idx) and np.array_equal(top_scores, want_scores)
+    # the candidates are every document, ordered by the INT8 scores
+    assert all(sorted(row) == list(range(40)) for row in cand.tolist())
+
+
+def test_two_stage_properties_and_integer_agreement():
+    # integer embeddings with unit scales: both stages compute the same exact scores
+    Q8, qs, D8, ds, Q16, D16 = _two_stage_inputs(79, 2, 4, 60, 5, 32, integer=True)
+    top_idx, top_scores, s8, cand, s16 = oracle.two_stage_topk(Q8, qs, D8, ds, Q16, D16, "f16", 20, 8)
+    assert np.array_equal(s16, np.take_along_axis(s8, cand.astype(np.int64), axis=1))
+    want_idx, want_scores = oracle.topk(s8, 8)
+    assert np.array_equal(top_idx, want_idx) and np.array_equal(top_scores, want_scores)
+    # Gaussian embeddings: the final documents are candidates, scores descending, and each
+    # final score is the f16 score of its document
+    Q8, qs, D8, ds, Q16, D16 = _two_stage_inputs(83, 2, 6, 50, 9, 32)
+    top_idx, top_scores, s8, cand, s16 = oracle.two_stage_topk(Q8, qs, D8, ds, Q16, D16, "f16", 12, 5)
+    exact, _, _ = oracle.fwd_dense(Q16, D16, "f16")
+    for i in range(2):
+        assert set(top_idx[i].tolist()) <= set(cand[i].tolist())
+        assert (np.diff(top_scores[i]) <= 0).all()
+        assert np.array_equal(top_scores[i], exact[i, top_idx[i]])
