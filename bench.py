@@ -17,6 +17,8 @@ Other workloads (measured the same way, for the design notes):
   colpali_cross    128 x 128 vs 128 x 1024 (bf16), masks, scores + argmax
   contrastive_bwd  the backward of 64 x 128 vs 64 x 1024 (bf16)
   int8_rerank      1 x 1024 vs 10,000 x 1024 (INT8, per-token scales)
+  two_stage_topk   32 x 32 vs 100,000 x 128: INT8 scores, top 1,000, f16
+                   rescoring, top 100 (docs/s)
 Inputs smaller than L2 are timed step by step with an L2 flush between steps.
 
 Prints one JSON line (rank 0). Under torchrun every rank scores its own
@@ -239,6 +241,17 @@ def describe(w, spec):
         cfg = {"workload": text, "B": w["B"], "N": w["N"], "M": w["M"], "dim": w["dim"],
                "l2": "inputs (2.4 MB) stay in L2 by design: the step is ALU-bound; no flush"}
         return cfg
+    if name == "two_stage_topk":
+        text = (f"two_stage_topk: Q [{w['Nq']},{w['Lq']},{w['dim']}] vs D [{w['Nd']},{w['Ld']},{w['dim']}], each as "
+                f"INT8 with per-token f32 scales and as f16 (the same l2-normalised Gaussian rows, seed "
+                f"{spec['seed']}); stage 1 INT8 scores of every pair, top k1={w['k1']} per query, f16 rescoring of "
+                f"the candidates, top k={w['k']}")
+        cfg = {"workload": text}
+        for key in ("Nq", "Lq", "Nd", "Ld", "dim", "k1", "k"):
+            cfg[key] = w[key]
+        cfg["l2"] = "inputs larger than L2 (the INT8 corpus alone is %.2f GB); no flush needed" % (
+            w["Nd"] * w["Ld"] * (w["dim"] + 4) / 1e9)
+        return cfg
     if name == "colbert_varlen":
         text = (f"colbert_varlen: Nq={w['Nq']} queries x Lq={w['Lq']} tokens vs Nd={w['Nd']} packed docs, "
                 f"Ld~U[{spec['ld_min']},{spec['ld_max']}] (sum Ld={w['total_d']}), d={w['dim']}, f16, "
@@ -301,6 +314,10 @@ def time_oracle(w, n_docs: int, threads: int = 0):
                           docs=docs, threads=threads)
     elif name == "int8_rerank":
         oracle.fwd_int8(w["Q"], w["q_scale"], w["D"], w["d_scale"], docs=docs, threads=threads)
+    elif name == "two_stage_topk":
+        k1 = min(w["k1"], n_docs)
+        oracle.two_stage_topk(w["Q8"], w["q_scale"], w["D8"][:n_docs], w["d_scale"][:n_docs], w["Q16"],
+                              w["D16"][:n_docs], "f16", k1, min(w["k"], k1), threads=threads)
     elif name == "contrastive_bwd":
         raise SystemExit("the oracle arm times forward workloads")
     else:
@@ -586,6 +603,64 @@ class ChamferCase:
         return sum(a.elapsed_time(b) for a, b in ev) / max(1, len(ev))
 
 
+class TwoStageCase:
+    """Two-stage INT8 -> f16 top-k over the whole corpus: INT8 scores of every
+    (query, document), the k1 best per query, their f16 rescoring, the k best.
+    The INT8 forward dominates the step."""
+
+    def __init__(self, w, device):
+        import torch as t
+
+        from maxsim_scoring_gb300 import _native, ops
+        self.w, self.device, self.ops, self.t = w, device, ops, t
+        self.name = w["name"]
+        Nq, Lq, Nd, Ld, dim, k1, k = (w[x] for x in ("Nq", "Lq", "Nd", "Ld", "dim", "k1", "k"))
+
+        def pinned(x):
+            return t.from_numpy(np.ascontiguousarray(x)).pin_memory()
+
+        self.h_in = {key: pinned(w[key]) for key in ("Q8", "q_scale", "D8", "d_scale")}
+        for key in ("Q16", "D16"):
+            self.h_in[key] = t.from_numpy(np.ascontiguousarray(w[key]).view(np.int16)).view(t.float16).pin_memory()
+        self.d_in = {key: v.to(device) for key, v in self.h_in.items()}
+        self.e2e_in = {key: t.empty_like(v) for key, v in self.d_in.items()}
+        self.ws = t.empty(ops.workspace_size(_native.OP_TWO_STAGE, Nq, Lq, Nd, Ld, dim), dtype=t.uint8, device=device)
+        self.h_out = {"idx": t.empty((Nq, k), dtype=t.int32).pin_memory(),
+                      "scores": t.empty((Nq, k), dtype=t.float32).pin_memory()}
+        self.out = None
+        self.units = Nd
+        # stage 1 over the corpus plus stage 2 over Nq * k1 candidates
+        self.flops = maxsim_flops(Nq * Lq, dim, Nd * Ld) + maxsim_flops(Lq, dim, Nq * k1 * Ld)
+        self.bytes = Nd * Ld * (dim + 4) + Nq * k1 * Ld * dim * 2 + Nq * Nd * 4
+        self.bound, self.dtype = "tensor", "int8 then f16 (f16 MMA, fp32 acc)"
+        # int8: repack + forward; topk; pairs + offsets; pairs: check_cu, count, scan, place, repack, forward; topk
+        self.launches = 2 + 1 + 2 + 6 + 1
+
+    def call(self, d):
+        w = self.w
+        self.out = self.ops.maxsim_two_stage_topk(d["Q8"], d["q_scale"], d["D8"], d["d_scale"], d["Q16"], d["D16"],
+                                                  w["k1"], w["k"], workspace=self.ws)
+
+    def step(self):
+        self.call(self.d_in)
+
+    def e2e_step(self):
+        for key, v in self.h_in.items():
+            self.e2e_in[key].copy_(v, non_blocking=True)
+        self.call(self.e2e_in)
+        self.h_out["idx"].copy_(self.out[0], non_blocking=True)
+        self.h_out["scores"].copy_(self.out[1], non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.h_in.values())
+
+    def d2h_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.h_out.values())
+
+    def flush(self):
+        pass  # the corpus (1.7 GB INT8 + 3.3 GB f16) is far larger than L2
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -596,7 +671,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     _native.lib()  # fail loudly without the extension
     w, spec = make_workload(args.workload, rank, world, args.shard, args.nd)
-    case = ChamferCase(w, device) if args.workload.startswith("chamfer") else Case(w, device)
+    case = (ChamferCase(w, device) if args.workload.startswith("chamfer") else
+            TwoStageCase(w, device) if args.workload == "two_stage_topk" else Case(w, device))
     metric, unit_name = metric_of(args.workload)
     stream = torch.cuda.current_stream(device)
 

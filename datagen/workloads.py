@@ -20,6 +20,9 @@ generators in this package.
                   (a reranker's candidate lists), seed 2
 Every row is an l2-normalised Gaussian vector rounded once to its storage type.
 
+ two_stage_topk   Q [32,32,128] and D [100000,128,128] as INT8 (per-token
+                  scales) and as f16: the same l2-normalised Gaussian rows
+                  quantised two ways; k1 = 1,000 candidates, k = 100, seed 7
  chamfer_100k     one pair of 3-D point clouds of 100,000 points each
                   (standard normal coordinates, float32) and an upstream
                   gradient N(0,1) per pair, seed 6: the Chamfer-distance
@@ -42,6 +45,7 @@ SPECS = {
     "colbert_pairs": dict(Nq=32, Lq=32, Nd=100_000, ld_min=32, ld_max=300, dim=128, dtype="f16", seed=2,
                           pairs_per_query=10_000),
     "chamfer_100k": dict(B=1, N=100_000, M=100_000, dim=3, seed=6),
+    "two_stage_topk": dict(Nq=32, Lq=32, Nd=100_000, Ld=128, dim=128, k1=1000, k=100, seed=7),
 }
 
 
@@ -93,6 +97,17 @@ def int8(Nq, Lq, Nd, Ld, dim, seed):
     return w
 
 
+def two_stage(Nq, Lq, Nd, Ld, dim, k1, k, seed):
+    """INT8 (with per-token scales) and f16 versions of the same dense Q / D:
+    every row is drawn once and quantised both ways."""
+    w = int8(Nq, Lq, Nd, Ld, dim, seed)
+    w["Q8"], w["D8"] = w.pop("Q"), w.pop("D")
+    w["Q16"] = gaussian_rows(seed, TID_Q, Nq * Lq, dim, "f16").reshape(Nq, Lq, dim)
+    w["D16"] = gaussian_rows(seed, TID_D, Nd * Ld, dim, "f16").reshape(Nd, Ld, dim)
+    w.update(k1=k1, k=k, dtype="f16")
+    return w
+
+
 def clouds(B, N, M, dim, seed):
     """Point clouds P [B,N,dim], Q [B,M,dim] (float32, standard normal
     coordinates) and an upstream gradient grad [B] (float32, N(0,1))."""
@@ -115,5 +130,7 @@ def make(name: str, **overrides):
         return int8(**spec)
     if name == "chamfer_100k":
         return clouds(**spec)
+    if name == "two_stage_topk":
+        return two_stage(**spec)
     grad = name == "contrastive_bwd"
     return dense(**spec, grad=grad)

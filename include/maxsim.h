@@ -58,7 +58,8 @@ typedef enum { MAXSIM_F16 = 0, MAXSIM_BF16 = 1 } maxsim_dtype;
 
 /* Operation codes for maxsim_workspace_size(). */
 enum { MAXSIM_OP_FWD = 0, MAXSIM_OP_FWD_VARLEN = 1, MAXSIM_OP_BWD = 2, MAXSIM_OP_FWD_INT8 = 3,
-       MAXSIM_OP_SCORE_PAIRS = 4, MAXSIM_OP_CHAMFER_FWD = 5, MAXSIM_OP_CHAMFER_BWD = 6 };
+       MAXSIM_OP_SCORE_PAIRS = 4, MAXSIM_OP_CHAMFER_FWD = 5, MAXSIM_OP_CHAMFER_BWD = 6,
+       MAXSIM_OP_TWO_STAGE = 7 };
 
 /*
  * Dense forward.
@@ -228,6 +229,43 @@ maxsim_status maxsim_chamfer_bwd(const float *P, const float *Q, int64_t B, int6
                                  float *dQ, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Top-k of every row of a score matrix (the retrieval step after scoring:
+ * TileMaxSim paper, "End-to-End Retrieval Latency"; the top-K scan among the
+ * forward variants of "Flash-MaxSim" Sec. 4).
+ *   scores      [rows, n] f32 (device)
+ *   top_idx     [rows, k] i32 (out): column indices of the k largest values,
+ *               by descending value, the lower index first among equal values
+ *               (-0.0 equals +0.0; NaN ranks below every number)
+ *   top_scores  [rows, k] f32 (out, optional): those values
+ * 1 <= k <= min(n, 4096). One block per row: a radix select of the k-th value
+ * (four 8-bit passes), an index-ordered compaction, a bitonic sort.
+ */
+maxsim_status maxsim_topk(const float *scores, int64_t rows, int64_t n, int64_t k, int32_t *top_idx,
+                          float *top_scores, void *stream);
+
+/*
+ * Two-stage INT8 -> f16 / bf16 top-k ("Flash-MaxSim" Sec. 4: the two-stage
+ * INT8 -> FP16 top-K scan among the forward variants):
+ *   1. s8 = maxsim_fwd_int8 scores of every (query, document) pair;
+ *   2. the k1 best documents of each query by s8 (maxsim_topk order);
+ *   3. those Nq * k1 pairs rescored from the f16 / bf16 embeddings
+ *      (maxsim_score_pairs_packed on the dense corpus);
+ *   4. the k best of each query's rescored candidates.
+ *   Q8 [Nq, Lq, dim] i8 + q_scale [Nq, Lq] f32;  D8 [Nd, Ld, dim] i8 + d_scale [Nd, Ld] f32
+ *   Q16 [Nq, Lq, dim], D16 [Nd, Ld, dim] in `dtype`: the same embeddings at 16 bits
+ *   top_idx [Nq, k] i32 (out): document indices;  top_scores [Nq, k] f32 (out, optional)
+ *   stage1_scores [Nq, Nd] f32 (out, optional): s8;  candidates [Nq, k1] i32 (out, optional)
+ * dim a multiple of 32 up to 128 and Lq <= 512 (the rescoring stage holds one
+ * query per unit); 1 <= k <= k1 <= min(Nd, 4096). No masks. Workspace:
+ * maxsim_workspace_size(MAXSIM_OP_TWO_STAGE, Nq, Lq, Nd, Ld, dim), 256-byte aligned.
+ */
+maxsim_status maxsim_two_stage_topk(const int8_t *Q8, const float *q_scale, const int8_t *D8, const float *d_scale,
+                                    const void *Q16, const void *D16, maxsim_dtype dtype, int64_t Nq, int64_t Lq,
+                                    int64_t Nd, int64_t Ld, int64_t dim, int64_t k1, int64_t k, int32_t *top_idx,
+                                    float *top_scores, float *stage1_scores, int32_t *candidates, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace an operation needs for a shape (0 if none).
  *   MAXSIM_OP_FWD / MAXSIM_OP_FWD_INT8: (Nq, Lq, Nd, Ld, dim)
  *   MAXSIM_OP_FWD_VARLEN:              (Nq, max_lq, Nd, total_d, dim); assumes
@@ -236,6 +274,8 @@ maxsim_status maxsim_chamfer_bwd(const float *P, const float *Q, int64_t B, int6
  *                                      outputs are NULL (an upper bound)
  *   MAXSIM_OP_SCORE_PAIRS:             (Nq, max_lq, Nd, num_pairs, dim)
  *   MAXSIM_OP_CHAMFER_FWD / _BWD:      (B, N, M, 0, dim)
+ *   MAXSIM_OP_TWO_STAGE:               (Nq, Lq, Nd, Ld, dim); enough for any
+ *                                      k1 <= min(Nd, 4096)
  * Returns (size_t)-1 for an invalid shape.
  */
 size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim);

@@ -26,7 +26,7 @@ STATUS = {
 }
 
 OP_FWD, OP_FWD_VARLEN, OP_BWD, OP_FWD_INT8, OP_SCORE_PAIRS = 0, 1, 2, 3, 4
-OP_CHAMFER_FWD, OP_CHAMFER_BWD = 5, 6
+OP_CHAMFER_FWD, OP_CHAMFER_BWD, OP_TWO_STAGE = 5, 6, 7
 F16, BF16 = 0, 1
 
 # Every symbol the header declares, with its ctypes signature.
@@ -45,6 +45,9 @@ SIGNATURES = {
                                        _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_chamfer_fwd": (_I, [_VP, _VP, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_chamfer_bwd": (_I, [_VP, _VP, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "maxsim_topk": (_I, [_VP, _I64, _I64, _I64, _VP, _VP, _VP]),
+    "maxsim_two_stage_topk": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _VP,
+                                   _VP, _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_workspace_size": (_SZ, [_I, _I64, _I64, _I64, _I64, _I64]),
     "maxsim_status_string": (ctypes.c_char_p, [_I]),
     "maxsim_device_status": (_I, [_VP]),

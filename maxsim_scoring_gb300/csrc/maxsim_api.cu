@@ -13,6 +13,7 @@
 #include "maxsim.h"
 #include "bwd_kernels.cuh"
 #include "chamfer_kernels.cuh"
+#include "topk_kernels.cuh"
 #include "fwd_kernel.cuh"
 
 namespace maxsim {
@@ -676,6 +677,63 @@ maxsim_status launch_chamfer_nn(DeviceInfo* dev, int slot, const ChamferFwdArgs&
     return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
 }
 
+inline int32_t pow2_at_least(int64_t k) {
+    int32_t p = 1;
+    while (p < k) p <<= 1;
+    return p;
+}
+
+maxsim_status launch_topk(DeviceInfo* dev, const float* scores, int64_t rows, int64_t n, int64_t row_stride,
+                          int64_t k, const int32_t* id_map, int64_t map_stride, int32_t* out_idx, float* out_val,
+                          int64_t out_stride, cudaStream_t st) {
+    (void)dev;
+    if (rows == 0 || k == 0) return MAXSIM_OK;
+    if (rows > 2147483647) return MAXSIM_ERR_UNSUPPORTED;
+    TopkArgs t{};
+    t.scores = scores;
+    t.n = n;
+    t.row_stride = row_stride;
+    t.k = static_cast<int32_t>(k);
+    t.pow2 = pow2_at_least(k);
+    t.id_map = id_map;
+    t.map_stride = map_stride;
+    t.out_idx = out_idx;
+    t.out_val = out_val;
+    t.out_stride = out_stride;
+    const size_t smem = static_cast<size_t>(t.pow2) * 8;  // keys and positions
+    topk_kernel<<<static_cast<unsigned>(rows), kTopkThreads, smem, st>>>(t);
+    return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
+struct TwoStagePlan {
+    size_t off_s8 = 0, off_cand = 0, off_pairs = 0, off_cu = 0, off_s16 = 0, off_stage = 0, bytes = 0;
+    size_t stage_bytes = 0;
+    bool ok = false;
+};
+
+TwoStagePlan plan_two_stage(int64_t Nq, int64_t Lq, int64_t Nd, int64_t dim, int64_t k1) {
+    TwoStagePlan p;
+    const FwdPlan p8 = plan_fwd(Nq, Lq, Nd, dim, false, true);
+    const FwdPlan p16 = plan_fwd(Nq, Lq, Nd, dim, true, false);
+    if (!p8.ok || !p16.ok || p16.n_chunks > 1) return p;
+    p.stage_bytes = std::max(p8.ws_bytes, pairs_ws(p16.ws_bytes, Nq, Nq * k1).bytes);
+    size_t off = 0;
+    p.off_s8 = off;
+    off = round_up(off + static_cast<size_t>(Nq * Nd) * 4, 256);
+    p.off_cand = off;
+    off = round_up(off + static_cast<size_t>(Nq * k1) * 4, 256);
+    p.off_pairs = off;
+    off = round_up(off + static_cast<size_t>(Nq * k1) * 8, 256);
+    p.off_cu = off;
+    off = round_up(off + static_cast<size_t>(Nd + 1) * 4, 256);
+    p.off_s16 = off;
+    off = round_up(off + static_cast<size_t>(Nq * k1) * 4, 256);
+    p.off_stage = off;
+    p.bytes = round_up(off + p.stage_bytes, 256);
+    p.ok = true;
+    return p;
+}
+
 }  // namespace
 }  // namespace maxsim
 
@@ -729,6 +787,10 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
         off = round_up(off + static_cast<size_t>(Nd * Ld + 1) * 4, 256); // row_ptr
         off = round_up(off + static_cast<size_t>(Nq * Nd * Lq) * 4, 256);  // col
         return off;
+    }
+    case MAXSIM_OP_TWO_STAGE: {  // (Nq, Lq, Nd, Ld, dim), for any k1 <= min(Nd, 4096)
+        const TwoStagePlan p = plan_two_stage(Nq, Lq, Nd, dim, std::min<int64_t>(Nd, kTopkMaxK));
+        return p.ok ? p.bytes : static_cast<size_t>(-1);
     }
     case MAXSIM_OP_CHAMFER_FWD:  // (B, N, M, unused, dim)
         if (check_chamfer_shape(Nq, Lq, Nd, dim) == MAXSIM_ERR_INVALID_ARG) return static_cast<size_t>(-1);
@@ -1181,6 +1243,70 @@ maxsim_status maxsim_chamfer_bwd(const float* P, const float* Q, int64_t B, int6
     if (dim <= 3) chamfer_grad_kernel<3><<<grid, 256, 0, st>>>(g);
     else chamfer_grad_kernel<kChMaxDim><<<grid, 256, 0, st>>>(g);
     return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
+maxsim_status maxsim_topk(const float* scores, int64_t rows, int64_t n, int64_t k, int32_t* top_idx,
+                          float* top_scores, void* stream) {
+    if (rows < 0 || n < 0 || k < 0) return MAXSIM_ERR_INVALID_ARG;
+    if (rows == 0 || k == 0) return MAXSIM_OK;
+    if (k > n) return MAXSIM_ERR_INVALID_ARG;
+    if (k > kTopkMaxK || n > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
+    if (!scores || !aligned(scores, 4) || !top_idx || !aligned(top_idx, 4) || (top_scores && !aligned(top_scores, 4)))
+        return MAXSIM_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    maxsim_status rc = device_info(&dev);
+    if (rc != MAXSIM_OK) return rc;
+    return launch_topk(dev, scores, rows, n, n, k, nullptr, 0, top_idx, top_scores, k, static_cast<cudaStream_t>(stream));
+}
+
+maxsim_status maxsim_two_stage_topk(const int8_t* Q8, const float* q_scale, const int8_t* D8, const float* d_scale,
+                                    const void* Q16, const void* D16, maxsim_dtype dtype, int64_t Nq, int64_t Lq,
+                                    int64_t Nd, int64_t Ld, int64_t dim, int64_t k1, int64_t k, int32_t* top_idx,
+                                    float* top_scores, float* stage1_scores, int32_t* candidates, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    if (dtype != MAXSIM_F16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_INVALID_ARG;
+    if (Nq < 0 || Lq < 0 || Nd < 0 || Ld < 0 || k1 < 0 || k < 0) return MAXSIM_ERR_INVALID_ARG;
+    maxsim_status rc = check_dim(dim, 32);
+    if (rc != MAXSIM_OK) return rc;
+    if (Nq == 0 || k == 0) return MAXSIM_OK;
+    if (k1 > Nd || k > k1) return MAXSIM_ERR_INVALID_ARG;
+    if (k1 > kTopkMaxK) return MAXSIM_ERR_UNSUPPORTED;
+    if (!top_idx || !aligned(top_idx, 4) || (top_scores && !aligned(top_scores, 4)) ||
+        (stage1_scores && !aligned(stage1_scores, 4)) || (candidates && !aligned(candidates, 4)))
+        return MAXSIM_ERR_INVALID_ARG;
+    if (Lq > 0 && (!Q8 || !aligned16(Q8) || !q_scale || !aligned(q_scale, 4) || !Q16 || !aligned16(Q16)))
+        return MAXSIM_ERR_INVALID_ARG;
+    if (Ld > 0 && (!D8 || !aligned16(D8) || !d_scale || !aligned(d_scale, 4) || !D16 || !aligned16(D16)))
+        return MAXSIM_ERR_INVALID_ARG;
+    if (Nd * Ld > kI32Max || Nq * pad_lq(Lq) > kI32Max || Nq * Nd > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
+    const TwoStagePlan p = plan_two_stage(Nq, Lq, Nd, dim, k1);
+    if (!p.ok) return MAXSIM_ERR_UNSUPPORTED;  // the rescoring stage takes queries of up to 512 rows
+    if (workspace_bytes < p.bytes || !workspace || !aligned(workspace, 256)) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* s8 = stage1_scores ? stage1_scores : reinterpret_cast<float*>(ws + p.off_s8);
+    int32_t* cand = candidates ? candidates : reinterpret_cast<int32_t*>(ws + p.off_cand);
+    int32_t* pairs = reinterpret_cast<int32_t*>(ws + p.off_pairs);
+    int32_t* cu = reinterpret_cast<int32_t*>(ws + p.off_cu);
+    float* s16 = reinterpret_cast<float*>(ws + p.off_s16);
+    void* stage = ws + p.off_stage;
+    // 1. INT8 scores of every (query, document)
+    rc = maxsim_fwd_int8(Q8, q_scale, D8, d_scale, Nq, Lq, Nd, Ld, dim, nullptr, nullptr, s8, nullptr, nullptr, stage,
+                         p.stage_bytes, stream);
+    if (rc != MAXSIM_OK) return rc;
+    // 2. the k1 best documents of each query
+    if ((rc = launch_topk(dev, s8, Nq, Nd, Nd, k1, nullptr, 0, cand, nullptr, k1, st)) != MAXSIM_OK) return rc;
+    // 3. rescore the candidates from the f16 / bf16 embeddings (dense documents as packed rows)
+    two_stage_pairs_kernel<<<grid_for(Nq * k1, 256, dev->num_sms), 256, 0, st>>>(cand, Nq, k1, pairs);
+    uniform_offsets_kernel<<<grid_for(Nd + 1, 256, dev->num_sms), 256, 0, st>>>(Nd, Ld, cu);
+    if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+    rc = maxsim_score_pairs_packed(Q16, nullptr, Lq, D16, cu, Nd * Ld, dtype, Nq, Nd, dim, nullptr, nullptr, pairs,
+                                   Nq * k1, s16, nullptr, stage, p.stage_bytes, stream);
+    if (rc != MAXSIM_OK) return rc;
+    // 4. the k best rescored candidates, as document indices
+    return launch_topk(dev, s16, Nq, k1, k1, k, cand, k1, top_idx, top_scores, k, st);
 }
 
 }  // extern "C"

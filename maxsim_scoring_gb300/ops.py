@@ -272,6 +272,49 @@ def chamfer_bwd(P: torch.Tensor, Q: torch.Tensor, idx_p: torch.Tensor, idx_q: to
     return dP, dQ
 
 
+def maxsim_topk(scores: torch.Tensor, k: int):
+    """(values [R, k] f32, indices [R, k] i32): the k largest entries of every
+    row of scores [R, n] (f32), descending, the lower index first among ties."""
+    s = _contig(scores, "scores", torch.float32)
+    if s.dim() != 2:
+        raise ValueError("scores must be [rows, n]")
+    R, n = s.shape
+    idx = torch.empty((R, k), dtype=torch.int32, device=s.device)
+    vals = torch.empty((R, k), dtype=torch.float32, device=s.device)
+    rc = _native.lib().maxsim_topk(_ptr(s), R, n, k, _ptr(idx), _ptr(vals), _stream(s.device))
+    _native.check(rc, "maxsim_topk")
+    return vals, idx
+
+
+def maxsim_two_stage_topk(Q8: torch.Tensor, q_scale: torch.Tensor, D8: torch.Tensor, d_scale: torch.Tensor,
+                          Q16: torch.Tensor, D16: torch.Tensor, k1: int, k: int, *, want_stage1: bool = False,
+                          workspace: Optional[torch.Tensor] = None):
+    """Two-stage INT8 -> f16 / bf16 top-k: (top_idx [Nq,k] i32, top_scores [Nq,k] f32,
+    stage1_scores [Nq,Nd] or None, candidates [Nq,k1] or None)."""
+    dev = Q8.device
+    Q8 = _contig(Q8, "Q8", torch.int8)
+    D8 = _contig(D8, "D8", torch.int8, dev)
+    qs = _contig(q_scale, "q_scale", torch.float32, dev)
+    ds = _contig(d_scale, "d_scale", torch.float32, dev)
+    if Q16.dtype not in _DT or D16.dtype != Q16.dtype:
+        raise TypeError("Q16 and D16 must both be float16 or both bfloat16")
+    Q16, D16 = _contig(Q16, "Q16", device=dev), _contig(D16, "D16", device=dev)
+    Nq, Lq, dim = Q8.shape
+    Nd, Ld, _ = D8.shape
+    if tuple(Q16.shape) != (Nq, Lq, dim) or tuple(D16.shape) != (Nd, Ld, dim):
+        raise ValueError("Q16 / D16 must have the shapes of Q8 / D8")
+    top_idx = torch.empty((Nq, k), dtype=torch.int32, device=dev)
+    top_scores = torch.empty((Nq, k), dtype=torch.float32, device=dev)
+    s8 = torch.empty((Nq, Nd), dtype=torch.float32, device=dev) if want_stage1 else None
+    cand = torch.empty((Nq, k1), dtype=torch.int32, device=dev) if want_stage1 else None
+    ws, nbytes = _workspace(workspace_size(_native.OP_TWO_STAGE, Nq, Lq, Nd, Ld, dim), dev, workspace)
+    rc = _native.lib().maxsim_two_stage_topk(_ptr(Q8), _ptr(qs), _ptr(D8), _ptr(ds), _ptr(Q16), _ptr(D16),
+                                             _DT[Q16.dtype], Nq, Lq, Nd, Ld, dim, k1, k, _ptr(top_idx),
+                                             _ptr(top_scores), _ptr(s8), _ptr(cand), _ptr(ws), nbytes, _stream(dev))
+    _native.check(rc, "maxsim_two_stage_topk")
+    return top_idx, top_scores, s8, cand
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device status word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)

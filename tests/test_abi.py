@@ -129,3 +129,33 @@ def test_chamfer_workspace_sizes(lib):
     assert ws(6, B, N, M, 0, 3) >= 16 * B * (N + M) + 4 * (B * (N + M) + 1)
     assert ws(6, 0, 0, 0, 0, 3) == 0
     assert ws(5, 1, 1, 1, 0, 0) == ctypes.c_size_t(-1).value
+
+
+def test_topk_and_two_stage_host_validation(lib):
+    t = lib.maxsim_topk
+    # scores, rows, n, k, idx, vals, stream
+    assert t(FAKE, 0, 10, 3, None, None, None) == 0       # nothing to do
+    assert t(FAKE, 2, 10, 11, FAKE, None, None) == 1      # k > n
+    assert t(FAKE, 2, 10000, 5000, FAKE, None, None) == 2  # k above 4096
+    assert t(None, 2, 10, 3, FAKE, None, None) == 1
+    assert t(FAKE + 2, 2, 10, 3, FAKE, None, None) == 1   # misaligned
+    ts = lib.maxsim_two_stage_topk
+    need = lib.maxsim_workspace_size(7, 4, 32, 1000, 64, 128)
+    assert need != ctypes.c_size_t(-1).value and need >= 4 * 1000 * 4
+    # Q8, qs, D8, ds, Q16, D16, dtype, Nq, Lq, Nd, Ld, dim, k1, k, idx, scores, s8, cand, ws, bytes, stream
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 32, 1000, 64, 128, 100, 10, FAKE, None, None, None, FAKE, need,
+            None]
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return ts(*a)
+    assert call(a13=0) == 0              # k = 0: nothing to do
+    assert call(a12=1001) == 1           # k1 > Nd
+    assert call(a13=101) == 1            # k > k1
+    assert call(a11=48) == 2             # dim not a multiple of 32
+    assert call(a8=600) == 2             # the rescoring stage takes up to 512 query rows
+    assert call(a6=5) == 1               # dtype
+    assert call(a14=None) == 1           # no output
+    assert call(a19=1024) == 5            # far too small
+    assert call(a18=FAKE + 16) == 5      # workspace alignment
