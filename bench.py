@@ -19,6 +19,8 @@ Other workloads (measured the same way, for the design notes):
   int8_rerank      1 x 1024 vs 10,000 x 1024 (INT8, per-token scales)
   two_stage_topk   32 x 32 vs 100,000 x 128: INT8 scores, top 1,000, f16
                    rescoring, top 100 (docs/s)
+  colpali_out_of_core  1 x 32 vs 100,000 x 1024 (bf16, 26 GB) streamed from
+                   page-locked host memory in 20,000-document blocks
 Inputs smaller than L2 are timed step by step with an L2 flush between steps.
 
 Prints one JSON line (rank 0). Under torchrun every rank scores its own
@@ -241,6 +243,16 @@ def describe(w, spec):
         cfg = {"workload": text, "B": w["B"], "N": w["N"], "M": w["M"], "dim": w["dim"],
                "l2": "inputs (2.4 MB) stay in L2 by design: the step is ALU-bound; no flush"}
         return cfg
+    if name == "colpali_out_of_core":
+        text = (f"colpali_out_of_core: Q [{w['Nq']},{w['Lq']},{w['dim']}] {w['dtype']} on the device vs a corpus D "
+                f"[{w['Nd']},{w['Ld']},{w['dim']}] {w['dtype']} ({w['Nd'] * w['Ld'] * w['dim'] * 2 / 1e9:.1f} GB) in "
+                f"page-locked host memory, streamed in blocks of {w['block_docs']} documents; l2-normalised Gaussian "
+                f"rows, seed {spec['seed']}")
+        cfg = {"workload": text}
+        for key in ("Nq", "Lq", "Nd", "Ld", "dim", "block_docs"):
+            cfg[key] = w[key]
+        cfg["l2"] = "the corpus comes from host memory every step; no flush needed"
+        return cfg
     if name == "two_stage_topk":
         text = (f"two_stage_topk: Q [{w['Nq']},{w['Lq']},{w['dim']}] vs D [{w['Nd']},{w['Ld']},{w['dim']}], each as "
                 f"INT8 with per-token f32 scales and as f16 (the same l2-normalised Gaussian rows, seed "
@@ -314,6 +326,11 @@ def time_oracle(w, n_docs: int, threads: int = 0):
                           docs=docs, threads=threads)
     elif name == "int8_rerank":
         oracle.fwd_int8(w["Q"], w["q_scale"], w["D"], w["d_scale"], docs=docs, threads=threads)
+    elif name == "colpali_out_of_core":
+        from datagen import workloads
+        D = workloads.fill_corpus(dict(w, Nd=n_docs), np.empty((n_docs * w["Ld"], w["dim"]), np.uint16))
+        t0 = time.perf_counter()  # the corpus sample is generated outside the timing
+        oracle.fwd_dense(w["Q"], D.reshape(n_docs, w["Ld"], w["dim"]), w["dtype"], threads=threads)
     elif name == "two_stage_topk":
         k1 = min(w["k1"], n_docs)
         oracle.two_stage_topk(w["Q8"], w["q_scale"], w["D8"][:n_docs], w["d_scale"][:n_docs], w["Q16"],
@@ -661,6 +678,78 @@ class TwoStageCase:
         pass  # the corpus (1.7 GB INT8 + 3.3 GB f16) is far larger than L2
 
 
+class OutOfCoreCase:
+    """One query against a corpus in page-locked host memory, scored block by
+    block (maxsim_fwd_streamed). The host-to-device link bounds it: its peak
+    is a plain pinned copy measured here."""
+
+    def __init__(self, w, device):
+        import torch as t
+
+        from datagen import workloads
+        from maxsim_scoring_gb300 import _native, ops
+        self.w, self.device, self.ops, self.t = w, device, ops, t
+        self.name = w["name"]
+        Nq, Lq, Nd, Ld, dim, blk = (w[x] for x in ("Nq", "Lq", "Nd", "Ld", "dim", "block_docs"))
+        dt = t.bfloat16 if w["dtype"] == "bf16" else t.float16
+        self.h_q = t.from_numpy(np.ascontiguousarray(w["Q"]).view(np.int16)).view(dt).pin_memory()
+        self.d_q = self.h_q.to(device)
+        self.e2e_q = t.empty_like(self.d_q)
+        corpus = t.empty((Nd * Ld, dim), dtype=t.int16).pin_memory()
+        workloads.fill_corpus(w, corpus.numpy().view(np.uint16))
+        self.D_host = corpus.view(dt).view(Nd, Ld, dim)
+        self.scores = t.empty((Nq, Nd), dtype=t.float32, device=device)
+        self.h_scores = t.empty((Nq, Nd), dtype=t.float32).pin_memory()
+        self.ws = t.empty(ops.workspace_size(_native.OP_FWD_STREAMED, Nq, Lq, min(blk, Nd), Ld, dim), dtype=t.uint8,
+                          device=device)
+        self.units = Nd
+        self.corpus_bytes = Nd * Ld * dim * 2
+        self.bytes = self.corpus_bytes + Nq * Lq * dim * 2 + Nq * Nd * 4
+        self.flops = maxsim_flops(Nq * Lq, dim, Nd * Ld)
+        self.bound, self.dtype = "h2d", w["dtype"]
+        n_blocks = -(-Nd // blk)
+        self.launches = n_blocks * (1 + (0 if Lq % 32 == 0 else 1))  # forward (+ query repack) per block
+        self.peak_gbs = self._copy_peak()
+
+    def _copy_peak(self):
+        """GB/s of one plain cudaMemcpyAsync of 4 GiB of the pinned corpus."""
+        t = self.t
+        n = min(self.corpus_bytes, 4 << 30) // 2
+        src = self.D_host.view(-1)[:n]
+        dst = t.empty(n, dtype=src.dtype, device=self.device)
+        best = 0.0
+        for _ in range(3):
+            e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+            e0.record()
+            dst.copy_(src, non_blocking=True)
+            e1.record()
+            t.cuda.synchronize(self.device)
+            best = max(best, 2 * n / (e0.elapsed_time(e1) / 1e3) / 1e9)
+        del dst
+        return best
+
+    def call(self, q):
+        self.ops.maxsim_fwd_streamed(q, self.D_host, block_docs=self.w["block_docs"], scores=self.scores,
+                                     workspace=self.ws)
+
+    def step(self):
+        self.call(self.d_q)
+
+    def e2e_step(self):
+        self.e2e_q.copy_(self.h_q, non_blocking=True)
+        self.call(self.e2e_q)
+        self.h_scores.copy_(self.scores, non_blocking=True)
+
+    def h2d_bytes(self):
+        return self.corpus_bytes + self.h_q.numel() * 2
+
+    def d2h_bytes(self):
+        return self.h_scores.numel() * 4
+
+    def flush(self):
+        pass  # the corpus arrives from host memory every step
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -672,7 +761,8 @@ def run_ours(args, rank, world, local_rank):
     _native.lib()  # fail loudly without the extension
     w, spec = make_workload(args.workload, rank, world, args.shard, args.nd)
     case = (ChamferCase(w, device) if args.workload.startswith("chamfer") else
-            TwoStageCase(w, device) if args.workload == "two_stage_topk" else Case(w, device))
+            TwoStageCase(w, device) if args.workload == "two_stage_topk" else
+            OutOfCoreCase(w, device) if args.workload == "colpali_out_of_core" else Case(w, device))
     metric, unit_name = metric_of(args.workload)
     stream = torch.cuda.current_stream(device)
 
@@ -736,7 +826,11 @@ def run_ours(args, rank, world, local_rank):
     ms = total_ms / args.steps
     value = all_units / (ms / 1e3)
     peaks, peak_src = load_peaks()
-    if case.bound == "alu":
+    if case.bound == "h2d":
+        achieved = case.corpus_bytes / (ms / 1e3) / 1e9
+        peak, unit = round(case.peak_gbs, 1), "GB/s"
+        src = "host-to-device link: a plain 4 GiB pinned cudaMemcpyAsync measured in this run"
+    elif case.bound == "alu":
         # fp32 FMA peak: lanes x SMs x 2 FLOP x the maximum SM clock
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         max_mhz = clk.get("sm_max_mhz") or 2070.0
@@ -759,7 +853,9 @@ def run_ours(args, rank, world, local_rank):
     roofline = {
         "bound": case.bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": src,
-        "kernel": ("chamfer_nn_kernel (duration = the whole maxsim_chamfer_fwd call, CUDA events per step: "
+        "kernel": ("the streamed corpus copy (cudaMemcpyAsync, overlapped with maxsim_fwd_kernel on each block; "
+                   "duration = the whole maxsim_fwd_streamed call)" if case.bound == "h2d" else
+                   "chamfer_nn_kernel (duration = the whole maxsim_chamfer_fwd call, CUDA events per step: "
                    f"{kernel_ms:.4f} ms; it also runs the merge and loss kernels)" if case.bound == "alu" else
                    "maxsim_fwd_kernel (duration = whole entry-point call, which also runs small helper kernels)"
                    if case.name != "contrastive_bwd" else "backward kernels (whole maxsim_bwd call)"),

@@ -23,6 +23,9 @@ Every row is an l2-normalised Gaussian vector rounded once to its storage type.
  two_stage_topk   Q [32,32,128] and D [100000,128,128] as INT8 (per-token
                   scales) and as f16: the same l2-normalised Gaussian rows
                   quantised two ways; k1 = 1,000 candidates, k = 100, seed 7
+ colpali_out_of_core  one query Q [1,32,128] bf16 against a corpus of 100,000
+                  documents x 1,024 patches x 128 bf16 (26 GB) held in host
+                  memory and streamed in blocks of 20,000 documents, seed 8
  chamfer_100k     one pair of 3-D point clouds of 100,000 points each
                   (standard normal coordinates, float32) and an upstream
                   gradient N(0,1) per pair, seed 6: the Chamfer-distance
@@ -46,6 +49,7 @@ SPECS = {
                           pairs_per_query=10_000),
     "chamfer_100k": dict(B=1, N=100_000, M=100_000, dim=3, seed=6),
     "two_stage_topk": dict(Nq=32, Lq=32, Nd=100_000, Ld=128, dim=128, k1=1000, k=100, seed=7),
+    "colpali_out_of_core": dict(Nq=1, Lq=32, Nd=100_000, Ld=1024, dim=128, dtype="bf16", block_docs=20_000, seed=8),
 }
 
 
@@ -108,6 +112,23 @@ def two_stage(Nq, Lq, Nd, Ld, dim, k1, k, seed):
     return w
 
 
+def out_of_core(Nq, Lq, Nd, Ld, dim, dtype, block_docs, seed):
+    """The query batch only: the corpus is written by fill_corpus into
+    caller-provided (page-locked) host memory, block by block."""
+    w = dict(Nq=Nq, Lq=Lq, Nd=Nd, Ld=Ld, dim=dim, dtype=dtype, block_docs=block_docs, seed=seed)
+    w["Q"] = gaussian_rows(seed, TID_Q, Nq * Lq, dim, dtype).reshape(Nq, Lq, dim)
+    return w
+
+
+def fill_corpus(w, out, chunk_docs=4096):
+    """Document rows of an out-of-core workload into out (uint16 [Nd*Ld, dim])."""
+    rows = w["Ld"] * chunk_docs
+    for r0 in range(0, w["Nd"] * w["Ld"], rows):
+        n = min(rows, w["Nd"] * w["Ld"] - r0)
+        gaussian_rows(w["seed"], TID_D, n, w["dim"], w["dtype"], row0=r0, out=out[r0:r0 + n])
+    return out
+
+
 def clouds(B, N, M, dim, seed):
     """Point clouds P [B,N,dim], Q [B,M,dim] (float32, standard normal
     coordinates) and an upstream gradient grad [B] (float32, N(0,1))."""
@@ -132,5 +153,7 @@ def make(name: str, **overrides):
         return clouds(**spec)
     if name == "two_stage_topk":
         return two_stage(**spec)
+    if name == "colpali_out_of_core":
+        return out_of_core(**spec)
     grad = name == "contrastive_bwd"
     return dense(**spec, grad=grad)

@@ -59,7 +59,7 @@ typedef enum { MAXSIM_F16 = 0, MAXSIM_BF16 = 1 } maxsim_dtype;
 /* Operation codes for maxsim_workspace_size(). */
 enum { MAXSIM_OP_FWD = 0, MAXSIM_OP_FWD_VARLEN = 1, MAXSIM_OP_BWD = 2, MAXSIM_OP_FWD_INT8 = 3,
        MAXSIM_OP_SCORE_PAIRS = 4, MAXSIM_OP_CHAMFER_FWD = 5, MAXSIM_OP_CHAMFER_BWD = 6,
-       MAXSIM_OP_TWO_STAGE = 7 };
+       MAXSIM_OP_TWO_STAGE = 7, MAXSIM_OP_FWD_STREAMED = 8 };
 
 /*
  * Dense forward.
@@ -266,6 +266,27 @@ maxsim_status maxsim_two_stage_topk(const int8_t *Q8, const float *q_scale, cons
                                     size_t workspace_bytes, void *stream);
 
 /*
+ * Out-of-core dense forward ("Flash-MaxSim" Sec. 5.3): the corpus stays in
+ * host memory and is scored in blocks of `block_docs` documents, so device
+ * memory holds two blocks whatever the corpus size.
+ *   Q       [Nq, Lq, dim] f16 / bf16, DEVICE pointer;  q_mask [Nq, Lq] u8 device or NULL
+ *   D_host  [Nd, Ld, dim] same dtype, HOST pointer (page-locked memory lets the
+ *           copies overlap the scoring; pageable memory is correct but slower)
+ *   scores  [Nq, Nd] f32, device (out): equal to maxsim_fwd's
+ * The copy of block b + 1 (cudaMemcpyAsync on a copy stream the library owns,
+ * one per device) overlaps the forward of block b on `stream`; events order
+ * the two. The call only enqueues: later work on `stream` sees the scores.
+ * D_host must stay valid and unchanged until `stream` reaches that point.
+ * Calls from several host threads are serialised inside the library. No
+ * d_mask and no argmax. Workspace (two blocks, the block's scores, the
+ * forward's own scratch; 256-byte aligned):
+ * maxsim_workspace_size(MAXSIM_OP_FWD_STREAMED, Nq, Lq, block_docs, Ld, dim).
+ */
+maxsim_status maxsim_fwd_streamed(const void *Q, const void *D_host, maxsim_dtype dtype, int64_t Nq, int64_t Lq,
+                                  int64_t Nd, int64_t Ld, int64_t dim, int64_t block_docs, const uint8_t *q_mask,
+                                  float *scores, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace an operation needs for a shape (0 if none).
  *   MAXSIM_OP_FWD / MAXSIM_OP_FWD_INT8: (Nq, Lq, Nd, Ld, dim)
  *   MAXSIM_OP_FWD_VARLEN:              (Nq, max_lq, Nd, total_d, dim); assumes
@@ -276,6 +297,8 @@ maxsim_status maxsim_two_stage_topk(const int8_t *Q8, const float *q_scale, cons
  *   MAXSIM_OP_CHAMFER_FWD / _BWD:      (B, N, M, 0, dim)
  *   MAXSIM_OP_TWO_STAGE:               (Nq, Lq, Nd, Ld, dim); enough for any
  *                                      k1 <= min(Nd, 4096)
+ *   MAXSIM_OP_FWD_STREAMED:            (Nq, Lq, block_docs, Ld, dim); independent
+ *                                      of the corpus size
  * Returns (size_t)-1 for an invalid shape.
  */
 size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim);

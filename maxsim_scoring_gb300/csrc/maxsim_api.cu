@@ -734,6 +734,32 @@ TwoStagePlan plan_two_stage(int64_t Nq, int64_t Lq, int64_t Nd, int64_t dim, int
     return p;
 }
 
+struct StreamedPlan {
+    int64_t blk = 0;
+    size_t buf_bytes = 0, off_buf[2] = {0, 0}, off_scores = 0, off_fwd = 0, fwd_bytes = 0, bytes = 0;
+    bool ok = false;
+};
+
+StreamedPlan plan_streamed(int64_t Nq, int64_t Lq, int64_t blk, int64_t Ld, int64_t dim, int64_t elem) {
+    StreamedPlan p;
+    const FwdPlan f = plan_fwd(Nq, Lq, blk, dim, false, false);
+    if (!f.ok) return p;
+    p.blk = blk;
+    p.buf_bytes = static_cast<size_t>(blk * Ld * dim * elem);
+    size_t off = 0;
+    for (int i = 0; i < 2; ++i) {
+        p.off_buf[i] = off;
+        off = round_up(off + p.buf_bytes, 256);
+    }
+    p.off_scores = off;
+    off = round_up(off + static_cast<size_t>(Nq * blk) * 4, 256);
+    p.off_fwd = off;
+    p.fwd_bytes = f.ws_bytes;
+    p.bytes = round_up(off + f.ws_bytes, 256);
+    p.ok = true;
+    return p;
+}
+
 }  // namespace
 }  // namespace maxsim
 
@@ -787,6 +813,10 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
         off = round_up(off + static_cast<size_t>(Nd * Ld + 1) * 4, 256); // row_ptr
         off = round_up(off + static_cast<size_t>(Nq * Nd * Lq) * 4, 256);  // col
         return off;
+    }
+    case MAXSIM_OP_FWD_STREAMED: {  // (Nq, Lq, block_docs, Ld, dim)
+        const StreamedPlan p = plan_streamed(Nq, Lq, Nd, Ld, dim, 2);
+        return p.ok ? p.bytes : static_cast<size_t>(-1);
     }
     case MAXSIM_OP_TWO_STAGE: {  // (Nq, Lq, Nd, Ld, dim), for any k1 <= min(Nd, 4096)
         const TwoStagePlan p = plan_two_stage(Nq, Lq, Nd, dim, std::min<int64_t>(Nd, kTopkMaxK));
@@ -1359,4 +1389,96 @@ extern "C" maxsim_status maxsim_fwd_varlen_noalloc(const void* Q, const int32_t*
     return maxsim_fwd_varlen(Q, cu_seqlens_q, max_lq, D, cu_seqlens_d, total_d, dtype, Nq, Nd, dim, q_mask, d_mask,
                              scores, argmax, scratch, need > 0 ? static_cast<size_t>(MAXSIM_NOALLOC_SCRATCH_BYTES) : 0,
                              stream);
+}
+
+// ---------------------------------------------------------------- out-of-core forward
+//
+// A corpus held in host memory is scored block by block ("Flash-MaxSim" Sec.
+// 5.3: peak device memory is one streamed document block): the copy of block
+// b + 1 into one of two device buffers runs on the library's copy stream
+// while block b is scored on the caller's stream. Events order the two
+// streams: a buffer is refilled only after the forward that read it, and a
+// forward starts only after its block has arrived.
+
+namespace maxsim {
+namespace {
+
+struct StreamRes {
+    bool init = false;
+    cudaStream_t copy = nullptr;
+    cudaEvent_t start = nullptr, copied[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr};
+};
+
+std::mutex g_stream_mu;  // also serialises the enqueue of whole streamed calls
+StreamRes g_stream_res[kMaxDevices];
+
+maxsim_status stream_res(StreamRes** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MAXSIM_ERR_CUDA;
+    StreamRes& r = g_stream_res[dev];
+    if (!r.init) {
+        if (cudaStreamCreateWithFlags(&r.copy, cudaStreamNonBlocking) != cudaSuccess) return MAXSIM_ERR_CUDA;
+        cudaEvent_t* evs[5] = {&r.start, &r.copied[0], &r.copied[1], &r.done[0], &r.done[1]};
+        for (cudaEvent_t* e : evs)
+            if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return MAXSIM_ERR_CUDA;
+        r.init = true;
+    }
+    *out = &r;
+    return MAXSIM_OK;
+}
+
+}  // namespace
+}  // namespace maxsim
+
+extern "C" maxsim_status maxsim_fwd_streamed(const void* Q, const void* D_host, maxsim_dtype dtype, int64_t Nq,
+                                             int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim, int64_t block_docs,
+                                             const uint8_t* q_mask, float* scores, void* workspace,
+                                             size_t workspace_bytes, void* stream) {
+    if (dtype != MAXSIM_F16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_INVALID_ARG;
+    if (Nq < 0 || Lq < 0 || Nd < 0 || Ld < 0 || block_docs <= 0) return MAXSIM_ERR_INVALID_ARG;
+    maxsim_status rc = check_dim(dim, 16);
+    if (rc != MAXSIM_OK) return rc;
+    if (Nq * Nd == 0) return MAXSIM_OK;
+    if (!scores || !aligned(scores, 4) || (Lq > 0 && (!Q || !aligned16(Q))) || (Ld > 0 && !D_host))
+        return MAXSIM_ERR_INVALID_ARG;
+    const int64_t blk = std::min(block_docs, Nd);
+    if (blk * Ld > kI32Max || Nq * pad_lq(Lq) > kI32Max || Nq * Nd > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
+    const StreamedPlan p = plan_streamed(Nq, Lq, blk, Ld, dim, 2);
+    if (!p.ok) return MAXSIM_ERR_UNSUPPORTED;
+    if (workspace_bytes < p.bytes || !workspace || !aligned(workspace, 256)) return MAXSIM_ERR_WORKSPACE;
+    std::lock_guard<std::mutex> lock(g_stream_mu);
+    StreamRes* res = nullptr;
+    if ((rc = stream_res(&res)) != MAXSIM_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t doc_bytes = static_cast<size_t>(Ld * dim * 2);
+    const uint8_t* host = static_cast<const uint8_t*>(D_host);
+    // the copy stream starts after everything already queued on the caller's stream
+    if (cudaEventRecord(res->start, st) != cudaSuccess || cudaStreamWaitEvent(res->copy, res->start, 0) != cudaSuccess)
+        return MAXSIM_ERR_CUDA;
+    const int64_t n_blocks = (Nd + blk - 1) / blk;
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        const int s = static_cast<int>(b & 1);
+        const int64_t j0 = b * blk, nb = std::min(blk, Nd - j0);
+        void* buf = ws + p.off_buf[s];
+        if (b >= 2 && cudaStreamWaitEvent(res->copy, res->done[s], 0) != cudaSuccess) return MAXSIM_ERR_CUDA;
+        if (nb * Ld > 0 && cudaMemcpyAsync(buf, host + static_cast<size_t>(j0) * doc_bytes,
+                                           static_cast<size_t>(nb) * doc_bytes, cudaMemcpyHostToDevice,
+                                           res->copy) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        if (cudaEventRecord(res->copied[s], res->copy) != cudaSuccess ||
+            cudaStreamWaitEvent(st, res->copied[s], 0) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        // one query: its block of scores is contiguous in the output
+        float* out = Nq == 1 ? scores + j0 : reinterpret_cast<float*>(ws + p.off_scores);
+        rc = maxsim_fwd(Q, buf, dtype, Nq, Lq, nb, Ld, dim, q_mask, nullptr, out, nullptr, ws + p.off_fwd,
+                        p.fwd_bytes, stream);
+        if (rc != MAXSIM_OK) return rc;
+        if (Nq > 1 && cudaMemcpy2DAsync(scores + j0, static_cast<size_t>(Nd) * 4, out, static_cast<size_t>(nb) * 4,
+                                        static_cast<size_t>(nb) * 4, static_cast<size_t>(Nq),
+                                        cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        if (cudaEventRecord(res->done[s], st) != cudaSuccess) return MAXSIM_ERR_CUDA;
+    }
+    return MAXSIM_OK;
 }

@@ -315,6 +315,32 @@ def maxsim_two_stage_topk(Q8: torch.Tensor, q_scale: torch.Tensor, D8: torch.Ten
     return top_idx, top_scores, s8, cand
 
 
+def maxsim_fwd_streamed(Q: torch.Tensor, D_host: torch.Tensor, q_mask=None, *, block_docs: int = 20_000,
+                        scores: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Scores [Nq, Nd] of a device query batch Q [Nq,Lq,d] against a corpus
+    D_host [Nd,Ld,d] in host memory (pin it for copy/compute overlap),
+    streamed in blocks of block_docs documents. The copies are asynchronous:
+    keep D_host alive and unchanged until the current stream has passed this
+    call (synchronise, or wait on an event recorded after it)."""
+    if Q.dtype not in _DT or D_host.dtype != Q.dtype:
+        raise TypeError("Q and D_host must both be float16 or both bfloat16")
+    if D_host.is_cuda or not D_host.is_contiguous():
+        raise ValueError("D_host must be a contiguous host tensor")
+    dev = Q.device
+    Q = _contig(Q, "Q")
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, _ = D_host.shape
+    qm = _mask(q_mask, "q_mask", dev)
+    if scores is None:
+        scores = torch.empty((Nq, Nd), dtype=torch.float32, device=dev)
+    ws, nbytes = _workspace(workspace_size(_native.OP_FWD_STREAMED, Nq, Lq, min(block_docs, max(Nd, 1)), Ld, dim),
+                            dev, workspace)
+    rc = _native.lib().maxsim_fwd_streamed(_ptr(Q), D_host.data_ptr(), _DT[Q.dtype], Nq, Lq, Nd, Ld, dim, block_docs,
+                                           _ptr(qm), _ptr(scores), _ptr(ws), nbytes, _stream(dev))
+    _native.check(rc, "maxsim_fwd_streamed")
+    return scores
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device status word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)

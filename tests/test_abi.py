@@ -159,3 +159,17 @@ def test_topk_and_two_stage_host_validation(lib):
     assert call(a14=None) == 1           # no output
     assert call(a19=1024) == 5            # far too small
     assert call(a18=FAKE + 16) == 5      # workspace alignment
+
+
+def test_streamed_host_validation(lib):
+    f = lib.maxsim_fwd_streamed
+    need = lib.maxsim_workspace_size(8, 1, 32, 20000, 1024, 128)
+    assert need >= 2 * 20000 * 1024 * 128 * 2          # two device blocks
+    assert lib.maxsim_workspace_size(8, 1, 32, 20000, 1024, 128) == need  # independent of the corpus size
+    # Q, D_host, dtype, Nq, Lq, Nd, Ld, dim, block, q_mask, scores, ws, bytes, stream
+    assert f(FAKE, FAKE, 0, 1, 32, 0, 1024, 128, 20000, None, FAKE, None, 0, None) == 0  # no documents
+    assert f(FAKE, FAKE, 0, 1, 32, 5, 1024, 128, 0, None, FAKE, FAKE, need, None) == 1   # block of 0
+    assert f(FAKE, FAKE, 0, 1, 32, 5, 1024, 128, 20000, None, None, FAKE, need, None) == 1
+    assert f(FAKE, None, 0, 1, 32, 5, 1024, 128, 20000, None, FAKE, FAKE, need, None) == 1
+    assert f(FAKE, FAKE, 0, 1, 32, 5, 1024, 24, 20000, None, FAKE, FAKE, need, None) == 2  # dim
+    assert f(FAKE, FAKE, 0, 1, 32, 50000, 1024, 128, 20000, None, FAKE, FAKE, 1024, None) == 5
