@@ -243,6 +243,15 @@ def describe(w, spec):
         cfg = {"workload": text, "B": w["B"], "N": w["N"], "M": w["M"], "dim": w["dim"],
                "l2": "inputs (2.4 MB) stay in L2 by design: the step is ALU-bound; no flush"}
         return cfg
+    if name == "colbert_varlen_bwd":
+        text = (f"colbert_varlen_bwd: backward of Q [{w['Nq']},{w['Lq']},{w['dim']}] {w['dtype']} vs Nd={w['Nd']} "
+                f"packed documents, Ld~U[{spec['ld_min']},{spec['ld_max']}] (sum Ld={w['total_d']}), grad N(0,1), "
+                f"argmax from one varlen forward at setup; l2-normalised Gaussian rows, seed {spec['seed']}")
+        cfg = {"workload": text, "Nq": w["Nq"], "Lq": w["Lq"], "Nd": w["Nd"], "total_d": w["total_d"], "dim": w["dim"]}
+        moved = (w["total_d"] * w["dim"] * 6 + 3 * w["Nq"] * w["Nd"] * w["Lq"] * 4)
+        cfg["l2"] = ("D, dD, the argmax and the CSR (%.2f GB) exceed L2: no flush" % (moved / 1e9)
+                     if moved > L2_BYTES else "smaller than L2")
+        return cfg
     if name == "colpali_out_of_core":
         text = (f"colpali_out_of_core: Q [{w['Nq']},{w['Lq']},{w['dim']}] {w['dtype']} on the device vs a corpus D "
                 f"[{w['Nd']},{w['Ld']},{w['dim']}] {w['dtype']} ({w['Nd'] * w['Ld'] * w['dim'] * 2 / 1e9:.1f} GB) in "
@@ -678,6 +687,68 @@ class TwoStageCase:
         pass  # the corpus (1.7 GB INT8 + 3.3 GB f16) is far larger than L2
 
 
+class VarlenBwdCase:
+    """Backward over packed documents (maxsim_bwd_varlen) through the argmax
+    of one varlen forward done at setup: CSR build, dD, dQ."""
+
+    def __init__(self, w, device):
+        import torch as t
+
+        from maxsim_scoring_gb300 import _native, ops
+        self.w, self.device, self.ops, self.t = w, device, ops, t
+        self.name = w["name"]
+        Nq, Lq, Nd, T, dim = w["Nq"], w["Lq"], w["Nd"], w["total_d"], w["dim"]
+        dt = t.bfloat16 if w["dtype"] == "bf16" else t.float16
+
+        def pinned(x):
+            return t.from_numpy(np.ascontiguousarray(x)).pin_memory()
+
+        self.h_in = {"Q": t.from_numpy(np.ascontiguousarray(w["Q"]).view(np.int16)).view(dt).pin_memory(),
+                     "D": t.from_numpy(np.ascontiguousarray(w["D"]).view(np.int16)).view(dt).pin_memory(),
+                     "cu_seqlens_d": pinned(w["cu_seqlens_d"]), "grad": pinned(w["grad"])}
+        self.d_in = {k: v.to(device) for k, v in self.h_in.items()}
+        self.e2e_in = {k: t.empty_like(v) for k, v in self.d_in.items()}
+        _, self.argmax = ops.maxsim_fwd_varlen(self.d_in["Q"], None, Lq, self.d_in["D"], self.d_in["cu_seqlens_d"],
+                                               want_argmax=True)
+        self.h_argmax = self.argmax.cpu().pin_memory()
+        self.h_in["argmax"] = self.h_argmax
+        self.d_in["argmax"] = self.argmax
+        self.e2e_in["argmax"] = t.empty_like(self.argmax)
+        self.ws = t.empty(ops.workspace_size(_native.OP_BWD_VARLEN, Nq, Lq, Nd, T, dim), dtype=t.uint8, device=device)
+        self.out = None
+        self.h_dq = t.empty((Nq, Lq, dim), dtype=t.float32).pin_memory()
+        self.units = Nd
+        n_src = Nq * Nd * Lq
+        self.flops = 2 * 2 * Nq * Nd * Lq * dim
+        # read Q, D, argmax (count and place), g; write and re-read the CSR; write dQ and dD
+        self.bytes = (Nq * Lq * dim * 2 + T * dim * 2 + 2 * n_src * 4 + Nq * Nd * 4
+                      + 2 * (T + 1 + n_src) * 4 + (Nq * Lq + T) * dim * 4)
+        self.bound, self.dtype, self.launches = "hbm", w["dtype"], 6  # check_cu, count, scan, build, dD, dQ
+
+    def call(self, d):
+        w = self.w
+        self.out = self.ops.maxsim_bwd_varlen(d["Q"], None, w["Lq"], d["D"], d["cu_seqlens_d"], w["max_ld"],
+                                              d["argmax"], d["grad"], workspace=self.ws)
+
+    def step(self):
+        self.call(self.d_in)
+
+    def e2e_step(self):
+        for k, v in self.h_in.items():
+            self.e2e_in[k].copy_(v, non_blocking=True)
+        self.call(self.e2e_in)
+        self.h_dq.copy_(self.out[0], non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.h_in.values())
+
+    def d2h_bytes(self):
+        return self.h_dq.numel() * 4
+
+    def flush(self):
+        pass  # D (0.17 GB), argmax and the CSR exceed L2 together; see config
+
+
 class OutOfCoreCase:
     """One query against a corpus in page-locked host memory, scored block by
     block (maxsim_fwd_streamed). The host-to-device link bounds it: its peak
@@ -762,7 +833,8 @@ def run_ours(args, rank, world, local_rank):
     w, spec = make_workload(args.workload, rank, world, args.shard, args.nd)
     case = (ChamferCase(w, device) if args.workload.startswith("chamfer") else
             TwoStageCase(w, device) if args.workload == "two_stage_topk" else
-            OutOfCoreCase(w, device) if args.workload == "colpali_out_of_core" else Case(w, device))
+            OutOfCoreCase(w, device) if args.workload == "colpali_out_of_core" else
+            VarlenBwdCase(w, device) if args.workload == "colbert_varlen_bwd" else Case(w, device))
     metric, unit_name = metric_of(args.workload)
     stream = torch.cuda.current_stream(device)
 
@@ -853,7 +925,8 @@ def run_ours(args, rank, world, local_rank):
     roofline = {
         "bound": case.bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": src,
-        "kernel": ("the streamed corpus copy (cudaMemcpyAsync, overlapped with maxsim_fwd_kernel on each block; "
+        "kernel": ("backward kernels (whole maxsim_bwd_varlen call)" if case.name == "colbert_varlen_bwd" else
+                   "the streamed corpus copy (cudaMemcpyAsync, overlapped with maxsim_fwd_kernel on each block; "
                    "duration = the whole maxsim_fwd_streamed call)" if case.bound == "h2d" else
                    "chamfer_nn_kernel (duration = the whole maxsim_chamfer_fwd call, CUDA events per step: "
                    f"{kernel_ms:.4f} ms; it also runs the merge and loss kernels)" if case.bound == "alu" else
@@ -872,7 +945,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": case.launches * args.steps,
         "step_ms_min_median_max": [min(per_step_ms), statistics.median(per_step_ms), max(per_step_ms)],
     }
-    if world == 1 and not args.no_cpu_baseline and case.name != "contrastive_bwd":
+    if world == 1 and not args.no_cpu_baseline and case.name not in ("contrastive_bwd", "colbert_varlen_bwd"):
         n = calibrated_sample(w, target_s=args.cpu_seconds)
         rate, dt, what = oracle_sample(w, n)
         line["cpu_baseline"] = {"value": rate, "unit": unit_name, "cores": oracle_cores(w), "kind": "oracle",

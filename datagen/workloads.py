@@ -20,6 +20,9 @@ generators in this package.
                   (a reranker's candidate lists), seed 2
 Every row is an l2-normalised Gaussian vector rounded once to its storage type.
 
+ colbert_varlen_bwd  training-side backward on packed documents: Q [64,32,128]
+                  bf16, D packed with Ld ~ U{32..300}, Nd = 4,096, grad [64,4096]
+                  f32 N(0,1), seed 9
  two_stage_topk   Q [32,32,128] and D [100000,128,128] as INT8 (per-token
                   scales) and as f16: the same l2-normalised Gaussian rows
                   quantised two ways; k1 = 1,000 candidates, k = 100, seed 7
@@ -49,6 +52,7 @@ SPECS = {
                           pairs_per_query=10_000),
     "chamfer_100k": dict(B=1, N=100_000, M=100_000, dim=3, seed=6),
     "two_stage_topk": dict(Nq=32, Lq=32, Nd=100_000, Ld=128, dim=128, k1=1000, k=100, seed=7),
+    "colbert_varlen_bwd": dict(Nq=64, Lq=32, Nd=4096, ld_min=32, ld_max=300, dim=128, dtype="bf16", seed=9),
     "colpali_out_of_core": dict(Nq=1, Lq=32, Nd=100_000, Ld=1024, dim=128, dtype="bf16", block_docs=20_000, seed=8),
 }
 
@@ -147,6 +151,10 @@ def make(name: str, **overrides):
         return varlen(**spec)
     if name == "colbert_pairs":
         return pairs(**spec)
+    if name == "colbert_varlen_bwd":
+        w = varlen(**spec)
+        w["grad"] = normal_f32(spec["seed"], TID_GRAD, w["Nq"] * w["Nd"]).reshape(w["Nq"], w["Nd"])
+        return w
     if name == "int8_rerank":
         return int8(**spec)
     if name == "chamfer_100k":

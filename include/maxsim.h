@@ -59,7 +59,7 @@ typedef enum { MAXSIM_F16 = 0, MAXSIM_BF16 = 1 } maxsim_dtype;
 /* Operation codes for maxsim_workspace_size(). */
 enum { MAXSIM_OP_FWD = 0, MAXSIM_OP_FWD_VARLEN = 1, MAXSIM_OP_BWD = 2, MAXSIM_OP_FWD_INT8 = 3,
        MAXSIM_OP_SCORE_PAIRS = 4, MAXSIM_OP_CHAMFER_FWD = 5, MAXSIM_OP_CHAMFER_BWD = 6,
-       MAXSIM_OP_TWO_STAGE = 7, MAXSIM_OP_FWD_STREAMED = 8 };
+       MAXSIM_OP_TWO_STAGE = 7, MAXSIM_OP_FWD_STREAMED = 8, MAXSIM_OP_BWD_VARLEN = 9 };
 
 /*
  * Dense forward.
@@ -287,6 +287,32 @@ maxsim_status maxsim_fwd_streamed(const void *Q, const void *D_host, maxsim_dtyp
                                   float *scores, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Backward over packed layouts: the gradient of maxsim_fwd_varlen through its
+ * saved argmax ("Flash-MaxSim" Sec. 4.2, Eqs. (2)-(3), on the packed layout of
+ * Sec. 4.3.2; the pages' own varlen backward scatters with atomics, this one
+ * keeps the destination-owned CSR reduction of Sec. 4.2.3).
+ *   Q, cu_seqlens_q, max_lq   as for maxsim_fwd_varlen (dense Q when cu_seqlens_q is NULL)
+ *   D [total_d, dim], cu_seqlens_d [Nd + 1]; max_ld >= every document length
+ *   argmax       [Nq * Nd, max_lq] i32 from maxsim_fwd_varlen (t relative to the
+ *                document's first row, -1 past a query's end)
+ *   grad_scores  [Nq, Nd] f32;  q_mask one byte per query row of Q's layout, or NULL
+ *   dQ           Q's layout, f32 (out, optional): packed [cu_seqlens_q[Nq], dim] or
+ *                dense [Nq, max_lq, dim]
+ *   dD           [total_d, dim] f32 (out, optional)
+ *   csr_row_ptr  [total_d + 1] i32 (out, optional): CSR rows are D's packed rows
+ *   csr_col      [Nq * Nd * max_lq] i32 (out, optional): sources p = (i*Nd + j)*max_lq + s
+ * Deterministic, no atomics on the gradients. Inconsistent offsets, a document
+ * longer than max_ld, or an argmax outside its document or past its query's end
+ * are skipped and reported as MAXSIM_ERR_DEVICE_INPUT. Workspace:
+ * maxsim_workspace_size(MAXSIM_OP_BWD_VARLEN, Nq, max_lq, Nd, total_d, dim).
+ */
+maxsim_status maxsim_bwd_varlen(const void *Q, const int32_t *cu_seqlens_q, int64_t max_lq, const void *D,
+                                const int32_t *cu_seqlens_d, int64_t total_d, int64_t max_ld, maxsim_dtype dtype,
+                                int64_t Nq, int64_t Nd, int64_t dim, const uint8_t *q_mask, const int32_t *argmax,
+                                const float *grad_scores, float *dQ, float *dD, int32_t *csr_row_ptr,
+                                int32_t *csr_col, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace an operation needs for a shape (0 if none).
  *   MAXSIM_OP_FWD / MAXSIM_OP_FWD_INT8: (Nq, Lq, Nd, Ld, dim)
  *   MAXSIM_OP_FWD_VARLEN:              (Nq, max_lq, Nd, total_d, dim); assumes
@@ -299,6 +325,8 @@ maxsim_status maxsim_fwd_streamed(const void *Q, const void *D_host, maxsim_dtyp
  *                                      k1 <= min(Nd, 4096)
  *   MAXSIM_OP_FWD_STREAMED:            (Nq, Lq, block_docs, Ld, dim); independent
  *                                      of the corpus size
+ *   MAXSIM_OP_BWD_VARLEN:              (Nq, max_lq, Nd, total_d, dim); assumes
+ *                                      the CSR outputs are NULL (an upper bound)
  * Returns (size_t)-1 for an invalid shape.
  */
 size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim);

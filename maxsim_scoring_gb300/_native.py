@@ -26,7 +26,7 @@ STATUS = {
 }
 
 OP_FWD, OP_FWD_VARLEN, OP_BWD, OP_FWD_INT8, OP_SCORE_PAIRS = 0, 1, 2, 3, 4
-OP_CHAMFER_FWD, OP_CHAMFER_BWD, OP_TWO_STAGE, OP_FWD_STREAMED = 5, 6, 7, 8
+OP_CHAMFER_FWD, OP_CHAMFER_BWD, OP_TWO_STAGE, OP_FWD_STREAMED, OP_BWD_VARLEN = 5, 6, 7, 8, 9
 F16, BF16 = 0, 1
 
 # Every symbol the header declares, with its ctypes signature.
@@ -46,6 +46,8 @@ SIGNATURES = {
     "maxsim_chamfer_fwd": (_I, [_VP, _VP, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_chamfer_bwd": (_I, [_VP, _VP, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_topk": (_I, [_VP, _I64, _I64, _I64, _VP, _VP, _VP]),
+    "maxsim_bwd_varlen": (_I, [_VP, _VP, _I64, _VP, _VP, _I64, _I64, _I, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP,
+                               _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_fwd_streamed": (_I, [_VP, _VP, _I, _I64, _I64, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_two_stage_topk": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _VP,
                                    _VP, _VP, _VP, _VP, _SZ, _VP]),

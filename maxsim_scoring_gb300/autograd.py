@@ -51,3 +51,31 @@ def chamfer_distance(P: torch.Tensor, Q: torch.Tensor) -> torch.Tensor:
     (float32): the forward saves the nearest indices, the backward routes the
     gradient through their inverse ("Flash-MaxSim" Sec. 4.2.4)."""
     return _Chamfer.apply(P, Q)
+
+
+class _MaxSimVarlen(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, Q, cu_seqlens_q, max_lq, D, cu_seqlens_d, max_ld):
+        scores, argmax = ops.maxsim_fwd_varlen(Q, cu_seqlens_q, max_lq, D, cu_seqlens_d, want_argmax=True)
+        ctx.save_for_backward(Q, D, argmax, cu_seqlens_d,
+                              cu_seqlens_q if cu_seqlens_q is not None else torch.empty(0, dtype=torch.int32))
+        ctx.has_cu_q = cu_seqlens_q is not None
+        ctx.max_lq, ctx.max_ld = max_lq, max_ld
+        return scores
+
+    @staticmethod
+    def backward(ctx, grad_scores):
+        Q, D, argmax, cu_d, cu_q = ctx.saved_tensors
+        dQ, dD, _, _ = ops.maxsim_bwd_varlen(Q, cu_q if ctx.has_cu_q else None, ctx.max_lq, D, cu_d, ctx.max_ld, argmax,
+                                             grad_scores.float().contiguous(), want_dq=ctx.needs_input_grad[0],
+                                             want_dd=ctx.needs_input_grad[3])
+        dQ = dQ.to(Q.dtype) if dQ is not None else None
+        dD = dD.to(D.dtype) if dD is not None else None
+        return dQ, None, None, dD, None, None
+
+
+def maxsim_varlen(Q: torch.Tensor, cu_seqlens_q, max_lq: int, D: torch.Tensor, cu_seqlens_d: torch.Tensor,
+                  max_ld: int) -> torch.Tensor:
+    """Differentiable MaxSim over packed documents (and optionally packed
+    queries): scores [Nq, Nd]."""
+    return _MaxSimVarlen.apply(Q, cu_seqlens_q, max_lq, D, cu_seqlens_d, max_ld)

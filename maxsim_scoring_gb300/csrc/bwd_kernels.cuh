@@ -8,6 +8,10 @@
 //  * dQ, row-owned: one warp per query token gathers D at the winners of every
 //    document in ascending j (Eq. (2)).
 // Everything is deterministic: integer counts, fixed summation orders.
+// Packed layouts (the varlen path of Sec. 4.3.2) change only where rows live:
+// document j owns D rows cu_d[j] .. cu_d[j+1]-1 (its CSR rows are the same
+// row numbers), query i owns Q rows cu_q[i] .. cu_q[i+1]-1; the argmax keeps
+// its [Nq*Nd, max_lq] layout with -1 past a query's end.
 #pragma once
 
 #include <cstdint>
@@ -29,7 +33,26 @@ struct BwdArgs {
     int32_t* doc_cnt;      // [Nd]
     int32_t* doc_base;     // [Nd + 1]
     int* status;
+    const int32_t* cu_q;   // [Nq + 1] or NULL: dense Q, rows i*lq + s
+    const int32_t* cu_d;   // [Nd + 1] or NULL: dense D, rows j*ld + t (packed: ld is the longest document)
+    int64_t d_rows;        // rows of D: Nd*ld dense, total_d packed
 };
+
+// Length of document j (-1: an inconsistent packed offset, reported, no rows used).
+__device__ __forceinline__ int32_t doc_len(const BwdArgs& b, int32_t j) {
+    if (!b.cu_d) return b.ld;
+    const int32_t n = b.cu_d[j + 1] - b.cu_d[j];
+    return (n < 0 || n > b.ld) ? -1 : n;
+}
+__device__ __forceinline__ int64_t doc_row0(const BwdArgs& b, int32_t j) {
+    return b.cu_d ? static_cast<int64_t>(b.cu_d[j]) : static_cast<int64_t>(j) * b.ld;
+}
+__device__ __forceinline__ int32_t query_len(const BwdArgs& b, int32_t i) {
+    return b.cu_q ? b.cu_q[i + 1] - b.cu_q[i] : b.lq;
+}
+__device__ __forceinline__ int64_t query_row(const BwdArgs& b, int32_t i, int32_t s) {
+    return b.cu_q ? static_cast<int64_t>(b.cu_q[i]) + s : static_cast<int64_t>(i) * b.lq + s;
+}
 
 __device__ __forceinline__ float bits_to_f32(uint16_t h, int32_t is_bf16) {
     return is_bf16 ? __uint_as_float(static_cast<uint32_t>(h) << 16) : __half2float(__ushort_as_half(h));
@@ -43,17 +66,29 @@ __device__ __forceinline__ int64_t src_index(const BwdArgs& b, int32_t j, int32_
     return (static_cast<int64_t>(i) * b.nd + j) * b.lq + s;
 }
 
+// A source past its query's end (packed Q) has no Q row: it may only hold -1.
+__device__ __forceinline__ bool src_in_query(const BwdArgs& b, int32_t n) {
+    if (!b.cu_q) return true;
+    const int32_t i = n / b.lq, s = n - (n / b.lq) * b.lq;
+    return s < query_len(b, i);
+}
+
 // Per-document count of sources with a valid winner.
 __global__ void __launch_bounds__(256) csr_count_kernel(const BwdArgs b) {
     const int32_t j = blockIdx.x;
     const int32_t nsrc = b.nq * b.lq;
+    const int32_t ldj = doc_len(b, j);
     int32_t cnt = 0;
-    bool bad = false;
+    bool bad = ldj < 0;
 #pragma unroll 8
-    for (int32_t n = threadIdx.x; n < nsrc; n += blockDim.x) {
+    for (int32_t n = threadIdx.x; n < nsrc && ldj >= 0; n += blockDim.x) {
         int32_t a = b.argmax[src_index(b, j, n)];
-        if (a >= 0 && a < b.ld) ++cnt;
-        else if (!argmax_ok(a, b.ld)) bad = true;
+        if (a >= 0 && !src_in_query(b, n)) {
+            bad = true;
+            continue;
+        }
+        if (a >= 0 && a < ldj) ++cnt;
+        else if (!argmax_ok(a, ldj)) bad = true;
     }
     if (bad && b.status) atomicCAS(b.status, 0, 6);
     __shared__ int32_t red[8];
@@ -101,7 +136,7 @@ __global__ void __launch_bounds__(1024) csr_doc_scan_kernel(const BwdArgs b) {
     }
     if (threadIdx.x == 0) {
         b.doc_base[b.nd] = carry;
-        b.row_ptr[static_cast<int64_t>(b.nd) * b.ld] = carry;
+        b.row_ptr[b.d_rows] = carry;
     }
 }
 
@@ -116,6 +151,8 @@ __global__ void __launch_bounds__(256) csr_build_kernel(const BwdArgs b, int32_t
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int32_t nsrc = b.nq * b.lq;
     const int32_t per = (nsrc + nw - 1) / nw;
+    const int32_t ldj = max(doc_len(b, j), 0);  // an inconsistent document gets no rows
+    const int64_t row0 = doc_row0(b, j);
     for (int32_t x = threadIdx.x; x < nw * b.ld; x += blockDim.x) hist[x] = 0;
     __syncthreads();
     if (warp < nw) {
@@ -123,15 +160,15 @@ __global__ void __launch_bounds__(256) csr_build_kernel(const BwdArgs b, int32_t
 #pragma unroll 4
         for (int32_t n = n0 + lane; n < n1; n += 32) {
             int32_t a = b.argmax[src_index(b, j, n)];
-            if (a >= 0 && a < b.ld) atomicAdd(&hist[warp * b.ld + a], 1);
+            if (a >= 0 && a < ldj && src_in_query(b, n)) atomicAdd(&hist[warp * b.ld + a], 1);
         }
     }
     __syncthreads();
     // exclusive scan over destinations t of the per-row totals; each thread
     // owns a contiguous range of t
     __shared__ int32_t part[256];
-    const int32_t tper = (b.ld + blockDim.x - 1) / blockDim.x;
-    const int32_t t0 = threadIdx.x * tper, t1 = min(t0 + tper, b.ld);
+    const int32_t tper = (ldj + blockDim.x - 1) / blockDim.x;
+    const int32_t t0 = min(threadIdx.x * tper, ldj), t1 = min(t0 + tper, ldj);
     int32_t local = 0;
     for (int32_t t = t0; t < t1; ++t)
         for (int32_t w = 0; w < nw; ++w) local += hist[w * b.ld + t];
@@ -160,7 +197,7 @@ __global__ void __launch_bounds__(256) csr_build_kernel(const BwdArgs b, int32_t
     }
     int32_t run = b.doc_base[j] + part[threadIdx.x];
     for (int32_t t = t0; t < t1; ++t) {
-        b.row_ptr[static_cast<int64_t>(j) * b.ld + t] = run;
+        b.row_ptr[row0 + t] = run;
         for (int32_t w = 0; w < nw; ++w) {
             int32_t c = hist[w * b.ld + t];
             hist[w * b.ld + t] = run;  // becomes warp w's next free slot in row t
@@ -177,7 +214,7 @@ __global__ void __launch_bounds__(256) csr_build_kernel(const BwdArgs b, int32_t
             if (n < n1) {
                 p = src_index(b, j, n);
                 a = b.argmax[p];
-                if (!(a >= 0 && a < b.ld)) a = -1;
+                if (!(a >= 0 && a < ldj && src_in_query(b, n))) a = -1;
             }
             const uint32_t peers = __match_any_sync(0xFFFFFFFFu, a);
             if (a >= 0) {
@@ -257,24 +294,27 @@ template <int kVec>  // floats per lane (dim / 32, rounded up)
 __global__ void __launch_bounds__(256) dd_kernel(const BwdArgs b) {
     const int lane = threadIdx.x & 31;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int64_t nrows = static_cast<int64_t>(b.nd) * b.ld;
-    if (r >= nrows) return;
-    const int32_t j = static_cast<int32_t>(r / b.ld);
+    if (r >= b.d_rows) return;
     float acc[kVec];
 #pragma unroll
     for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
-    const int32_t e0 = b.row_ptr[r], e1 = b.row_ptr[r + 1];
+    int32_t e0 = b.row_ptr[r], e1 = b.row_ptr[r + 1];
+    // inconsistent packed offsets (reported by the checks) leave rows unset:
+    // never read outside the CSR
+    const int64_t n_col = static_cast<int64_t>(b.nq) * b.nd * b.lq;
+    if (e0 < 0 || e1 < e0 || e1 > n_col) e1 = e0 = 0;
     for (int32_t eb = e0; eb < e1; eb += 32) {
         const int32_t cnt = min(32, e1 - eb);
         int64_t off = 0;  // element offset of this lane's source row in Q
         float wl = 0.f;
         if (lane < cnt) {
-            const int32_t p = b.col[eb + lane];
+            const int32_t p = b.col[eb + lane];  // (i * Nd + j) * lq + s
             const int32_t s = p % b.lq;
-            const int32_t i = (p / b.lq) / b.nd;
+            const int32_t i = (p / b.lq) / b.nd, j = (p / b.lq) % b.nd;
+            const int64_t qr = query_row(b, i, s);
             wl = b.g[static_cast<int64_t>(i) * b.nd + j];
-            if (b.q_mask && !b.q_mask[static_cast<int64_t>(i) * b.lq + s]) wl = 0.f;
-            off = (static_cast<int64_t>(i) * b.lq + s) * b.dim;
+            if (b.q_mask && !b.q_mask[qr]) wl = 0.f;
+            off = qr * b.dim;
         }
         for (int32_t k = 0; k < cnt; k += kGather) {
             float x[kGather][kVec];
@@ -298,29 +338,37 @@ __global__ void __launch_bounds__(256) dd_kernel(const BwdArgs b) {
     store_row<kVec>(b.dD + r * b.dim, lane, b.dim, acc);
 }
 
-// dQ: one warp per query row (i, s), ascending j. The winners and weights of
-// 32 documents are loaded at once, one per lane.
+// dQ: one warp per (query row (i, s), chunk of documents), ascending j. The
+// winners and weights of 32 documents are loaded at once, one per lane. With
+// one chunk the warp writes dQ; with several (gridDim.y > 1, many documents
+// per query row) each chunk writes its partial row to `part` and
+// dq_reduce_kernel adds the chunks in order: a fixed summation order either way.
 template <int kVec>
-__global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b) {
+__global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b, float* __restrict__ part) {
     const int lane = threadIdx.x & 31;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nrows = static_cast<int64_t>(b.nq) * b.lq;
     if (r >= nrows) return;
     const int32_t i = static_cast<int32_t>(r / b.lq);
     const int32_t s = static_cast<int32_t>(r - static_cast<int64_t>(i) * b.lq);
+    if (s >= query_len(b, i)) return;  // no such row in packed Q
+    const int64_t qr = query_row(b, i, s);
+    const int32_t n_chunks = static_cast<int32_t>(gridDim.y);
+    const int32_t per = (b.nd + n_chunks - 1) / n_chunks;
+    const int32_t j_lo = static_cast<int32_t>(blockIdx.y) * per, j_hi = min(j_lo + per, b.nd);
     float acc[kVec];
 #pragma unroll
     for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
-    for (int32_t jb = 0; jb < b.nd; jb += 32) {
-        const int32_t cnt = min(32, b.nd - jb);
+    for (int32_t jb = j_lo; jb < j_hi; jb += 32) {
+        const int32_t cnt = min(32, j_hi - jb);
         int64_t off = 0;
         float wl = 0.f;  // 0 for a document without a winner (argmax -1)
         if (lane < cnt) {
             const int32_t j = jb + lane;
             const int32_t a = b.argmax[(static_cast<int64_t>(i) * b.nd + j) * b.lq + s];
-            if (a >= 0 && a < b.ld) {
+            if (a >= 0 && a < doc_len(b, j)) {
                 wl = b.g[static_cast<int64_t>(i) * b.nd + j];
-                off = (static_cast<int64_t>(j) * b.ld + a) * b.dim;
+                off = (doc_row0(b, j) + a) * b.dim;
             } else {
                 off = -1;
             }
@@ -346,12 +394,29 @@ __global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b) {
             }
         }
     }
-    const bool active = b.q_mask == nullptr || b.q_mask[r] != 0;
+    const bool active = b.q_mask == nullptr || b.q_mask[qr] != 0;
     if (!active) {
 #pragma unroll
         for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
     }
-    store_row<kVec>(b.dQ + r * b.dim, lane, b.dim, acc);
+    if (n_chunks == 1) store_row<kVec>(b.dQ + qr * b.dim, lane, b.dim, acc);
+    else store_row<kVec>(part + (static_cast<int64_t>(blockIdx.y) * nrows + r) * b.dim, lane, b.dim, acc);
+}
+
+// dQ row (i, s) = the chunk partials added in chunk order.
+__global__ void __launch_bounds__(256) dq_reduce_kernel(const BwdArgs b, const float* __restrict__ part,
+                                                        int32_t n_chunks) {
+    const int64_t nrows = static_cast<int64_t>(b.nq) * b.lq;
+    const int64_t total = nrows * b.dim;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = e / b.dim;
+        const int32_t i = static_cast<int32_t>(r / b.lq), s = static_cast<int32_t>(r % b.lq);
+        if (s >= query_len(b, i)) continue;
+        float v = part[e];
+        for (int32_t c = 1; c < n_chunks; ++c) v = __fadd_rn(v, part[c * total + e]);
+        b.dQ[query_row(b, i, s) * b.dim + (e - r * b.dim)] = v;
+    }
 }
 
 }  // namespace maxsim

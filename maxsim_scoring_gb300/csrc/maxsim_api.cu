@@ -760,6 +760,138 @@ StreamedPlan plan_streamed(int64_t Nq, int64_t Lq, int64_t blk, int64_t Ld, int6
     return p;
 }
 
+// Document chunks of the dQ gather: enough warps to fill the GPU when a query
+// row has many documents to visit, at least 64 documents per chunk.
+int32_t dq_chunks(int64_t Nq, int64_t lq, int64_t Nd) {
+    const int64_t rows = std::max<int64_t>(1, Nq * lq);
+    const int64_t want = (16384 + rows - 1) / rows;
+    return static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(want, Nd / 64)));
+}
+
+size_t bwd_ws_bytes(int64_t Nq, int64_t lq, int64_t Nd, int64_t d_rows, int64_t dim, bool have_rp, bool have_col) {
+    size_t off = 0;
+    off = round_up(off + static_cast<size_t>(Nd) * 4, 256);          // doc_cnt
+    off = round_up(off + static_cast<size_t>(Nd + 1) * 4, 256);      // doc_base
+    if (!have_rp) off = round_up(off + static_cast<size_t>(d_rows + 1) * 4, 256);
+    if (!have_col) off = round_up(off + static_cast<size_t>(Nq * Nd * lq) * 4, 256);
+    const int32_t c = dq_chunks(Nq, lq, Nd);
+    if (c > 1) off = round_up(off + static_cast<size_t>(c) * Nq * lq * dim * 4, 256);  // dQ partials
+    return off;
+}
+
+// Backward for dense (cu_q = cu_d = NULL, ld = the document length) and
+// packed layouts (cu_d given, ld = the longest document).
+maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void* D, const int32_t* cu_d,
+                      int64_t d_rows, int64_t Ld, maxsim_dtype dtype, int64_t Nq, int64_t Nd, int64_t dim,
+                      const uint8_t* q_mask, const int32_t* argmax, const float* grad_scores, float* dQ, float* dD,
+                      int32_t* csr_row_ptr, int32_t* csr_col, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    if (dtype != MAXSIM_F16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_INVALID_ARG;
+    maxsim_status rc = check_dim(dim, 16);
+    if (rc != MAXSIM_OK) return rc;
+    if (Nq * Nd * Lq > kI32Max || d_rows >= kI32Max || Nd * Ld >= (int64_t(1) << 40)) return MAXSIM_ERR_UNSUPPORTED;
+    // destination histograms: at least one warp's worth of Ld counters must fit
+    if (Ld * 4 > 200 * 1024) return MAXSIM_ERR_UNSUPPORTED;
+    const bool need_csr = dD || csr_row_ptr || csr_col;
+    if (need_csr || dQ) {
+        if (!argmax || !grad_scores) return MAXSIM_ERR_INVALID_ARG;
+        if ((Nq * Lq > 0 && (!Q || !aligned16(Q))) || (d_rows > 0 && (!D || !aligned16(D))))
+            return MAXSIM_ERR_INVALID_ARG;
+    }
+    // the gradient rows are written as whole vectors
+    if ((dQ && !aligned16(dQ)) || (dD && !aligned16(dD))) return MAXSIM_ERR_INVALID_ARG;
+    size_t off = 0;
+    const size_t off_cnt = off;
+    off = round_up(off + static_cast<size_t>(Nd) * 4, 256);
+    const size_t off_base = off;
+    off = round_up(off + static_cast<size_t>(Nd + 1) * 4, 256);
+    size_t off_rp = 0, off_col = 0, off_part = 0;
+    if (!csr_row_ptr) { off_rp = off; off = round_up(off + static_cast<size_t>(d_rows + 1) * 4, 256); }
+    if (!csr_col) { off_col = off; off = round_up(off + static_cast<size_t>(Nq * Nd * Lq) * 4, 256); }
+    const int32_t n_chunks = dQ ? dq_chunks(Nq, Lq, Nd) : 1;
+    if (n_chunks > 1) { off_part = off; off = round_up(off + static_cast<size_t>(n_chunks) * Nq * Lq * dim * 4, 256); }
+    if ((need_csr || n_chunks > 1) && (workspace_bytes < off || !workspace)) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+    BwdArgs b{};
+    b.Q = static_cast<const uint16_t*>(Q);
+    b.D = static_cast<const uint16_t*>(D);
+    b.is_bf16 = dtype == MAXSIM_BF16;
+    b.nq = static_cast<int32_t>(Nq);
+    b.lq = static_cast<int32_t>(Lq);
+    b.nd = static_cast<int32_t>(Nd);
+    b.ld = static_cast<int32_t>(Ld);
+    b.dim = static_cast<int32_t>(dim);
+    b.q_mask = q_mask;
+    b.argmax = argmax;
+    b.g = grad_scores;
+    b.dQ = dQ;
+    b.dD = dD;
+    b.status = dev->status;
+    b.cu_q = cu_q;
+    b.cu_d = cu_d;
+    b.d_rows = d_rows;
+    if (cu_d) check_cu_kernel<<<grid_for(Nd + 1, 256, dev->num_sms), 256, 0, st>>>(cu_d, Nd, d_rows, dev->status);
+    if (cu_q) check_cu_kernel<<<grid_for(Nq + 1, 256, dev->num_sms), 256, 0, st>>>(cu_q, Nq, -1, dev->status);
+    if (need_csr) {
+        b.doc_cnt = reinterpret_cast<int32_t*>(ws + off_cnt);
+        b.doc_base = reinterpret_cast<int32_t*>(ws + off_base);
+        b.row_ptr = csr_row_ptr ? csr_row_ptr : reinterpret_cast<int32_t*>(ws + off_rp);
+        b.col = csr_col ? csr_col : reinterpret_cast<int32_t*>(ws + off_col);
+        // packed: rows no document covers (inconsistent offsets) stay empty
+        if (cu_d && cudaMemsetAsync(b.row_ptr, 0, static_cast<size_t>(d_rows + 1) * 4, st) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        if (Nd > 0) {
+            csr_count_kernel<<<static_cast<int>(Nd), 256, 0, st>>>(b);
+        }
+        csr_doc_scan_kernel<<<1, 1024, 0, st>>>(b);
+        if (Nd > 0 && Ld > 0) {
+            int32_t nw = static_cast<int32_t>(std::min<int64_t>(8, (200 * 1024) / (Ld * 4)));
+            size_t shm = static_cast<size_t>(nw) * Ld * 4;
+            if (shm > 48 * 1024)
+                cudaFuncSetAttribute(csr_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(shm));
+            csr_build_kernel<<<static_cast<int>(Nd), 256, shm, st>>>(b, nw);
+        }
+        if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+    }
+    const int vec = static_cast<int>((dim + 31) / 32);
+    if (dD && d_rows > 0) {
+        const int grid = static_cast<int>((d_rows + 7) / 8);
+        switch (vec) {
+        case 1: dd_kernel<1><<<grid, 256, 0, st>>>(b); break;
+        case 2: dd_kernel<2><<<grid, 256, 0, st>>>(b); break;
+        case 3: dd_kernel<3><<<grid, 256, 0, st>>>(b); break;
+        case 4: dd_kernel<4><<<grid, 256, 0, st>>>(b); break;
+        case 5: dd_kernel<5><<<grid, 256, 0, st>>>(b); break;
+        case 6: dd_kernel<6><<<grid, 256, 0, st>>>(b); break;
+        case 7: dd_kernel<7><<<grid, 256, 0, st>>>(b); break;
+        default: dd_kernel<8><<<grid, 256, 0, st>>>(b); break;
+        }
+    }
+    if (dQ && Nq * Lq > 0) {
+        const int64_t rows = Nq * Lq;
+        const dim3 grid(static_cast<unsigned>((rows + 7) / 8), static_cast<unsigned>(n_chunks));
+        float* part = n_chunks > 1 ? reinterpret_cast<float*>(ws + off_part) : nullptr;
+        switch (vec) {
+        case 1: dq_kernel<1><<<grid, 256, 0, st>>>(b, part); break;
+        case 2: dq_kernel<2><<<grid, 256, 0, st>>>(b, part); break;
+        case 3: dq_kernel<3><<<grid, 256, 0, st>>>(b, part); break;
+        case 4: dq_kernel<4><<<grid, 256, 0, st>>>(b, part); break;
+        case 5: dq_kernel<5><<<grid, 256, 0, st>>>(b, part); break;
+        case 6: dq_kernel<6><<<grid, 256, 0, st>>>(b, part); break;
+        case 7: dq_kernel<7><<<grid, 256, 0, st>>>(b, part); break;
+        default: dq_kernel<8><<<grid, 256, 0, st>>>(b, part); break;
+        }
+        if (n_chunks > 1)
+            dq_reduce_kernel<<<grid_for(rows * dim, 256, dev->num_sms), 256, 0, st>>>(b, part, n_chunks);
+    }
+    return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace maxsim
 
@@ -806,14 +938,10 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
         return pairs_ws(plan_fwd(Nq, Lq, Nd, dim, true, false).ws_bytes, Nq, Ld).bytes;
     case MAXSIM_OP_FWD_INT8:
         return plan_fwd(Nq, Lq, Nd, dim, false, true).ws_bytes;
-    case MAXSIM_OP_BWD: {
-        size_t off = 0;
-        off = round_up(off + static_cast<size_t>(Nd) * 4, 256);          // doc_cnt
-        off = round_up(off + static_cast<size_t>(Nd + 1) * 4, 256);      // doc_base
-        off = round_up(off + static_cast<size_t>(Nd * Ld + 1) * 4, 256); // row_ptr
-        off = round_up(off + static_cast<size_t>(Nq * Nd * Lq) * 4, 256);  // col
-        return off;
-    }
+    case MAXSIM_OP_BWD:
+        return bwd_ws_bytes(Nq, Lq, Nd, Nd * Ld, dim, false, false);
+    case MAXSIM_OP_BWD_VARLEN:  // (Nq, max_lq, Nd, total_d, dim)
+        return bwd_ws_bytes(Nq, Lq, Nd, Ld, dim, false, false);
     case MAXSIM_OP_FWD_STREAMED: {  // (Nq, Lq, block_docs, Ld, dim)
         const StreamedPlan p = plan_streamed(Nq, Lq, Nd, Ld, dim, 2);
         return p.ok ? p.bytes : static_cast<size_t>(-1);
@@ -1022,99 +1150,20 @@ maxsim_status maxsim_bwd(const void* Q, const void* D, maxsim_dtype dtype, int64
                          int64_t Ld, int64_t dim, const uint8_t* q_mask, const int32_t* argmax,
                          const float* grad_scores, float* dQ, float* dD, int32_t* csr_row_ptr, int32_t* csr_col,
                          void* workspace, size_t workspace_bytes, void* stream) {
-    if (dtype != MAXSIM_F16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_INVALID_ARG;
     if (Nq < 0 || Lq < 0 || Nd < 0 || Ld < 0) return MAXSIM_ERR_INVALID_ARG;
-    maxsim_status rc = check_dim(dim, 16);
-    if (rc != MAXSIM_OK) return rc;
-    if (Nq * Nd * Lq > kI32Max || Nd * Ld >= kI32Max) return MAXSIM_ERR_UNSUPPORTED;
-    // destination histograms: at least one warp's worth of Ld counters must fit
-    if (Ld * 4 > 200 * 1024) return MAXSIM_ERR_UNSUPPORTED;
-    const bool need_csr = dD || csr_row_ptr || csr_col;
-    if (need_csr || dQ) {
-        if (!argmax || !grad_scores) return MAXSIM_ERR_INVALID_ARG;
-        if ((Nq * Lq > 0 && (!Q || !aligned16(Q))) || (Nd * Ld > 0 && (!D || !aligned16(D))))
-            return MAXSIM_ERR_INVALID_ARG;
-    }
-    // the gradient rows are written as whole vectors
-    if ((dQ && !aligned16(dQ)) || (dD && !aligned16(dD))) return MAXSIM_ERR_INVALID_ARG;
-    size_t off = 0;
-    const size_t off_cnt = off;
-    off = round_up(off + static_cast<size_t>(Nd) * 4, 256);
-    const size_t off_base = off;
-    off = round_up(off + static_cast<size_t>(Nd + 1) * 4, 256);
-    size_t off_rp = 0, off_col = 0;
-    if (!csr_row_ptr) { off_rp = off; off = round_up(off + static_cast<size_t>(Nd * Ld + 1) * 4, 256); }
-    if (!csr_col) { off_col = off; off = round_up(off + static_cast<size_t>(Nq * Nd * Lq) * 4, 256); }
-    if (need_csr && (workspace_bytes < off || !workspace)) return MAXSIM_ERR_WORKSPACE;
-    DeviceInfo* dev = nullptr;
-    if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    return run_bwd(Q, nullptr, Lq, D, nullptr, Nd * Ld, Ld, dtype, Nq, Nd, dim, q_mask, argmax, grad_scores, dQ, dD,
+                   csr_row_ptr, csr_col, workspace, workspace_bytes, stream);
+}
 
-    BwdArgs b{};
-    b.Q = static_cast<const uint16_t*>(Q);
-    b.D = static_cast<const uint16_t*>(D);
-    b.is_bf16 = dtype == MAXSIM_BF16;
-    b.nq = static_cast<int32_t>(Nq);
-    b.lq = static_cast<int32_t>(Lq);
-    b.nd = static_cast<int32_t>(Nd);
-    b.ld = static_cast<int32_t>(Ld);
-    b.dim = static_cast<int32_t>(dim);
-    b.q_mask = q_mask;
-    b.argmax = argmax;
-    b.g = grad_scores;
-    b.dQ = dQ;
-    b.dD = dD;
-    b.status = dev->status;
-    if (need_csr) {
-        b.doc_cnt = reinterpret_cast<int32_t*>(ws + off_cnt);
-        b.doc_base = reinterpret_cast<int32_t*>(ws + off_base);
-        b.row_ptr = csr_row_ptr ? csr_row_ptr : reinterpret_cast<int32_t*>(ws + off_rp);
-        b.col = csr_col ? csr_col : reinterpret_cast<int32_t*>(ws + off_col);
-        if (Nd > 0) {
-            csr_count_kernel<<<static_cast<int>(Nd), 256, 0, st>>>(b);
-        }
-        csr_doc_scan_kernel<<<1, 1024, 0, st>>>(b);
-        if (Nd > 0 && Ld > 0) {
-            int32_t nw = static_cast<int32_t>(std::min<int64_t>(8, (200 * 1024) / (Ld * 4)));
-            size_t shm = static_cast<size_t>(nw) * Ld * 4;
-            if (shm > 48 * 1024)
-                cudaFuncSetAttribute(csr_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(shm));
-            csr_build_kernel<<<static_cast<int>(Nd), 256, shm, st>>>(b, nw);
-        }
-        if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
-    }
-    const int vec = static_cast<int>((dim + 31) / 32);
-    if (dD && Nd * Ld > 0) {
-        const int64_t rows = Nd * Ld;
-        const int grid = static_cast<int>((rows + 7) / 8);
-        switch (vec) {
-        case 1: dd_kernel<1><<<grid, 256, 0, st>>>(b); break;
-        case 2: dd_kernel<2><<<grid, 256, 0, st>>>(b); break;
-        case 3: dd_kernel<3><<<grid, 256, 0, st>>>(b); break;
-        case 4: dd_kernel<4><<<grid, 256, 0, st>>>(b); break;
-        case 5: dd_kernel<5><<<grid, 256, 0, st>>>(b); break;
-        case 6: dd_kernel<6><<<grid, 256, 0, st>>>(b); break;
-        case 7: dd_kernel<7><<<grid, 256, 0, st>>>(b); break;
-        default: dd_kernel<8><<<grid, 256, 0, st>>>(b); break;
-        }
-    }
-    if (dQ && Nq * Lq > 0) {
-        const int64_t rows = Nq * Lq;
-        const int grid = static_cast<int>((rows + 7) / 8);
-        switch (vec) {
-        case 1: dq_kernel<1><<<grid, 256, 0, st>>>(b); break;
-        case 2: dq_kernel<2><<<grid, 256, 0, st>>>(b); break;
-        case 3: dq_kernel<3><<<grid, 256, 0, st>>>(b); break;
-        case 4: dq_kernel<4><<<grid, 256, 0, st>>>(b); break;
-        case 5: dq_kernel<5><<<grid, 256, 0, st>>>(b); break;
-        case 6: dq_kernel<6><<<grid, 256, 0, st>>>(b); break;
-        case 7: dq_kernel<7><<<grid, 256, 0, st>>>(b); break;
-        default: dq_kernel<8><<<grid, 256, 0, st>>>(b); break;
-        }
-    }
-    return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+maxsim_status maxsim_bwd_varlen(const void* Q, const int32_t* cu_seqlens_q, int64_t max_lq, const void* D,
+                                const int32_t* cu_seqlens_d, int64_t total_d, int64_t max_ld, maxsim_dtype dtype,
+                                int64_t Nq, int64_t Nd, int64_t dim, const uint8_t* q_mask, const int32_t* argmax,
+                                const float* grad_scores, float* dQ, float* dD, int32_t* csr_row_ptr,
+                                int32_t* csr_col, void* workspace, size_t workspace_bytes, void* stream) {
+    if (Nq < 0 || max_lq < 0 || Nd < 0 || total_d < 0 || max_ld < 0) return MAXSIM_ERR_INVALID_ARG;
+    if (!cu_seqlens_d) return MAXSIM_ERR_INVALID_ARG;
+    return run_bwd(Q, cu_seqlens_q, max_lq, D, cu_seqlens_d, total_d, max_ld, dtype, Nq, Nd, dim, q_mask, argmax,
+                   grad_scores, dQ, dD, csr_row_ptr, csr_col, workspace, workspace_bytes, stream);
 }
 
 maxsim_status maxsim_fwd_int8(const int8_t* Q, const float* q_scale, const int8_t* D, const float* d_scale,

@@ -196,6 +196,39 @@ def maxsim_bwd(Q: torch.Tensor, D: torch.Tensor, argmax: torch.Tensor, grad_scor
     return dQ, dD, row_ptr, col
 
 
+def maxsim_bwd_varlen(Q: torch.Tensor, cu_seqlens_q: Optional[torch.Tensor], max_lq: int, D: torch.Tensor,
+                      cu_seqlens_d: torch.Tensor, max_ld: int, argmax: torch.Tensor, grad_scores: torch.Tensor,
+                      q_mask=None, *, want_dq: bool = True, want_dd: bool = True, want_csr: bool = False,
+                      workspace: Optional[torch.Tensor] = None):
+    """Gradient of maxsim_fwd_varlen: dQ in Q's layout, dD [total_d, d] (f32),
+    and optionally the CSR (row_ptr over D's packed rows, col)."""
+    if Q.dtype not in _DT or D.dtype != Q.dtype:
+        raise TypeError("Q and D must both be float16 or both bfloat16")
+    dev = Q.device
+    Q, D = _contig(Q, "Q"), _contig(D, "D", device=dev)
+    cu_q = _contig(cu_seqlens_q, "cu_seqlens_q", torch.int32, dev)
+    cu_d = _contig(cu_seqlens_d, "cu_seqlens_d", torch.int32, dev)
+    dim = Q.shape[-1]
+    Nq = (cu_q.numel() - 1) if cu_q is not None else Q.shape[0]
+    Nd = cu_d.numel() - 1
+    total_d = D.shape[0]
+    am = _contig(argmax, "argmax", torch.int32, dev)
+    g = _contig(grad_scores, "grad_scores", torch.float32, dev)
+    if am.numel() != Nq * Nd * max_lq or g.numel() != Nq * Nd:
+        raise ValueError("argmax must be [Nq*Nd, max_lq] and grad_scores [Nq, Nd]")
+    qm = _mask(q_mask, "q_mask", dev)
+    dQ = torch.empty(Q.shape, dtype=torch.float32, device=dev) if want_dq else None
+    dD = torch.empty((total_d, dim), dtype=torch.float32, device=dev) if want_dd else None
+    row_ptr = torch.empty(total_d + 1, dtype=torch.int32, device=dev) if want_csr else None
+    col = torch.empty(max(1, Nq * Nd * max_lq), dtype=torch.int32, device=dev) if want_csr else None
+    ws, nbytes = _workspace(workspace_size(_native.OP_BWD_VARLEN, Nq, max_lq, Nd, total_d, dim), dev, workspace)
+    rc = _native.lib().maxsim_bwd_varlen(_ptr(Q), _ptr(cu_q), max_lq, _ptr(D), _ptr(cu_d), total_d, max_ld,
+                                         _DT[Q.dtype], Nq, Nd, dim, _ptr(qm), _ptr(am), _ptr(g), _ptr(dQ), _ptr(dD),
+                                         _ptr(row_ptr), _ptr(col), _ptr(ws), nbytes, _stream(dev))
+    _native.check(rc, "maxsim_bwd_varlen")
+    return dQ, dD, row_ptr, col
+
+
 def maxsim_fwd_int8(Q: torch.Tensor, q_scale: torch.Tensor, D: torch.Tensor, d_scale: torch.Tensor, q_mask=None,
                     d_mask=None, *, want_argmax: bool = False, want_win_dot: bool = False,
                     scores: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):

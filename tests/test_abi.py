@@ -93,7 +93,7 @@ def test_workspace_sizes(lib):
     assert ws(1, 32, 32, 1000, 50000, 128) > 0                    # varlen always repacks the queries
     assert ws(2, 4, 8, 3, 10, 128) >= 4 * (3 + 4 + 31 + 96)      # counts, bases, row_ptr, col
     assert ws(4, 32, 32, 1000, 5000, 128) >= ws(1, 32, 32, 1000, 50000, 128) + 4 * (32 * 4 + 5000)  # + grouping
-    assert ws(9, 1, 1, 1, 1, 16) == ctypes.c_size_t(-1).value
+    assert ws(99, 1, 1, 1, 1, 16) == ctypes.c_size_t(-1).value
     assert ws(0, -1, 1, 1, 1, 16) == ctypes.c_size_t(-1).value
 
 
@@ -173,3 +173,24 @@ def test_streamed_host_validation(lib):
     assert f(FAKE, None, 0, 1, 32, 5, 1024, 128, 20000, None, FAKE, FAKE, need, None) == 1
     assert f(FAKE, FAKE, 0, 1, 32, 5, 1024, 24, 20000, None, FAKE, FAKE, need, None) == 2  # dim
     assert f(FAKE, FAKE, 0, 1, 32, 50000, 1024, 128, 20000, None, FAKE, FAKE, 1024, None) == 5
+
+
+def test_bwd_varlen_host_validation(lib):
+    b = lib.maxsim_bwd_varlen
+    need = lib.maxsim_workspace_size(9, 4, 32, 10, 1000, 128)
+    assert need >= 4 * (1000 + 1) + 4 * 4 * 10 * 32
+    # Q, cu_q, max_lq, D, cu_d, total_d, max_ld, dtype, Nq, Nd, dim, q_mask, argmax, g, dQ, dD, rp, col, ws, bytes, st
+    args = [FAKE, None, 32, FAKE, FAKE, 1000, 300, 0, 4, 10, 128, None, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, need,
+            None]
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return b(*a)
+    assert call(a4=None) == 1            # no document offsets
+    assert call(a12=None) == 1           # no argmax
+    assert call(a7=3) == 1               # dtype
+    assert call(a10=24) == 2             # dim
+    assert call(a6=60000) == 2           # a document histogram beyond shared memory
+    assert call(a19=64) == 5             # workspace
+    assert call(a15=FAKE + 4) == 1       # misaligned gradient
