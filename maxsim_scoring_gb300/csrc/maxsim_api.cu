@@ -13,6 +13,7 @@
 #include "maxsim.h"
 #include "bwd_kernels.cuh"
 #include "chamfer_kernels.cuh"
+#include "chamfer_tc.cuh"
 #include "topk_kernels.cuh"
 #include "fwd_kernel.cuh"
 
@@ -623,6 +624,61 @@ ChamferFwdPlan plan_chamfer_fwd(int64_t B, int64_t N, int64_t M, int64_t dim) {
     return p;
 }
 
+// Tensor-core nearest-point search (dim <= kTcMaxDim): augmented operand rows
+// of both sets, partial results per target span, loss partials.
+struct ChamferTcPlan {
+    int64_t s_rows[2] = {0, 0}, t_rows[2] = {0, 0};  // per set of P (0) and Q (1)
+    int64_t n_sb[2] = {0, 0}, n_span[2] = {0, 0}, n_mblk[2] = {0, 0};  // per direction
+    int64_t items = 0;
+    size_t off_s[2] = {0, 0}, off_t[2] = {0, 0}, off_best[2] = {0, 0}, off_idx[2] = {0, 0}, off_loss[2] = {0, 0};
+    size_t ws_bytes = 0;
+};
+
+ChamferTcPlan plan_chamfer_tc(int64_t B, int64_t N, int64_t M) {
+    ChamferTcPlan p;
+    const int64_t n[2] = {N, M};
+    size_t off = 0;
+    for (int c = 0; c < 2; ++c) {  // operand rows of P and of Q
+        p.s_rows[c] = (n[c] + kTcSources - 1) / kTcSources * kTcSources;
+        p.t_rows[c] = (n[c] + kTcN - 1) / kTcN * kTcN;
+        p.off_s[c] = off;
+        off = round_up(off + static_cast<size_t>(B * p.s_rows[c]) * kTcRowBytes, 1024);
+        p.off_t[c] = off;
+        off = round_up(off + static_cast<size_t>(B * p.t_rows[c]) * kTcRowBytes, 1024);
+    }
+    const int64_t nx[2] = {N, M}, ny[2] = {M, N};
+    for (int d = 0; d < 2; ++d) {
+        p.n_sb[d] = (nx[d] + kTcSources - 1) / kTcSources;
+        p.n_span[d] = (ny[d] + kTcSpan - 1) / kTcSpan;
+        p.n_mblk[d] = (nx[d] + 255) / 256;
+        const size_t n_part = static_cast<size_t>(p.n_span[d]) * static_cast<size_t>(B * nx[d]);
+        p.off_best[d] = off;
+        off = round_up(off + n_part * 4, 256);
+        p.off_idx[d] = off;
+        off = round_up(off + n_part * 4, 256);
+        p.off_loss[d] = off;
+        off = round_up(off + static_cast<size_t>(B * p.n_mblk[d]) * 8, 256);
+    }
+    p.items = (N > 0 && M > 0) ? B * (p.n_sb[0] * p.n_span[0] + p.n_sb[1] * p.n_span[1]) : 0;
+    p.ws_bytes = off;
+    return p;
+}
+
+constexpr size_t kTcSmemBytes = static_cast<size_t>(kTcMT) * kTcATile + static_cast<size_t>(kTcStages) * kTcBTile +
+                                2ull * 4 * kTcSources * 4 + sizeof(TcSmemCtl) + 1024;
+
+// [rows, 16] fp32 rows with the 64-byte swizzle, box_rows rows per load.
+bool encode_rows_sw64(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kTcK), rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kTcRowBytes)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct ChamferBwdPlan {
     int64_t K = 0, nblocks = 0, hist_n = 0;
     int passes = 0;
@@ -657,6 +713,68 @@ maxsim_status check_chamfer_shape(int64_t B, int64_t N, int64_t M, int64_t dim) 
     if (dim > kChMaxDim) return MAXSIM_ERR_UNSUPPORTED;
     if (B * (N + M) >= kI32Max || B * (N + M) * dim >= (int64_t(1) << 40)) return MAXSIM_ERR_UNSUPPORTED;
     return MAXSIM_OK;
+}
+
+maxsim_status chamfer_fwd_tc(DeviceInfo* dev, const ChamferTcPlan& p, const float* P, const float* Q, int64_t B,
+                             int64_t N, int64_t M, int64_t dim, float* dist_p, int32_t* idx_p, float* dist_q,
+                             int32_t* idx_q, float* loss, uint8_t* ws, cudaStream_t st) {
+    ChamferFwdArgs a{};
+    a.X[0] = P; a.Y[0] = Q; a.X[1] = Q; a.Y[1] = P;
+    a.nx[0] = N; a.ny[0] = M; a.nx[1] = M; a.ny[1] = N;
+    a.B = B;
+    a.dim = static_cast<int32_t>(dim);
+    a.dist[0] = dist_p; a.idx[0] = idx_p; a.dist[1] = dist_q; a.idx[1] = idx_q;
+    a.loss = loss;
+    a.status = dev->status;
+    ChamferTcArgs t{};
+    t.B = B;
+    t.items = p.items;
+    t.status = dev->status;
+    t.timeout_ns = kTimeoutNs;
+    const int64_t n[2] = {N, M};
+    for (int d = 0; d < 2; ++d) {
+        t.nx[d] = a.nx[d];
+        t.ny[d] = a.ny[d];
+        t.n_sb[d] = p.n_sb[d];
+        t.n_span[d] = p.n_span[d];
+        t.part_best[d] = reinterpret_cast<float*>(ws + p.off_best[d]);
+        t.part_idx[d] = reinterpret_cast<int32_t*>(ws + p.off_idx[d]);
+        a.n_mblk[d] = p.n_mblk[d];
+        a.loss_part[d] = reinterpret_cast<double*>(ws + p.off_loss[d]);
+    }
+    // direction 0: sources P, targets Q; direction 1: sources Q, targets P
+    t.s_rows[0] = p.s_rows[0]; t.t_rows[0] = p.t_rows[1];
+    t.s_rows[1] = p.s_rows[1]; t.t_rows[1] = p.t_rows[0];
+    if (p.items > 0) {
+        const float* pts[2] = {P, Q};
+        for (int c = 0; c < 2; ++c) {
+            const int64_t rows = B * std::max(p.s_rows[c], p.t_rows[c]);
+            chamfer_tc_prep_kernel<<<grid_for(rows, 256, dev->num_sms), 256, 0, st>>>(
+                pts[c], B, n[c], static_cast<int32_t>(dim), p.s_rows[c], p.t_rows[c],
+                reinterpret_cast<float*>(ws + p.off_s[c]), reinterpret_cast<float*>(ws + p.off_t[c]));
+        }
+        CUtensorMap ms0, mt0, ms1, mt1;
+        if (!encode_rows_sw64(&ms0, ws + p.off_s[0], static_cast<uint64_t>(B * p.s_rows[0]), kTcM) ||
+            !encode_rows_sw64(&mt0, ws + p.off_t[1], static_cast<uint64_t>(B * p.t_rows[1]), kTcN) ||
+            !encode_rows_sw64(&ms1, ws + p.off_s[1], static_cast<uint64_t>(B * p.s_rows[1]), kTcM) ||
+            !encode_rows_sw64(&mt1, ws + p.off_t[0], static_cast<uint64_t>(B * p.t_rows[0]), kTcN))
+            return MAXSIM_ERR_CUDA;
+        if (!dev->attrs_set[14]) {
+            if (cudaFuncSetAttribute(chamfer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kTcSmemBytes)) != cudaSuccess)
+                return MAXSIM_ERR_CUDA;
+            dev->attrs_set[14] = true;
+        }
+        const int64_t grid = std::min<int64_t>(p.items, dev->num_sms);
+        chamfer_tc_kernel<<<static_cast<unsigned>(grid), kTcThreads, kTcSmemBytes, st>>>(ms0, mt0, ms1, mt1, t);
+        if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+    }
+    const int64_t mblk = std::max(p.n_mblk[0], p.n_mblk[1]);
+    if (mblk > 0)
+        chamfer_tc_merge_kernel<<<dim3(static_cast<unsigned>(mblk), static_cast<unsigned>(B), 2), 256, 0, st>>>(
+            P, Q, static_cast<int32_t>(dim), t, a);
+    chamfer_loss_kernel<<<static_cast<unsigned>(B), kChLossThreads, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
 }
 
 template <int kD>
@@ -952,7 +1070,7 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
     }
     case MAXSIM_OP_CHAMFER_FWD:  // (B, N, M, unused, dim)
         if (check_chamfer_shape(Nq, Lq, Nd, dim) == MAXSIM_ERR_INVALID_ARG) return static_cast<size_t>(-1);
-        return plan_chamfer_fwd(Nq, Lq, Nd, dim).ws_bytes;
+        return dim <= kTcMaxDim ? plan_chamfer_tc(Nq, Lq, Nd).ws_bytes : plan_chamfer_fwd(Nq, Lq, Nd, dim).ws_bytes;
     case MAXSIM_OP_CHAMFER_BWD:
         if (check_chamfer_shape(Nq, Lq, Nd, dim) == MAXSIM_ERR_INVALID_ARG) return static_cast<size_t>(-1);
         return plan_chamfer_bwd(Nq, Lq, Nd).ws_bytes;
@@ -1237,6 +1355,14 @@ maxsim_status maxsim_chamfer_fwd(const float* P, const float* Q, int64_t B, int6
         return MAXSIM_ERR_INVALID_ARG;
     if (M > 0 && (!Q || !aligned(Q, 4) || !dist_q || !idx_q || !aligned(dist_q, 4) || !aligned(idx_q, 4)))
         return MAXSIM_ERR_INVALID_ARG;
+    if (dim <= kTcMaxDim) {
+        const ChamferTcPlan tp = plan_chamfer_tc(B, N, M);
+        if (workspace_bytes < tp.ws_bytes || !workspace || !aligned(workspace, 256)) return MAXSIM_ERR_WORKSPACE;
+        DeviceInfo* dev = nullptr;
+        if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
+        return chamfer_fwd_tc(dev, tp, P, Q, B, N, M, dim, dist_p, idx_p, dist_q, idx_q, loss,
+                              static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
+    }
     const ChamferFwdPlan p = plan_chamfer_fwd(B, N, M, dim);
     if (workspace_bytes < p.ws_bytes || !workspace || !aligned(workspace, 256)) return MAXSIM_ERR_WORKSPACE;
     DeviceInfo* dev = nullptr;
