@@ -509,6 +509,11 @@ class Case:
                 self.bound = "hbm" if name == "tiny_rerank" else "tensor"
                 self.launches = 1
         self.ws = t.empty(max(1, ws), dtype=t.uint8, device=device)
+        if name == "colbert_varlen":
+            self.h_cu = self.h_in["cu_seqlens_d"]  # page-locked host offsets of the corpus
+            self.e2e_ws = t.empty(ops.workspace_size(_native.OP_FWD_VARLEN_STREAMED, Nq, w["Lq"], min(5000, Nd),
+                                                     1 << 20, dim), dtype=t.uint8, device=device)
+            self.e2e_api = "maxsim_fwd_varlen_streamed (host corpus, 5,000-document blocks)"
         in_bytes = sum(v.numel() * v.element_size() for v in self.d_in.values())
         self.flush_buf = (t.empty(256 * 1024 * 1024 // 4, dtype=t.float32, device=device)
                           if in_bytes < 2 * L2_BYTES else None)
@@ -533,6 +538,15 @@ class Case:
         self.call(self.d_in)
 
     def e2e_step(self):
+        if self.name == "colbert_varlen":
+            # a corpus in host memory goes through the out-of-core call: its
+            # document blocks are copied while the previous block is scored
+            self.e2e_in["Q"].copy_(self.h_in["Q"], non_blocking=True)
+            self.ops.maxsim_fwd_varlen_streamed(self.e2e_in["Q"], None, self.w["Lq"], self.h_in["D"],
+                                                self.h_cu, block_docs=5000, block_tokens=1 << 20,
+                                                scores=self.scores, workspace=self.e2e_ws)
+            self.h_scores.copy_(self.scores, non_blocking=True)
+            return
         for k, v in self.h_in.items():
             self.e2e_in[k].copy_(v, non_blocking=True)
         self.call(self.e2e_in)
@@ -879,17 +893,21 @@ def run_ours(args, rank, world, local_rank):
 
     # end to end through the same public call: H2D of the step's inputs, the
     # call, D2H of the result, all on the stream and inside the events
-    e2e_steps = max(1, min(args.steps, 5))
+    # per-step events; the host-to-device link of these machines is shared and
+    # has slow episodes, so the line reports the median step (the mean too)
+    e2e_steps = max(1, min(args.steps, 7))
     barrier()
     torch.cuda.synchronize(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    for k in range(e2e_steps):
+        ev[k][0].record(stream)
         case.e2e_step()
-    e1.record(stream)
+        ev[k][1].record(stream)
     torch.cuda.synchronize(device)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_each = [a.elapsed_time(b) for a, b in ev]
+    e2e_ms = statistics.median(e2e_each)
+    e2e_mean_ms = sum(e2e_each) / len(e2e_each)
 
     # max over ranks; units summed over ranks
     t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=device)
@@ -954,7 +972,9 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": case.dtype, "data": "synthetic", "config": describe(w, spec), "clocks": clk,
         "roofline": roofline,
         "e2e": {"value": all_units / (e2e_ms / 1e3), "unit": unit_name, "h2d_bytes_per_step": case.h2d_bytes(),
-                "d2h_bytes_per_step": case.d2h_bytes()},
+                "d2h_bytes_per_step": case.d2h_bytes(), "steps": e2e_steps, "statistic": "median step",
+                "value_mean": all_units / (e2e_mean_ms / 1e3) if world == 1 else None,
+                "api": getattr(case, "e2e_api", "the same call, inputs copied from page-locked host memory first")},
         "gpu_launches": case.launches * args.steps,
         "step_ms_min_median_max": [min(per_step_ms), statistics.median(per_step_ms), max(per_step_ms)],
     }

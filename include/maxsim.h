@@ -59,7 +59,8 @@ typedef enum { MAXSIM_F16 = 0, MAXSIM_BF16 = 1 } maxsim_dtype;
 /* Operation codes for maxsim_workspace_size(). */
 enum { MAXSIM_OP_FWD = 0, MAXSIM_OP_FWD_VARLEN = 1, MAXSIM_OP_BWD = 2, MAXSIM_OP_FWD_INT8 = 3,
        MAXSIM_OP_SCORE_PAIRS = 4, MAXSIM_OP_CHAMFER_FWD = 5, MAXSIM_OP_CHAMFER_BWD = 6,
-       MAXSIM_OP_TWO_STAGE = 7, MAXSIM_OP_FWD_STREAMED = 8, MAXSIM_OP_BWD_VARLEN = 9 };
+       MAXSIM_OP_TWO_STAGE = 7, MAXSIM_OP_FWD_STREAMED = 8, MAXSIM_OP_BWD_VARLEN = 9,
+       MAXSIM_OP_FWD_VARLEN_STREAMED = 10 };
 
 /*
  * Dense forward.
@@ -313,6 +314,27 @@ maxsim_status maxsim_bwd_varlen(const void *Q, const int32_t *cu_seqlens_q, int6
                                 int32_t *csr_col, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Out-of-core packed forward ("Flash-MaxSim" Sec. 5.3 applied to the packed
+ * layout of Sec. 4.3.2): maxsim_fwd_varlen over a corpus held in host memory.
+ *   Q, cu_seqlens_q, max_lq, q_mask   DEVICE, as for maxsim_fwd_varlen
+ *   D_host             packed [total_d, dim] rows, HOST memory (page-locked for overlap)
+ *   cu_seqlens_d_host  [Nd + 1] i32, HOST memory; read by this call on the host
+ *   block_docs, block_tokens   a block is the longest run of whole documents within
+ *                      both limits; every document must fit block_tokens
+ *   scores             [Nq, Nd] f32, device (out): equal to maxsim_fwd_varlen's
+ * Block b + 1 is copied (rows and offsets, cudaMemcpyAsync on the library's
+ * copy stream) while block b is scored on `stream`; the call only enqueues,
+ * and the host buffers must stay valid until `stream` passes it. No d_mask
+ * and no argmax. Workspace: maxsim_workspace_size(MAXSIM_OP_FWD_VARLEN_STREAMED,
+ * Nq, max_lq, block_docs, block_tokens, dim), 256-byte aligned.
+ */
+maxsim_status maxsim_fwd_varlen_streamed(const void *Q, const int32_t *cu_seqlens_q, int64_t max_lq,
+                                         const void *D_host, const int32_t *cu_seqlens_d_host, int64_t total_d,
+                                         maxsim_dtype dtype, int64_t Nq, int64_t Nd, int64_t dim,
+                                         const uint8_t *q_mask, int64_t block_docs, int64_t block_tokens,
+                                         float *scores, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace an operation needs for a shape (0 if none).
  *   MAXSIM_OP_FWD / MAXSIM_OP_FWD_INT8: (Nq, Lq, Nd, Ld, dim)
  *   MAXSIM_OP_FWD_VARLEN:              (Nq, max_lq, Nd, total_d, dim); assumes
@@ -327,6 +349,8 @@ maxsim_status maxsim_bwd_varlen(const void *Q, const int32_t *cu_seqlens_q, int6
  *                                      of the corpus size
  *   MAXSIM_OP_BWD_VARLEN:              (Nq, max_lq, Nd, total_d, dim); assumes
  *                                      the CSR outputs are NULL (an upper bound)
+ *   MAXSIM_OP_FWD_VARLEN_STREAMED:     (Nq, max_lq, block_docs, block_tokens, dim);
+ *                                      independent of the corpus size
  * Returns (size_t)-1 for an invalid shape.
  */
 size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim);

@@ -27,6 +27,7 @@ STATUS = {
 
 OP_FWD, OP_FWD_VARLEN, OP_BWD, OP_FWD_INT8, OP_SCORE_PAIRS = 0, 1, 2, 3, 4
 OP_CHAMFER_FWD, OP_CHAMFER_BWD, OP_TWO_STAGE, OP_FWD_STREAMED, OP_BWD_VARLEN = 5, 6, 7, 8, 9
+OP_FWD_VARLEN_STREAMED = 10
 F16, BF16 = 0, 1
 
 # Every symbol the header declares, with its ctypes signature.
@@ -49,6 +50,8 @@ SIGNATURES = {
     "maxsim_bwd_varlen": (_I, [_VP, _VP, _I64, _VP, _VP, _I64, _I64, _I, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP,
                                _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_fwd_streamed": (_I, [_VP, _VP, _I, _I64, _I64, _I64, _I64, _I64, _I64, _VP, _VP, _VP, _SZ, _VP]),
+    "maxsim_fwd_varlen_streamed": (_I, [_VP, _VP, _I64, _VP, _VP, _I64, _I, _I64, _I64, _I64, _VP, _I64, _I64, _VP,
+                                        _VP, _SZ, _VP]),
     "maxsim_two_stage_topk": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _VP,
                                    _VP, _VP, _VP, _VP, _SZ, _VP]),
     "maxsim_workspace_size": (_SZ, [_I, _I64, _I64, _I64, _I64, _I64]),

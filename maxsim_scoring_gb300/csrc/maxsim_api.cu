@@ -1060,6 +1060,17 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
         return bwd_ws_bytes(Nq, Lq, Nd, Nd * Ld, dim, false, false);
     case MAXSIM_OP_BWD_VARLEN:  // (Nq, max_lq, Nd, total_d, dim)
         return bwd_ws_bytes(Nq, Lq, Nd, Ld, dim, false, false);
+    case MAXSIM_OP_FWD_VARLEN_STREAMED: {  // (Nq, max_lq, block_docs, block_tokens, dim)
+        const FwdPlan f = plan_fwd(Nq, Lq, Nd, dim, true, false);
+        if (!f.ok) return static_cast<size_t>(-1);
+        size_t off = 0;
+        for (int i = 0; i < 2; ++i) {
+            off = round_up(off + static_cast<size_t>(Ld * dim * 2), 256);
+            off = round_up(off + static_cast<size_t>(Nd + 1) * 4, 256);
+        }
+        off = round_up(off + static_cast<size_t>(Nq * Nd) * 4, 256);
+        return round_up(off + f.ws_bytes, 256);
+    }
     case MAXSIM_OP_FWD_STREAMED: {  // (Nq, Lq, block_docs, Ld, dim)
         const StreamedPlan p = plan_streamed(Nq, Lq, Nd, Ld, dim, 2);
         return p.ok ? p.bytes : static_cast<size_t>(-1);
@@ -1654,6 +1665,129 @@ extern "C" maxsim_status maxsim_fwd_streamed(const void* Q, const void* D_host, 
                                         cudaMemcpyDeviceToDevice, st) != cudaSuccess)
             return MAXSIM_ERR_CUDA;
         if (cudaEventRecord(res->done[s], st) != cudaSuccess) return MAXSIM_ERR_CUDA;
+    }
+    return MAXSIM_OK;
+}
+
+// ---------------------------------------------------------------- out-of-core packed forward
+//
+// The packed corpus stays in host memory with its offsets; blocks of whole
+// documents (at most block_docs documents and block_tokens rows) are copied
+// into one of two device buffers on the copy stream while the previous block
+// is scored by maxsim_fwd_varlen on the caller's stream. A block's offsets are
+// copied as they are and rebased on the device.
+
+namespace maxsim {
+namespace {
+
+__global__ void rebase_offsets_kernel(int32_t* __restrict__ cu, int64_t n, int32_t base) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i <= n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        cu[i] -= base;
+}
+
+struct VarlenStreamedPlan {
+    size_t off_buf[2] = {0, 0}, off_cu[2] = {0, 0}, off_scores = 0, off_fwd = 0, fwd_bytes = 0, bytes = 0;
+    bool ok = false;
+};
+
+VarlenStreamedPlan plan_varlen_streamed(int64_t Nq, int64_t max_lq, int64_t block_docs, int64_t block_tokens,
+                                        int64_t dim) {
+    VarlenStreamedPlan p;
+    const FwdPlan f = plan_fwd(Nq, max_lq, block_docs, dim, true, false);
+    if (!f.ok) return p;
+    size_t off = 0;
+    for (int i = 0; i < 2; ++i) {
+        p.off_buf[i] = off;
+        off = round_up(off + static_cast<size_t>(block_tokens * dim * 2), 256);
+        p.off_cu[i] = off;
+        off = round_up(off + static_cast<size_t>(block_docs + 1) * 4, 256);
+    }
+    p.off_scores = off;
+    off = round_up(off + static_cast<size_t>(Nq * block_docs) * 4, 256);
+    p.off_fwd = off;
+    p.fwd_bytes = f.ws_bytes;
+    p.bytes = round_up(off + f.ws_bytes, 256);
+    p.ok = true;
+    return p;
+}
+
+}  // namespace
+}  // namespace maxsim
+
+extern "C" maxsim_status maxsim_fwd_varlen_streamed(const void* Q, const int32_t* cu_seqlens_q, int64_t max_lq,
+                                                    const void* D_host, const int32_t* cu_seqlens_d_host,
+                                                    int64_t total_d, maxsim_dtype dtype, int64_t Nq, int64_t Nd,
+                                                    int64_t dim, const uint8_t* q_mask, int64_t block_docs,
+                                                    int64_t block_tokens, float* scores, void* workspace,
+                                                    size_t workspace_bytes, void* stream) {
+    if (dtype != MAXSIM_F16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_INVALID_ARG;
+    if (Nq < 0 || Nd < 0 || max_lq < 0 || total_d < 0 || block_docs <= 0 || block_tokens <= 0)
+        return MAXSIM_ERR_INVALID_ARG;
+    maxsim_status rc = check_dim(dim, 16);
+    if (rc != MAXSIM_OK) return rc;
+    if (Nq * Nd == 0) return MAXSIM_OK;
+    if (!scores || !aligned(scores, 4) || !cu_seqlens_d_host || (max_lq > 0 && (!Q || !aligned16(Q))) ||
+        (total_d > 0 && !D_host))
+        return MAXSIM_ERR_INVALID_ARG;
+    if (total_d > kI32Max || Nq * pad_lq(max_lq) > kI32Max || Nq * Nd > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
+    // the host offsets are read here: they must describe total_d rows, every document fitting a block
+    if (cu_seqlens_d_host[0] != 0 || cu_seqlens_d_host[Nd] != total_d) return MAXSIM_ERR_INVALID_ARG;
+    for (int64_t j = 0; j < Nd; ++j) {
+        const int64_t len = static_cast<int64_t>(cu_seqlens_d_host[j + 1]) - cu_seqlens_d_host[j];
+        if (len < 0) return MAXSIM_ERR_INVALID_ARG;
+        if (len > block_tokens) return MAXSIM_ERR_UNSUPPORTED;
+    }
+    const int64_t bdocs = std::min(block_docs, Nd);
+    const VarlenStreamedPlan p = plan_varlen_streamed(Nq, max_lq, bdocs, block_tokens, dim);
+    if (!p.ok) return MAXSIM_ERR_UNSUPPORTED;
+    if (workspace_bytes < p.bytes || !workspace || !aligned(workspace, 256)) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev)) != MAXSIM_OK) return rc;
+    std::lock_guard<std::mutex> lock(g_stream_mu);
+    StreamRes* res = nullptr;
+    if ((rc = stream_res(&res)) != MAXSIM_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t row_bytes = static_cast<size_t>(dim * 2);
+    const uint8_t* host = static_cast<const uint8_t*>(D_host);
+    if (cudaEventRecord(res->start, st) != cudaSuccess || cudaStreamWaitEvent(res->copy, res->start, 0) != cudaSuccess)
+        return MAXSIM_ERR_CUDA;
+    int64_t j0 = 0;
+    for (int64_t b = 0; j0 < Nd; ++b) {
+        // the next block: whole documents within both limits
+        int64_t j1 = j0;
+        while (j1 < Nd && j1 - j0 < bdocs &&
+               static_cast<int64_t>(cu_seqlens_d_host[j1 + 1]) - cu_seqlens_d_host[j0] <= block_tokens)
+            ++j1;
+        const int64_t nb = j1 - j0;
+        const int32_t t0 = cu_seqlens_d_host[j0];
+        const int64_t ntok = static_cast<int64_t>(cu_seqlens_d_host[j1]) - t0;
+        const int s = static_cast<int>(b & 1);
+        void* buf = ws + p.off_buf[s];
+        int32_t* cu = reinterpret_cast<int32_t*>(ws + p.off_cu[s]);
+        if (b >= 2 && cudaStreamWaitEvent(res->copy, res->done[s], 0) != cudaSuccess) return MAXSIM_ERR_CUDA;
+        if (ntok > 0 && cudaMemcpyAsync(buf, host + static_cast<size_t>(t0) * row_bytes,
+                                        static_cast<size_t>(ntok) * row_bytes, cudaMemcpyHostToDevice,
+                                        res->copy) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        if (cudaMemcpyAsync(cu, cu_seqlens_d_host + j0, static_cast<size_t>(nb + 1) * 4, cudaMemcpyHostToDevice,
+                            res->copy) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        if (cudaEventRecord(res->copied[s], res->copy) != cudaSuccess ||
+            cudaStreamWaitEvent(st, res->copied[s], 0) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        rebase_offsets_kernel<<<grid_for(nb + 1, 256, dev->num_sms), 256, 0, st>>>(cu, nb, t0);
+        float* out = Nq == 1 ? scores + j0 : reinterpret_cast<float*>(ws + p.off_scores);
+        rc = maxsim_fwd_varlen(Q, cu_seqlens_q, max_lq, ntok > 0 ? buf : ws + p.off_buf[s], cu, ntok, dtype, Nq, nb,
+                               dim, q_mask, nullptr, out, nullptr, ws + p.off_fwd, p.fwd_bytes, stream);
+        if (rc != MAXSIM_OK) return rc;
+        if (Nq > 1 && cudaMemcpy2DAsync(scores + j0, static_cast<size_t>(Nd) * 4, out, static_cast<size_t>(nb) * 4,
+                                        static_cast<size_t>(nb) * 4, static_cast<size_t>(Nq),
+                                        cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        if (cudaEventRecord(res->done[s], st) != cudaSuccess) return MAXSIM_ERR_CUDA;
+        j0 = j1;
     }
     return MAXSIM_OK;
 }

@@ -374,6 +374,41 @@ def maxsim_fwd_streamed(Q: torch.Tensor, D_host: torch.Tensor, q_mask=None, *, b
     return scores
 
 
+def maxsim_fwd_varlen_streamed(Q: torch.Tensor, cu_seqlens_q: Optional[torch.Tensor], max_lq: int,
+                               D_host: torch.Tensor, cu_seqlens_d_host: torch.Tensor, q_mask=None, *,
+                               block_docs: int = 20_000, block_tokens: int = 1 << 22,
+                               scores: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Scores [Nq, Nd] of device queries against a packed corpus in host
+    memory: D_host [total_d, d] rows and cu_seqlens_d_host [Nd+1] (int32, host),
+    streamed in blocks of whole documents. Keep the host tensors alive and
+    unchanged until the current stream has passed this call."""
+    if Q.dtype not in _DT or D_host.dtype != Q.dtype:
+        raise TypeError("Q and D_host must both be float16 or both bfloat16")
+    if D_host.is_cuda or cu_seqlens_d_host.is_cuda or not D_host.is_contiguous():
+        raise ValueError("D_host and cu_seqlens_d_host must be contiguous host tensors")
+    if cu_seqlens_d_host.dtype != torch.int32 or not cu_seqlens_d_host.is_contiguous():
+        raise TypeError("cu_seqlens_d_host must be a contiguous int32 host tensor")
+    dev = Q.device
+    Q = _contig(Q, "Q")
+    cu_q = _contig(cu_seqlens_q, "cu_seqlens_q", torch.int32, dev)
+    dim = Q.shape[-1]
+    Nq = (cu_q.numel() - 1) if cu_q is not None else Q.shape[0]
+    Nd = cu_seqlens_d_host.numel() - 1
+    total_d = D_host.shape[0]
+    qm = _mask(q_mask, "q_mask", dev)
+    if scores is None:
+        scores = torch.empty((Nq, Nd), dtype=torch.float32, device=dev)
+    bd = min(block_docs, max(Nd, 1))
+    ws, nbytes = _workspace(workspace_size(_native.OP_FWD_VARLEN_STREAMED, Nq, max_lq, bd, block_tokens, dim), dev,
+                            workspace)
+    rc = _native.lib().maxsim_fwd_varlen_streamed(_ptr(Q), _ptr(cu_q), max_lq, D_host.data_ptr(),
+                                                  cu_seqlens_d_host.data_ptr(), total_d, _DT[Q.dtype], Nq, Nd, dim,
+                                                  _ptr(qm), block_docs, block_tokens, _ptr(scores), _ptr(ws), nbytes,
+                                                  _stream(dev))
+    _native.check(rc, "maxsim_fwd_varlen_streamed")
+    return scores
+
+
 def device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device status word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)

@@ -59,3 +59,40 @@ def test_streamed_calls_back_to_back_reuse_the_buffers():
     wb, _ = ops.maxsim_fwd(Qd, dev_bits(D2, "bf16"))
     assert ops.device_status() == 0
     assert torch.equal(a, wa) and torch.equal(b, wb)
+
+
+@pytest.mark.parametrize("Nq,block_docs,block_tokens", [(4, 50, 4000), (1, 1000, 300), (3, 7, 100000), (2, 10000, 1 << 22)])
+def test_varlen_streamed_equals_the_device_forward(Nq, block_docs, block_tokens):
+    rng = np.random.default_rng(107 + Nq)
+    dtype, dim, Lq = "f16", 128, 32
+    lens = rng.integers(0, 301, size=600)
+    lens[::37] = 0
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    D = datagen.gaussian_rows(107, 2, int(cu[-1]), dim, dtype)
+    Q = datagen.gaussian_rows(107, 1, Nq * Lq, dim, dtype).reshape(Nq, Lq, dim)
+    Qd = dev_bits(Q, dtype)
+    Dh = host_bits(D, dtype)
+    cu_h = torch.from_numpy(cu)
+    got = ops.maxsim_fwd_varlen_streamed(Qd, None, Lq, Dh, cu_h, block_docs=block_docs, block_tokens=block_tokens)
+    want, _ = ops.maxsim_fwd_varlen(Qd, None, Lq, dev_bits(D, dtype), torch.from_numpy(cu).cuda())
+    assert ops.device_status() == 0
+    assert torch.equal(got, want)
+
+
+def test_varlen_streamed_packed_queries_and_document_too_long():
+    rng = np.random.default_rng(109)
+    dtype, dim = "bf16", 64
+    qlens = np.array([5, 32, 17])
+    cu_q = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    lens = rng.integers(1, 200, size=90)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    Q = datagen.gaussian_rows(109, 1, int(cu_q[-1]), dim, dtype)
+    D = datagen.gaussian_rows(109, 2, int(cu[-1]), dim, dtype)
+    Qd, cq = dev_bits(Q, dtype), torch.from_numpy(cu_q).cuda()
+    Dh, cu_h = host_bits(D, dtype), torch.from_numpy(cu)
+    got = ops.maxsim_fwd_varlen_streamed(Qd, cq, 32, Dh, cu_h, block_docs=16, block_tokens=1000)
+    want, _ = ops.maxsim_fwd_varlen(Qd, cq, 32, dev_bits(D, dtype), torch.from_numpy(cu).cuda())
+    assert ops.device_status() == 0
+    assert torch.equal(got, want)
+    with pytest.raises(Exception):  # a document longer than a block
+        ops.maxsim_fwd_varlen_streamed(Qd, cq, 32, Dh, cu_h, block_docs=16, block_tokens=int(lens.max()) - 1)
