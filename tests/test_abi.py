@@ -196,3 +196,20 @@ def test_bwd_varlen_host_validation(lib):
     assert call(a6=60000) == 2           # a document histogram beyond shared memory
     assert call(a19=64) == 5             # workspace
     assert call(a15=FAKE + 4) == 1       # misaligned gradient
+
+
+def test_varlen_streamed_host_validation(lib):
+    f = lib.maxsim_fwd_varlen_streamed
+    cu = (ctypes.c_int32 * 4)(0, 100, 100, 350)            # host offsets: 3 documents, 350 rows
+    bad = (ctypes.c_int32 * 4)(0, 100, 90, 350)            # decreasing
+    need = lib.maxsim_workspace_size(10, 2, 32, 3, 1000, 128)
+    # Q, cu_q, max_lq, D_host, cu_host, total_d, dtype, Nq, Nd, dim, q_mask, block_docs, block_tokens, scores, ws, n, st
+    p_cu = ctypes.cast(cu, ctypes.c_void_p).value
+    p_bad = ctypes.cast(bad, ctypes.c_void_p).value
+    assert f(FAKE, None, 32, FAKE, p_cu, 350, 0, 2, 3, 128, None, 3, 1000, FAKE, FAKE, need, None) != 1
+    assert f(FAKE, None, 32, FAKE, p_bad, 350, 0, 2, 3, 128, None, 3, 1000, FAKE, FAKE, need, None) == 1
+    assert f(FAKE, None, 32, FAKE, p_cu, 349, 0, 2, 3, 128, None, 3, 1000, FAKE, FAKE, need, None) == 1
+    assert f(FAKE, None, 32, FAKE, p_cu, 350, 0, 2, 3, 128, None, 3, 200, FAKE, FAKE, need, None) == 2  # 250 > 200
+    assert f(FAKE, None, 32, FAKE, p_cu, 350, 0, 2, 3, 128, None, 0, 1000, FAKE, FAKE, need, None) == 1
+    assert f(FAKE, None, 32, FAKE, p_cu, 350, 0, 2, 3, 128, None, 3, 1000, FAKE, FAKE, 64, None) == 5
+    assert f(FAKE, None, 32, FAKE, None, 350, 0, 2, 3, 128, None, 3, 1000, FAKE, FAKE, need, None) == 1
