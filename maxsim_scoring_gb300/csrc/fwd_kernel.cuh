@@ -726,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int32_t ka = 0; ka < a.k_atoms; ++ka) {
                                 uint4* rowp = reinterpret_cast<uint4*>(dst + ka * kDAtom + r * 128);
 #pragma unroll
-                                for (int c = 0; c < 8; ++c) rowp[c] = nan4;
+                                for (int c = 0; c < 8; ++c) rowp[(c + lane) & 7] = nan4;  // rotated: 8 rows per phase hit 8 bank groups
                             }
                         }
                         fence_proxy_async_smem();

@@ -96,6 +96,29 @@ def test_varlen_two_row_blocks_every_tail_length_exact(dim):
         assert np.array_equal(a.cpu().numpy(), ref_a)
 
 
+@pytest.mark.parametrize("Lq", [32, 8, 1])
+def test_varlen_many_tiny_documents_exact(Lq):
+    # runs of 0..3-token documents (more than 32 document ends inside one
+    # 128-row tile), then long ones; scores with and without the argmax, and
+    # the argmax, exact on integer inputs (first index among equal maxima)
+    dtype, dim, Nq = "f16", 64, 5
+    rng = np.random.default_rng(21 + Lq)
+    lens = np.concatenate([rng.integers(0, 4, 300), [0, 0, 129, 1, 0, 255], rng.integers(1, 3, 70), [128, 2, 0]])
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    Q = datagen.float_to_bits(integer_rows(rng, Nq * Lq, dim), dtype).reshape(Nq, Lq, dim)
+    D = datagen.float_to_bits(integer_rows(rng, int(cu[-1]), dim), dtype)
+    dm = (rng.random(int(cu[-1])) > 0.3).astype(np.uint8)
+    for d_mask in (None, dm):
+        args = (dev_bits(Q, dtype), None, Lq, dev_bits(D, dtype), dev(cu.astype(np.int32)))
+        s, a = ops.maxsim_fwd_varlen(*args, d_mask=dev(d_mask), want_argmax=True)
+        s0, _ = ops.maxsim_fwd_varlen(*args, d_mask=dev(d_mask))
+        assert ops.device_status() == 0
+        ref_s, ref_a, _ = oracle.fwd_packed(Q.reshape(-1, dim), np.arange(Nq + 1) * Lq, D, cu, dtype, d_mask=d_mask)
+        assert np.array_equal(s.cpu().numpy().astype(np.float64), ref_s)
+        assert np.array_equal(s0.cpu().numpy().astype(np.float64), ref_s)
+        assert np.array_equal(a.cpu().numpy(), ref_a)
+
+
 def test_varlen_equals_dense_with_trailing_mask():
     # "same as the padded path": a trailing d_mask equals shorter packed documents
     dtype, Nq, Lq, Nd, Ld, dim = "bf16", 2, 32, 5, 200, 128
