@@ -899,30 +899,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < 4; ++c)
                             if (c < nchunks) fold(v[c], c);
                     }
-                    if (closes) {
+                }
+                if (!ok) break;
+                if (closes) {
+                    // The document ends in this tile. Its reductions come after both
+                    // M-tiles' loads (they are off the path that hands the accumulator
+                    // buffers back to the MMA warps), the M-tiles' shuffles interleaved.
+                    float val[kKPer];
+#pragma unroll
+                    for (int q = 0; q < kKPer; ++q) {
                         const bool has = m[q] > kNegInf;
                         if (kArg && in_rb[q] && row_s[q] < a.lq_out)
                             a.argmax[out_index(a, row_i[q], tw.oj) * a.lq_out + row_s[q]] =
                                 (real[q] && has) ? am[q] : -1;
-                        float val = (active[q] && has) ? m[q] * qsc[q] : 0.f;
-                        if (a.lq_pad >= 32) {
+                        val[q] = (active[q] && has) ? m[q] * qsc[q] : 0.f;
+                    }
+                    const int32_t width = min(a.lq_pad, 32);
+                    for (int o = width >> 1; o > 0; o >>= 1) {
 #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) val += __shfl_xor_sync(0xFFFFFFFFu, val, o);
-                            if (a.lq_pad == 32 && !chunked) {
-                                if (lane == 0 && in_rb[q]) a.scores[out_index(a, row_i[q], tw.oj)] = val;
-                            } else if (lane == 0) {
-                                ctl->wslot[k * 4 + e] = val;
-                            }
-                        } else {
-                            for (int o = a.lq_pad >> 1; o > 0; o >>= 1) val += __shfl_xor_sync(0xFFFFFFFFu, val, o);
-                            if (in_rb[q] && (lane & (a.lq_pad - 1)) == 0)
-                                a.scores[out_index(a, row_i[q], tw.oj)] = val;
+                        for (int q = 0; q < kKPer; ++q) val[q] += __shfl_xor_sync(0xFFFFFFFFu, val[q], o);
+                    }
+#pragma unroll
+                    for (int q = 0; q < kKPer; ++q) {
+                        const int k = g + kEpiGroups * q;
+                        if (k >= w.mt) break;
+                        if (a.lq_pad < 32 || (a.lq_pad == 32 && !chunked)) {
+                            if (in_rb[q] && (lane & (width - 1)) == 0) a.scores[out_index(a, row_i[q], tw.oj)] = val[q];
+                        } else if (lane == 0) {
+                            ctl->wslot[k * 4 + e] = val[q];
                         }
                         m[q] = kNegInf;
                         am[q] = -1;
                     }
                 }
-                if (!ok) break;
                 buf += w.mt;
                 if (closes && (a.lq_pad > 32 || (a.lq_pad == 32 && chunked))) {
                     if (!epi_sync(a, ctl, epi_phase)) { ok = false; break; }
