@@ -978,6 +978,9 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": case.launches * args.steps,
         "step_ms_min_median_max": [min(per_step_ms), statistics.median(per_step_ms), max(per_step_ms)],
     }
+    if unit_name == UNIT and "Nq" in w and case.name != "colbert_pairs":  # the pair list counts pairs already
+        # every document is scored against every query of the call: (query, document) pairs/s
+        line["pairs_per_s"] = value * w["Nq"]
     if world == 1 and not args.no_cpu_baseline and case.name not in ("contrastive_bwd", "colbert_varlen_bwd"):
         n = calibrated_sample(w, target_s=args.cpu_seconds)
         rate, dt, what = oracle_sample(w, n)
