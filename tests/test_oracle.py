@@ -221,6 +221,77 @@ def test_mask_invariants():
     assert np.array_equal(perm[pa[clear]], a0[clear])
 
 
+def _ragged_problem(seed, lq_lens, ld_lens, dim, dtype):
+    """Packed queries / documents of the given lengths with random masks (one
+    byte per packed row)."""
+    rng = np.random.default_rng(seed)
+    q_off = np.concatenate([[0], np.cumsum(lq_lens)]).astype(np.int64)
+    d_off = np.concatenate([[0], np.cumsum(ld_lens)]).astype(np.int64)
+    Q = datagen.gaussian_rows(300 + seed, 1, int(q_off[-1]), dim, dtype)
+    D = datagen.gaussian_rows(300 + seed, 2, int(d_off[-1]), dim, dtype)
+    qm = (rng.random(int(q_off[-1])) > 0.3).astype(np.uint8)
+    dm = (rng.random(int(d_off[-1])) > 0.3).astype(np.uint8)
+    return Q, q_off, D, d_off, qm, dm
+
+
+def test_packed_queries_equal_padded_dense():
+    # Packed queries of lengths L_i ("late-interaction-kernels" notes, "Varlen /
+    # packed path": cu_seqlens on both sides) score exactly like dense queries
+    # padded to max L_i whose padding rows carry q_mask = 0 (the notes' "Problem":
+    # q_mask drops a row from the sum). Rows past a query's end report -1.
+    dim, dtype = 8, "bf16"
+    lq_lens = np.array([3, 7, 1, 5])
+    ld_lens = np.array([4, 0, 9, 2, 6])
+    Q, q_off, D, d_off, qm, dm = _ragged_problem(41, lq_lens, ld_lens, dim, dtype)
+    Nq, Nd, max_lq = len(lq_lens), len(ld_lens), int(lq_lens.max())
+    for q_mask, d_mask in ((None, None), (qm, None), (None, dm), (qm, dm)):
+        s, a, g = oracle.fwd_packed(Q, q_off, D, d_off, dtype, q_mask=q_mask, d_mask=d_mask)
+        assert a.shape == (Nq * Nd, max_lq)
+        # dense padded twin: padding rows hold unrelated values and q_mask = 0
+        Qd = datagen.gaussian_rows(77, 1, Nq * max_lq, dim, dtype).reshape(Nq, max_lq, dim)
+        qmd = np.zeros((Nq, max_lq), np.uint8)
+        for i in range(Nq):
+            L = lq_lens[i]
+            Qd[i, :L] = Q[q_off[i]:q_off[i + 1]]
+            qmd[i, :L] = 1 if q_mask is None else q_mask[q_off[i]:q_off[i + 1]]
+        ds_, da, _ = oracle.fwd_packed(Qd.reshape(-1, dim), np.arange(Nq + 1) * max_lq, D, d_off, dtype,
+                                       q_mask=qmd.reshape(-1), d_mask=d_mask)
+        assert np.array_equal(s, ds_)
+        for i in range(Nq):
+            L = lq_lens[i]
+            rows = slice(i * Nd, (i + 1) * Nd)
+            assert np.array_equal(a[rows, :L], da[rows, :L])
+            assert (a[rows, L:] == -1).all() and np.isinf(g[rows, L:]).all()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_packed_queries_brute_force(seed):
+    # Independent per-pair restatement on ragged queries and documents: slice the
+    # query's and the document's rows by their offsets, form S, hide masked
+    # document rows with -inf, take the row maxima and sum over active rows.
+    rng = np.random.default_rng(500 + seed)
+    dim = int(rng.integers(1, 9))
+    lq_lens = rng.integers(0, 7, size=int(rng.integers(1, 5)))
+    ld_lens = rng.integers(0, 8, size=int(rng.integers(1, 5)))
+    Q, q_off, D, d_off, qm, dm = _ragged_problem(seed, lq_lens, ld_lens, dim, "f16")
+    Qf, Df = datagen.bits_to_float(Q, "f16"), datagen.bits_to_float(D, "f16")
+    Nq, Nd = len(lq_lens), len(ld_lens)
+    s, a, g = oracle.fwd_packed(Q, q_off, D, d_off, "f16", q_mask=qm, d_mask=dm)
+    for i in range(Nq):
+        qi = Qf[q_off[i]:q_off[i + 1]]
+        act = qm[q_off[i]:q_off[i + 1]].astype(bool)
+        for j in range(Nd):
+            S = qi @ Df[d_off[j]:d_off[j + 1]].T  # [L_i, Ld_j]
+            S = np.where(dm[d_off[j]:d_off[j + 1]].astype(bool)[None, :], S, -np.inf)
+            m = S.max(axis=1) if S.shape[1] else np.full(S.shape[0], -np.inf)
+            want = np.where(np.isfinite(m) & act, m, 0.0).sum()
+            assert abs(s[i, j] - want) <= 1e-12 * max(1.0, abs(want))
+            arg = np.where(np.isfinite(m), S.argmax(axis=1) if S.shape[1] else 0, -1)
+            row = a[i * Nd + j, : len(m)]
+            clear = g[i * Nd + j, : len(m)] > 1e-9
+            assert np.array_equal(row[clear], arg[clear]) and np.array_equal(row == -1, arg == -1)
+
+
 # ---------------------------------------------------------------- INT8
 
 def test_int8_brute_force():
