@@ -43,3 +43,17 @@ def assert_grad(got: torch.Tensor, ref: np.ndarray):
     tol = 1e-3 * np.maximum(np.abs(ref), floor)
     bad = np.abs(got - ref) > tol
     assert not bad.any(), f"{bad.sum()} gradient entries beyond 1e-3 relative (max |d| {np.abs(got - ref).max()})"
+
+
+def assert_grad_rounded(got: torch.Tensor, ref: np.ndarray, dtype: str):
+    """Gradients returned in the input's 16-bit type: the fp32 kernel result
+    (within the gradient tolerance of ref) is rounded once more, so allow one
+    unit in the last place of that type on top of the tolerance."""
+    got = got.float().cpu().numpy().astype(np.float64)
+    floor = 1e-2 * np.sqrt(np.mean(ref ** 2)) if ref.size else 0.0
+    mant = {"f16": 10, "bf16": 7}[dtype]
+    mag = np.maximum(np.abs(ref), np.finfo(np.float64).tiny)
+    ulp = np.exp2(np.floor(np.log2(mag)) - mant)
+    tol = 1e-3 * np.maximum(np.abs(ref), floor) + ulp
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{bad.sum()} gradient entries beyond 1e-3 relative + 1 ulp (max |d| {np.abs(got - ref).max()})"

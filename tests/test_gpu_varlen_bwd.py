@@ -7,7 +7,8 @@ import torch
 import datagen
 import oracle
 from maxsim_scoring_gb300 import ops
-from tests.gpu_util import assert_argmax, assert_grad, assert_scores, dev, dev_bits, integer_rows
+from tests.gpu_util import (assert_argmax, assert_grad, assert_grad_rounded, assert_scores, dev, dev_bits,
+                            integer_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -205,15 +206,20 @@ def test_backward_out_of_range_argmax_reported():
 def test_autograd_wrapper():
     from maxsim_scoring_gb300 import maxsim
     Nq, Lq, Nd, Ld, dim = 3, 16, 4, 90, 64
-    Q = dev_bits(datagen.gaussian_rows(2, 1, Nq * Lq, dim, "bf16").reshape(Nq, Lq, dim), "bf16").requires_grad_()
-    D = dev_bits(datagen.gaussian_rows(2, 2, Nd * Ld, dim, "bf16").reshape(Nd, Ld, dim), "bf16").requires_grad_()
+    Qb = datagen.gaussian_rows(2, 1, Nq * Lq, dim, "bf16").reshape(Nq, Lq, dim)
+    Db = datagen.gaussian_rows(2, 2, Nd * Ld, dim, "bf16").reshape(Nd, Ld, dim)
+    Q = dev_bits(Qb, "bf16").requires_grad_()
+    D = dev_bits(Db, "bf16").requires_grad_()
+    g = datagen.normal_f32(2, 6, Nq * Nd).reshape(Nq, Nd)
     s = maxsim(Q, D)
-    s.sum().backward()
-    # reference through materialised similarities (float32)
-    Qr = Q.detach().float().requires_grad_()
-    Dr = D.detach().float().requires_grad_()
-    S = torch.einsum("isk,jtk->ijst", Qr, Dr)
-    S.max(dim=3).values.sum(dim=2).sum().backward()
-    assert torch.allclose(s.detach(), S.max(dim=3).values.sum(dim=2).detach(), atol=1e-3 * Lq)
-    assert torch.allclose(Q.grad.float(), Qr.grad, atol=2e-2)
-    assert torch.allclose(D.grad.float(), Dr.grad, atol=2e-2)
+    (s * dev(g)).sum().backward()
+    ref_s, ref_a, gap = oracle.fwd_dense(Qb, Db, "bf16")
+    assert_scores(s.detach(), ref_s, Lq)
+    # the gradient through the argmax the forward saved (the same call, deterministic)
+    _, a = ops.maxsim_fwd(Q.detach(), D.detach(), want_argmax=True)
+    am = a.cpu().numpy()
+    assert_argmax(a, ref_a, gap)
+    ref_dQ, ref_dD, _, _ = oracle.bwd(Qb, Db, "bf16", am, g)
+    # the wrapper returns the gradients in the inputs' type (bf16)
+    assert_grad_rounded(Q.grad, ref_dQ, "bf16")
+    assert_grad_rounded(D.grad, ref_dD, "bf16")

@@ -85,7 +85,7 @@ def test_int8_rerank_full_size_sampled():
     s_only, _, _ = ops.maxsim_fwd_int8(dev(w["Q"]), dev(w["q_scale"]), dev(w["D"]), dev(w["d_scale"]))
     assert ops.device_status() == 0
     assert torch.equal(s, s_only)
-    docs = sample_docs(Nd, 100, 24)
+    docs = sample_docs(Nd, 200, 24)
     ref_s, ref_a, ref_w, gap = oracle.fwd_int8(w["Q"], w["q_scale"], w["D"], w["d_scale"], docs=docs)
     assert_scores(s[:, docs], ref_s, Lq)
     got_a = a.view(Nq, Nd, Lq)[:, docs].reshape(-1, Lq)
