@@ -365,6 +365,23 @@ const char *maxsim_status_string(maxsim_status status);
 maxsim_status maxsim_device_status(void *stream);
 
 /*
+ * Fault-handling test hook (the papers have no counterpart): lets a test
+ * drive a device-side bounded wait past its limit without faulting the GPU.
+ * It arms a one-shot for the next forward-kernel launch from this process
+ * (maxsim_fwd, _fwd_varlen, _fwd_int8, _score_pairs_packed and the calls
+ * built on them): that launch's epilogue warps first wait on an mbarrier
+ * that nothing ever arrives at and give up after limit_ns
+ * (1 <= limit_ns <= 2e9, else MAXSIM_ERR_INVALID_ARG). Giving up records
+ * MAXSIM_ERR_TIMEOUT in the device status word and raises the CTA's abort
+ * flag; every other role stops at its next wait, the copies and MMAs already
+ * issued are drained (each drain bounded by the normal 2 s limit), tensor
+ * memory is freed and the kernel returns. The call itself returns MAXSIM_OK
+ * and its outputs are invalid; the next call runs normally. Nothing traps
+ * and no wait is endless.
+ */
+maxsim_status maxsim_debug_inject_wait_timeout(uint64_t limit_ns);
+
+/*
  * Allocation-free variant of maxsim_fwd_varlen (the pages have no counterpart:
  * this is a deployment convenience of this library).
  *

@@ -127,6 +127,10 @@ struct FwdArgs {
     uint32_t nan_pair;    // two 16-bit NaNs of the operand type
     int* status;          // device status word
     uint64_t timeout_ns;  // bound on any single wait
+    // Fault-handling test hook (0 = off): the epilogue warps first wait on a
+    // barrier that nothing arrives at, giving up after this many ns; every
+    // other wait and every drain keeps timeout_ns.
+    uint64_t inject_wait_ns;
 };
 
 struct RowBlock {
@@ -330,6 +334,7 @@ struct alignas(16) SmemCtl {
     uint64_t acc_full[kNAcc], acc_empty[kNAcc];
     uint64_t mma_done;
     uint64_t epi_bar;  // rendezvous of the epilogue warps
+    uint64_t never;    // never arrived at (the fault-handling test hook waits on it)
     uint32_t tmem_base;
     volatile int32_t abort;
     float wslot[kMaxMT * 4];   // per-warp partial sums of the document being closed
@@ -342,18 +347,19 @@ __device__ __forceinline__ void record_status(const FwdArgs& a, int code) {
     if (a.status) atomicCAS(a.status, 0, code);
 }
 
-// Bounded wait: gives up after timeout_ns (records the status and raises the
+// Bounded wait: gives up after limit_ns (records the status and raises the
 // CTA abort flag) or when another role has already aborted. Inlined: the
 // kernel's warpgroups run under different register budgets (setmaxnreg),
 // which an out-of-line call shared between them cannot follow.
 template <bool kCluster>
-__device__ __forceinline__ bool wait_bar_slow(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar_slow(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity,
+                                              uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (ctl->abort) return false;
-            if (global_timer_ns() - t0 > a.timeout_ns) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 ctl->abort = 1;
                 record_status(a, kStatusTimeout);
                 return false;
@@ -367,7 +373,7 @@ __device__ __forceinline__ bool wait_bar_slow(const FwdArgs& a, SmemCtl* ctl, ui
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(const FwdArgs& a, SmemCtl* ctl, uint32_t bar, uint32_t parity) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    return wait_bar_slow<kCluster>(a, ctl, bar, parity);
+    return wait_bar_slow<kCluster>(a, ctl, bar, parity, a.timeout_ns);
 }
 
 // wait_bar for a whole warp that runs warp-uniform code: every lane polls,
@@ -508,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(&ctl->mma_done), kMmaWarps);
         mbar_init(smem_u32(&ctl->epi_bar), kEpiWarps);
+        mbar_init(smem_u32(&ctl->never), 1);
         ctl->abort = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_q);
@@ -543,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t stage = 0;
             uint32_t phase = 0, q_phase = 0;
             bool first_unit = true;
-            int64_t issued = 0;
+            int64_t issued = 0, q_issued = 0;
             bool ok = true;
             for (int32_t u = u0; u < n_units && ok; u += u_step) {
                 const Unit w = make_unit<kPair>(a, u, rank);
@@ -558,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int32_t ka = 0; ka < a.k_atoms; ++ka)
                         tma_load_2d(smem_u32(sQ + k * q_tile_bytes + ka * kAtomBytes), &tm_q, qbar, ka * 64,
                                     w.rb.row0 + k * kBM);
+                ++q_issued;
                 TileWalk tw;
                 for (tw.begin(a, w); tw.valid(); tw.advance(a)) {
                     const uint32_t empty = smem_u32(kInt8 ? &ctl->d8_empty[stage] : &ctl->d_empty[stage]);
@@ -574,7 +582,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (ctl->abort) {
-                // Let every copy still in flight land before the CTA exits.
+                // Let every copy still in flight land before the CTA exits: the
+                // query rows of the current unit (the n-th load completes phase
+                // n - 1 of q_full; an earlier one was consumed before the next
+                // was issued) and the last ring stages.
+                if (q_issued > 0) {
+                    const uint64_t t0 = global_timer_ns();
+                    const uint32_t qb = smem_u32(&ctl->q_full), qp = static_cast<uint32_t>((q_issued - 1) & 1);
+                    while (!mbar_try_wait(qb, qp) && global_timer_ns() - t0 < a.timeout_ns) {}
+                }
                 const int64_t outstanding = issued < ring ? issued : ring;
                 int32_t s = stage;
                 uint32_t ph = phase;
@@ -753,6 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t buf = 0;                              // global index of the tile's first buffer
         uint32_t epi_phase = 0;
         bool ok = true;
+        if (a.inject_wait_ns != 0)  // fault-handling test hook: this wait can only give up
+            ok = wait_bar_slow<false>(a, ctl, smem_u32(&ctl->never), 0u, a.inject_wait_ns);
         for (int32_t u = u0; u < n_units && ok; u += u_step) {
             const Unit w = make_unit<kPair>(a, u, rank);
             const RowBlock& rb = w.rb;

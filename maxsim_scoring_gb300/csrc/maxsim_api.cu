@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -39,6 +40,10 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
+
+// Armed by maxsim_debug_inject_wait_timeout; taken (and cleared) by the next
+// forward launch.
+std::atomic<uint64_t> g_inject_wait_ns{0};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -431,6 +436,7 @@ maxsim_status run_fwd(DeviceInfo* dev, const FwdPlan& p, const FwdCall& c, uint8
     a.nan_pair = c.nan_pair;
     a.status = dev->status;
     a.timeout_ns = kTimeoutNs;
+    a.inject_wait_ns = g_inject_wait_ns.exchange(0);
     // One CTA per SM: the request always exceeds half of an SM's shared memory.
     const size_t smem = std::max<size_t>(p.smem, kSmemBudget / 2 + 1024);
     a.pr_pairs = c.pr_pairs;
@@ -1030,6 +1036,12 @@ const char* maxsim_status_string(maxsim_status s) {
     case MAXSIM_ERR_DEVICE_INPUT: return "an input failed a device-side check";
     }
     return "unknown status";
+}
+
+maxsim_status maxsim_debug_inject_wait_timeout(uint64_t limit_ns) {
+    if (limit_ns == 0 || limit_ns > kTimeoutNs) return MAXSIM_ERR_INVALID_ARG;
+    g_inject_wait_ns.store(limit_ns);
+    return MAXSIM_OK;
 }
 
 maxsim_status maxsim_device_status(void* stream) {

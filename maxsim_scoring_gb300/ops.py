@@ -413,3 +413,10 @@ def device_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device status word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     return int(_native.lib().maxsim_device_status(_stream(dev)))
+
+
+def debug_inject_wait_timeout(limit_ns: int) -> None:
+    """Fault-handling test hook: the next forward launch from this process
+    waits, in its epilogue, on a barrier nothing arrives at and gives up after
+    limit_ns, recording MAXSIM_ERR_TIMEOUT (read it with device_status())."""
+    _native.check(_native.lib().maxsim_debug_inject_wait_timeout(int(limit_ns)), "maxsim_debug_inject_wait_timeout")
