@@ -338,6 +338,161 @@ __global__ void __launch_bounds__(256) dd_kernel(const BwdArgs b) {
     store_row<kVec>(b.dD + r * b.dim, lane, b.dim, acc);
 }
 
+// dD without a materialised CSR (dense D, caller did not ask for the CSR):
+// one CTA per (document j, slice of kDdRows of its tokens). The CTA reads
+// the Nq*Lq sources of document j, keeps those whose winner lies in its
+// slice, and builds the slice's inverse-argmax CSR in shared memory with the
+// same stable counting sort as csr_build_kernel (per-warp histograms over
+// contiguous runs of sources, ranks within a warp by lane order), so each
+// destination row lists its sources in ascending p (Sec. 4.2.2). Each warp
+// then owns kDdRows / kDdWarps consecutive destination rows and walks their
+// sources as one run (batches of gathers may cross a row boundary; a row is
+// stored when its last source is added), in the same order as dd_kernel:
+// the result is bitwise the same (Sec. 4.2.3, Eq. (3)).
+constexpr int kDdRows = 128;     // destination rows per CTA
+constexpr int kDdWarps = 16;     // warps per CTA
+constexpr int kDdMaxSrc = 16384; // sources of one document the shared-memory sort takes (Nq * Lq)
+constexpr int kDdGather = 8;     // source rows loaded together
+
+inline size_t dd_fused_smem(int32_t nsrc) {
+    // slot byte per source, per-warp histograms, row starts, the sorted sources (u16)
+    return static_cast<size_t>(nsrc) + kDdWarps * kDdRows * 4 + (kDdRows + 1) * 4 + 2 * static_cast<size_t>(nsrc) +
+           16;
+}
+
+template <int kVec>
+__global__ void __launch_bounds__(32 * kDdWarps, 2) dd_fused_kernel(const BwdArgs b) {
+    constexpr int kG = kVec <= 4 ? kDdGather : kDdGather / 2;  // wide rows: fewer in flight (registers)
+    extern __shared__ __align__(16) uint8_t dd_smem[];
+    const int32_t nsrc = b.nq * b.lq;
+    int32_t* hist = reinterpret_cast<int32_t*>(dd_smem);     // [kDdWarps][kDdRows], then offsets
+    int32_t* rs = hist + kDdWarps * kDdRows;                 // [kDdRows + 1] row starts
+    uint16_t* list = reinterpret_cast<uint16_t*>(rs + kDdRows + 1);  // [nsrc] sorted sources
+    uint8_t* slot_of = reinterpret_cast<uint8_t*>(list + nsrc);      // [nsrc] slot, 0xFF = elsewhere
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t j = blockIdx.x;
+    const int32_t t0 = blockIdx.y * kDdRows, t1 = min(t0 + kDdRows, b.ld);
+    const int32_t nrows = t1 - t0;
+    for (int32_t x = threadIdx.x; x < kDdWarps * kDdRows; x += blockDim.x) hist[x] = 0;
+    __syncthreads();
+    // 1. slots and per-warp counts; every argmax is checked once (slice 0)
+    const int32_t per = (nsrc + kDdWarps - 1) / kDdWarps;
+    const int32_t n0 = min(warp * per, nsrc), n1 = min(n0 + per, nsrc);
+    bool bad = false;
+#pragma unroll 4
+    for (int32_t n = n0 + lane; n < n1; n += 32) {
+        const int32_t a = b.argmax[src_index(b, j, n)];
+        bad |= !argmax_ok(a, b.ld);
+        const bool mine = a >= t0 && a < t1;
+        slot_of[n] = mine ? static_cast<uint8_t>(a - t0) : 0xFFu;
+        if (mine) atomicAdd(&hist[warp * kDdRows + (a - t0)], 1);
+    }
+    if (bad && blockIdx.y == 0 && b.status) atomicCAS(b.status, 0, 6);
+    __syncthreads();
+    // 2. exclusive scan over (row, warp), row-major: thread x owns four entries
+    {
+        constexpr int kPer = kDdRows * kDdWarps / (32 * kDdWarps);  // 4
+        int32_t v[kPer], local = 0;
+        const int x0 = threadIdx.x * kPer;  // flat index r * kDdWarps + w
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int x = x0 + q, r = x / kDdWarps, w = x % kDdWarps;
+            v[q] = hist[w * kDdRows + r];
+            local += v[q];
+        }
+        int32_t incl = local;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        __shared__ int32_t wsum[kDdWarps];
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        int32_t before = 0;
+        for (int w = 0; w < warp; ++w) before += wsum[w];
+        int32_t run = before + incl - local;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int x = x0 + q, r = x / kDdWarps, w = x % kDdWarps;
+            if (w == 0) rs[r] = run;
+            hist[w * kDdRows + r] = run;  // warp w's next free place in row r
+            run += v[q];
+        }
+        if (threadIdx.x == blockDim.x - 1) rs[kDdRows] = run;
+    }
+    __syncthreads();
+    // 3. stable placement: in a warp's run of sources, equal slots rank by lane
+    for (int32_t nb = n0; nb < n1; nb += 32) {
+        const int32_t n = nb + lane;
+        const uint32_t sl = n < n1 ? slot_of[n] : 0xFFu;
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, sl);
+        if (sl != 0xFFu) {
+            const int32_t rank = __popc(peers & ((1u << lane) - 1u));
+            list[hist[warp * kDdRows + sl] + rank] = static_cast<uint16_t>(n);
+            __syncwarp(peers);
+            if ((peers >> lane) == 1u) hist[warp * kDdRows + sl] += __popc(peers);  // highest peer lane
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    // 4. destination rows r0 .. r1-1 of this warp, their sources in one run
+    constexpr int kRowsPerWarp = kDdRows / kDdWarps;
+    const int32_t r0 = warp * kRowsPerWarp, r1 = min(r0 + kRowsPerWarp, nrows);
+    if (r0 >= r1) return;
+    float* out = b.dD + (static_cast<int64_t>(j) * b.ld + t0) * b.dim;
+    float acc[kVec];
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
+    int32_t row = r0, row_end = rs[r0 + 1];
+    const int32_t e_end = rs[r1];
+    for (int32_t eb = rs[r0]; eb < e_end; eb += 32) {
+        const int32_t cnt = min(32, e_end - eb);
+        int64_t off = 0;
+        float wl = 0.f;
+        if (lane < cnt) {
+            const int32_t n = list[eb + lane];
+            const int32_t i = n / b.lq, sq = n - (n / b.lq) * b.lq;
+            const int64_t qr = static_cast<int64_t>(i) * b.lq + sq;
+            wl = b.g[static_cast<int64_t>(i) * b.nd + j];
+            if (b.q_mask && !b.q_mask[qr]) wl = 0.f;
+            off = qr * b.dim;
+        }
+        for (int32_t k = 0; k < cnt; k += kG) {
+            float x[kG][kVec];
+            float w[kG];
+#pragma unroll
+            for (int u = 0; u < kG; ++u) {
+                const int32_t src = min(k + u, cnt - 1);
+                w[u] = __shfl_sync(0xFFFFFFFFu, wl, src);
+                const int64_t o = __shfl_sync(0xFFFFFFFFu, off, src);
+                load_row<kVec>(b.Q + o, lane, b.dim, b.is_bf16, x[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kG; ++u) {
+                if (k + u < cnt) {
+                    const int32_t e = eb + k + u;
+                    while (e >= row_end) {  // the current row is complete (warp-uniform)
+                        store_row<kVec>(out + static_cast<int64_t>(row) * b.dim, lane, b.dim, acc);
+#pragma unroll
+                        for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
+                        ++row;
+                        row_end = rs[row + 1];
+                    }
+#pragma unroll
+                    for (int v = 0; v < kVec; ++v) acc[v] = fmaf(w[u], x[u][v], acc[v]);
+                }
+            }
+        }
+    }
+    for (; row < r1; ++row) {  // the last row with sources, then rows without any
+        store_row<kVec>(out + static_cast<int64_t>(row) * b.dim, lane, b.dim, acc);
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
+    }
+}
+
+constexpr int kDqGather = 8;  // D rows loaded together by the dQ gather
+
 // dQ: one warp per (query row (i, s), chunk of documents), ascending j. The
 // winners and weights of 32 documents are loaded at once, one per lane. With
 // one chunk the warp writes dQ; with several (gridDim.y > 1, many documents
@@ -373,12 +528,12 @@ __global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b, float* __restr
                 off = -1;
             }
         }
-        for (int32_t k = 0; k < cnt; k += kGather) {
-            float x[kGather][kVec];
-            float w[kGather];
-            bool use[kGather];
+        for (int32_t k = 0; k < cnt; k += kDqGather) {
+            float x[kDqGather][kVec];
+            float w[kDqGather];
+            bool use[kDqGather];
 #pragma unroll
-            for (int u = 0; u < kGather; ++u) {
+            for (int u = 0; u < kDqGather; ++u) {
                 const int32_t src = min(k + u, cnt - 1);
                 w[u] = __shfl_sync(0xFFFFFFFFu, wl, src);
                 const int64_t o = __shfl_sync(0xFFFFFFFFu, off, src);
@@ -386,7 +541,7 @@ __global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b, float* __restr
                 load_row<kVec>(b.D + (o >= 0 ? o : 0), lane, b.dim, b.is_bf16, x[u]);
             }
 #pragma unroll
-            for (int u = 0; u < kGather; ++u) {
+            for (int u = 0; u < kDqGather; ++u) {
                 if (use[u]) {
 #pragma unroll
                     for (int v = 0; v < kVec; ++v) acc[v] = fmaf(w[u], x[u][v], acc[v]);

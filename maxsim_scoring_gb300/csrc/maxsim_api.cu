@@ -474,16 +474,27 @@ maxsim_status run_fwd(DeviceInfo* dev, const FwdPlan& p, const FwdCall& c, uint8
 // ---------------------------------------------------------------- pair lists
 
 // Valid pairs counted per query; a pair outside [0, Nq) x [0, Nd) scores 0,
-// its argmax row is -1, and it is reported on the device status word.
+// its argmax row is -1, and it is reported on the device status word. The
+// lanes of a warp that hold pairs of the same query add their count with one
+// atomic (pair lists usually come grouped by query, so one per warp).
 __global__ void pairs_count_kernel(const int32_t* __restrict__ pairs, int64_t np, int64_t nq, int64_t nd,
                                    int32_t* __restrict__ qcnt, float* __restrict__ scores, int32_t* __restrict__ argmax,
                                    int64_t lq_out, int* status) {
-    for (int64_t p = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; p < np;
-         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int32_t q = pairs[2 * p], d = pairs[2 * p + 1];
-        if (q >= 0 && q < nq && d >= 0 && d < nd) {
-            atomicAdd(qcnt + q, 1);
-        } else {
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    // every lane of a warp runs the same iterations (warp-wide match below)
+    for (int64_t base = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x - lane; base < np;
+         base += stride) {
+        const int64_t p = base + lane;
+        int32_t key = -2;  // -2: no pair in this lane, -1: an invalid pair
+        if (p < np) {
+            const int32_t q = pairs[2 * p], d = pairs[2 * p + 1];
+            key = (q >= 0 && q < nq && d >= 0 && d < nd) ? q : -1;
+        }
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
+        if (key >= 0) {
+            if (qcnt && lane == __ffs(peers) - 1) atomicAdd(qcnt + key, __popc(peers));
+        } else if (key == -1) {
             scores[p] = 0.f;
             if (argmax)
                 for (int64_t s = 0; s < lq_out; ++s) argmax[p * lq_out + s] = -1;
@@ -549,14 +560,29 @@ __global__ void __launch_bounds__(1024) pairs_scan_kernel(const int32_t* __restr
     }
 }
 
-// Each valid pair to the next free slot of its query. The order inside a
-// query's group is free: every pair is scored on its own.
+// Each valid pair to a free slot of its query. The order inside a query's
+// group is free: every pair is scored on its own. The lanes of a warp with
+// pairs of the same query reserve their slots with one atomic.
 __global__ void pairs_place_kernel(const int32_t* __restrict__ pairs, int64_t np, int64_t nq, int64_t nd,
                                    int32_t* __restrict__ cursor, int32_t* __restrict__ sorted) {
-    for (int64_t p = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; p < np;
-         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int32_t q = pairs[2 * p], d = pairs[2 * p + 1];
-        if (q >= 0 && q < nq && d >= 0 && d < nd) sorted[atomicAdd(cursor + q, 1)] = static_cast<int32_t>(p);
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t base = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x - lane; base < np;
+         base += stride) {
+        const int64_t p = base + lane;
+        int32_t key = -1;
+        if (p < np) {
+            const int32_t q = pairs[2 * p], d = pairs[2 * p + 1];
+            if (q >= 0 && q < nq && d >= 0 && d < nd) key = q;
+        }
+        const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
+        if (key >= 0) {
+            const int leader = __ffs(peers) - 1;
+            int32_t slot = 0;
+            if (lane == leader) slot = atomicAdd(cursor + key, __popc(peers));
+            slot = __shfl_sync(peers, slot, leader) + __popc(peers & ((1u << lane) - 1u));
+            sorted[slot] = static_cast<int32_t>(p);
+        }
     }
 }
 
@@ -886,6 +912,16 @@ StreamedPlan plan_streamed(int64_t Nq, int64_t Lq, int64_t blk, int64_t Ld, int6
 
 // Document chunks of the dQ gather: enough warps to fill the GPU when a query
 // row has many documents to visit, at least 64 documents per chunk.
+template <int kVec>
+maxsim_status launch_dd_fused(dim3 grid, size_t shm, cudaStream_t st, const BwdArgs& b) {
+    if (shm > 48 * 1024 &&
+        cudaFuncSetAttribute(dd_fused_kernel<kVec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(shm)) != cudaSuccess)
+        return MAXSIM_ERR_CUDA;
+    dd_fused_kernel<kVec><<<grid, 32 * kDdWarps, shm, st>>>(b);
+    return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
 int32_t dq_chunks(int64_t Nq, int64_t lq, int64_t Nd) {
     const int64_t rows = std::max<int64_t>(1, Nq * lq);
     const int64_t want = (16384 + rows - 1) / rows;
@@ -960,7 +996,28 @@ maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void
     b.d_rows = d_rows;
     if (cu_d) check_cu_kernel<<<grid_for(Nd + 1, 256, dev->num_sms), 256, 0, st>>>(cu_d, Nd, d_rows, dev->status);
     if (cu_q) check_cu_kernel<<<grid_for(Nq + 1, 256, dev->num_sms), 256, 0, st>>>(cu_q, Nq, -1, dev->status);
-    if (need_csr) {
+    const int vec = static_cast<int>((dim + 31) / 32);
+    // dD alone, dense D: the CSR of each document slice is built in shared
+    // memory next to the reduction (the same sorted sources, the same sums)
+    const bool fused_dd = dD && !csr_row_ptr && !csr_col && !cu_d && !cu_q && Ld > 0 && Nd > 0 &&
+                          Nq * Lq <= kDdMaxSrc;
+    if (fused_dd) {
+        const dim3 grid(static_cast<unsigned>(Nd), static_cast<unsigned>((Ld + kDdRows - 1) / kDdRows));
+        const size_t shm = dd_fused_smem(static_cast<int32_t>(Nq * Lq));
+        static_assert(kDdMaxSrc * 3 + kDdWarps * kDdRows * 4 + (kDdRows + 1) * 4 + 16 <= 227 * 1024, "fused dD smem");
+        maxsim_status frc = MAXSIM_OK;
+        switch (vec) {
+        case 1: frc = launch_dd_fused<1>(grid, shm, st, b); break;
+        case 2: frc = launch_dd_fused<2>(grid, shm, st, b); break;
+        case 3: frc = launch_dd_fused<3>(grid, shm, st, b); break;
+        case 4: frc = launch_dd_fused<4>(grid, shm, st, b); break;
+        case 5: frc = launch_dd_fused<5>(grid, shm, st, b); break;
+        case 6: frc = launch_dd_fused<6>(grid, shm, st, b); break;
+        case 7: frc = launch_dd_fused<7>(grid, shm, st, b); break;
+        default: frc = launch_dd_fused<8>(grid, shm, st, b); break;
+        }
+        if (frc != MAXSIM_OK) return frc;
+    } else if (need_csr) {
         b.doc_cnt = reinterpret_cast<int32_t*>(ws + off_cnt);
         b.doc_base = reinterpret_cast<int32_t*>(ws + off_base);
         b.row_ptr = csr_row_ptr ? csr_row_ptr : reinterpret_cast<int32_t*>(ws + off_rp);
@@ -982,8 +1039,7 @@ maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void
         }
         if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
     }
-    const int vec = static_cast<int>((dim + 31) / 32);
-    if (dD && d_rows > 0) {
+    if (dD && d_rows > 0 && !fused_dd) {
         const int grid = static_cast<int>((d_rows + 7) / 8);
         switch (vec) {
         case 1: dd_kernel<1><<<grid, 256, 0, st>>>(b); break;

@@ -193,6 +193,67 @@ def test_backward_hot_token_contention():
     assert_grad(dD, ref_dD)
 
 
+@pytest.mark.parametrize("shape", [(5, 24, 6, 300, 128), (16, 32, 3, 64, 32), (2, 40, 4, 1030, 256),
+                                   (64, 128, 2, 1024, 128)])
+def test_backward_without_csr_equals_csr_path(shape):
+    # Without the CSR outputs, dD comes from the shared-memory CSR of each
+    # document slice: the same sources in the same order, so the same bits.
+    Nq, Lq, Nd, Ld, dim = shape
+    seed = 41
+    Q = datagen.gaussian_rows(seed, 1, Nq * Lq, dim, "bf16").reshape(Nq, Lq, dim)
+    D = datagen.gaussian_rows(seed, 2, Nd * Ld, dim, "bf16").reshape(Nd, Ld, dim)
+    qm = datagen.mask_drop_tail(seed, 4, Nq, Lq, 8)
+    dm = np.ones((Nd, Ld), np.uint8)
+    dm[-1, 5:] = 0  # one document's winners crowd into its first tokens
+    g = datagen.normal_f32(seed, 6, Nq * Nd).reshape(Nq, Nd)
+    Qd, Dd = dev_bits(Q, "bf16"), dev_bits(D, "bf16")
+    _, a = ops.maxsim_fwd(Qd, Dd, dev(qm), dev(dm), want_argmax=True)
+    dQ1, dD1, _, _ = ops.maxsim_bwd(Qd, Dd, a, dev(g), dev(qm), want_csr=True)
+    dQ2, dD2, _, _ = ops.maxsim_bwd(Qd, Dd, a, dev(g), dev(qm))
+    _, dD3, _, _ = ops.maxsim_bwd(Qd, Dd, a, dev(g), dev(qm), want_dq=False)
+    assert ops.device_status() == 0
+    assert torch.equal(dD1, dD2) and torch.equal(dD2, dD3) and torch.equal(dQ1, dQ2)
+    am = a.cpu().numpy()
+    ref_dQ, ref_dD, _, _ = oracle.bwd(Q, D, "bf16", am, g, q_mask=qm)
+    assert_grad(dQ2, ref_dQ)
+    assert_grad(dD2, ref_dD)
+
+
+def test_backward_without_csr_hot_token():
+    # every query token picks token 0 of its document: one destination row gets all sources
+    Nq, Lq, Nd, Ld, dim = 64, 128, 2, 300, 64
+    rng = np.random.default_rng(9)
+    Q = datagen.float_to_bits(np.abs(integer_rows(rng, Nq * Lq, dim)), "bf16").reshape(Nq, Lq, dim)
+    Dv = np.zeros((Nd * Ld, dim))
+    Dv[::Ld] = 1.0
+    D = datagen.float_to_bits(Dv, "bf16").reshape(Nd, Ld, dim)
+    g = datagen.normal_f32(3, 6, Nq * Nd).reshape(Nq, Nd)
+    Qd, Dd = dev_bits(Q, "bf16"), dev_bits(D, "bf16")
+    _, a = ops.maxsim_fwd(Qd, Dd, want_argmax=True)
+    _, dD, _, _ = ops.maxsim_bwd(Qd, Dd, a, dev(g))
+    _, dD_csr, _, _ = ops.maxsim_bwd(Qd, Dd, a, dev(g), want_csr=True)
+    assert ops.device_status() == 0
+    assert torch.equal(dD, dD_csr)
+    ref_dQ, ref_dD, _, _ = oracle.bwd(Q, D, "bf16", a.cpu().numpy(), g)
+    assert_grad(dD, ref_dD)
+
+
+def test_backward_without_csr_out_of_range_reported():
+    Nq, Lq, Nd, Ld, dim = 1, 4, 2, 8, 16
+    Q = dev_bits(datagen.gaussian_rows(1, 1, Nq * Lq, dim, "f16").reshape(Nq, Lq, dim), "f16")
+    D = dev_bits(datagen.gaussian_rows(1, 2, Nd * Ld, dim, "f16").reshape(Nd, Ld, dim), "f16")
+    a = dev(np.array([[0, 1, 9, -1], [2, 3, 4, -7]], np.int32))
+    g = dev(np.ones((Nq, Nd), np.float32))
+    _, dD, _, _ = ops.maxsim_bwd(Q, D, a, g)
+    assert ops.device_status() == 6
+    # the valid sources still land: rows 0, 1 of document 0 and 2, 3, 4 of document 1
+    got = dD.cpu().numpy()
+    q = datagen.bits_to_float(datagen.gaussian_rows(1, 1, Nq * Lq, dim, "f16"), "f16")
+    np.testing.assert_allclose(got[0, 0], q[0], rtol=1e-6)
+    np.testing.assert_allclose(got[1, 4], q[2], rtol=1e-6)
+    assert not got[0, 2:].any()
+
+
 def test_backward_out_of_range_argmax_reported():
     Nq, Lq, Nd, Ld, dim = 1, 4, 2, 8, 16
     Q = dev_bits(datagen.gaussian_rows(1, 1, Nq * Lq, dim, "f16").reshape(Nq, Lq, dim), "f16")
