@@ -485,6 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kPair) mbar_arrive_cluster(at_leader(bar));
         else mbar_arrive(smem_u32(bar));
     };
+    // accumulator buffer handed back: only tensor-memory reads precede it
+    auto release_acc = [&](const uint64_t* bar) {
+        if constexpr (kPair) mbar_arrive_remote(at_leader(bar));
+        else mbar_arrive(smem_u32(bar));
+    };
 
     // Ring depths index fixed-size barrier arrays: refuse a launch that breaks
     // them (both CTAs of a pair see the same arguments and return together).
@@ -890,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_ld();
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) arrive_leader(&ctl->acc_empty[slot]);
+                        if (lane == 0) release_acc(&ctl->acc_empty[slot]);
                         if constexpr (!kArg) {
                             m[q] = fmax3(m[q], fmax3(cm[0], cm[1], cm[2]), cm[3]);
                         } else {
@@ -912,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_ld();
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) arrive_leader(&ctl->acc_empty[slot]);
+                        if (lane == 0) release_acc(&ctl->acc_empty[slot]);
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
                             if (c < nchunks) fold(v[c], c);

@@ -149,6 +149,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive on an mbarrier given by its shared::cluster address, with the
+// default (CTA-scope) release: enough when the only accesses to order are
+// tensor-memory reads, which tcgen05.fence::before_thread_sync orders before
+// this arrive. A cluster-scope release would first wait for every earlier
+// memory operation of the thread (global stores included) to become visible
+// to the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
