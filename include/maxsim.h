@@ -364,6 +364,9 @@ const char *maxsim_status_string(maxsim_status status);
  */
 maxsim_status maxsim_device_status(void *stream);
 
+/* The same call under the name the problem statement of this library uses. */
+maxsim_status maxsim_last_device_status(void *stream);
+
 /*
  * Fault-handling test hook (the papers have no counterpart): lets a test
  * drive a device-side bounded wait past its limit without faulting the GPU.

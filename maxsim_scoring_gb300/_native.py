@@ -57,6 +57,7 @@ SIGNATURES = {
     "maxsim_workspace_size": (_SZ, [_I, _I64, _I64, _I64, _I64, _I64]),
     "maxsim_status_string": (ctypes.c_char_p, [_I]),
     "maxsim_device_status": (_I, [_VP]),
+    "maxsim_last_device_status": (_I, [_VP]),
     "maxsim_debug_inject_wait_timeout": (_I, [ctypes.c_uint64]),
     "maxsim_version": (_I, []),
 }

@@ -455,10 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // then costs no shared-memory bandwidth) next to two accumulator
     // buffers; CTA pairs keep them in shared memory next to four.
     constexpr int kAccBufs = kNAcc;
-    // Two MMA warps (1 and 3) share the issue work of a single CTA: M-tiles
-    // k = i, i + 2, ... go to warp i, so that one issues while the other
-    // waits or keeps books. A CTA pair has one issuer and two prep warps.
-    constexpr int kMmaWarps = kPair ? 1 : 2;
+    // Two MMA warps (1 and 3) share the issue work: M-tiles k = i, i + 2, ...
+    // go to warp i, so that one issues while the other waits or keeps books.
+    // An INT8 CTA pair has one issuer and two prep warps (the widening).
+    constexpr int kMmaWarps = (kPair && kInt8) ? 1 : 2;
     constexpr int kPrepWarps = 3 - kMmaWarps;
     constexpr int kDRows = kPair ? kBN / 2 : kBN;  // document rows per operand stage in this CTA
     constexpr int kDAtom = kDRows * 128;           // bytes of one 128-byte-wide K block of a stage

@@ -207,14 +207,16 @@ FwdPlan plan_fwd_mode(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varl
     return p;
 }
 
-// Pair mode for INT8 documents when there are at least two row blocks: the
-// INT8 staging ring and the 16-bit operand ring then fit beside four resident
-// query M-tiles (measured 1.8x faster on a 10K x 1024-token INT8 rerank). For
-// 16-bit documents the single-CTA kernel measured faster (ColBERT varlen,
-// ColPali cross product), so it stays the default there.
-FwdPlan plan_fwd(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varlen_q, bool int8) {
+// Pair mode whenever there are at least two row blocks: each SM then reads
+// from shared memory its own query rows and only half of every document tile
+// per MMA, so the MMAs run at the tensor rate (the single-CTA kernel is bound
+// by shared-memory operand reads at the short tiles of varlen documents), and
+// for INT8 the staging ring and the 16-bit operand ring fit beside four
+// resident query M-tiles. The pair-list walk (allow_pair = false) runs on
+// single CTAs.
+FwdPlan plan_fwd(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varlen_q, bool int8, bool allow_pair = true) {
     FwdPlan p = plan_fwd_mode(nq, lq, nd, dim, varlen_q, int8, false);
-    if (int8 && p.ok && p.n_rb >= 2) {
+    if (allow_pair && p.ok && p.n_rb >= 2) {
         FwdPlan q = plan_fwd_mode(nq, lq, nd, dim, varlen_q, int8, true);
         if (q.ok && q.n_rb >= 2) return q;
     }
@@ -452,10 +454,11 @@ maxsim_status run_fwd(DeviceInfo* dev, const FwdPlan& p, const FwdCall& c, uint8
 
     maxsim_status rc;
     const bool arg = c.argmax != nullptr;
-    if (p.pair) {  // planned for INT8 documents only
-        if (!p.int8) return MAXSIM_ERR_UNSUPPORTED;
-        rc = arg ? launch_fwd_kernel<true, true, true>(dev, 8, tq, td, a, smem, grid, st)
-                 : launch_fwd_kernel<false, true, true>(dev, 9, tq, td, a, smem, grid, st);
+    if (p.pair) {
+        if (p.int8) rc = arg ? launch_fwd_kernel<true, true, true>(dev, 8, tq, td, a, smem, grid, st)
+                             : launch_fwd_kernel<false, true, true>(dev, 9, tq, td, a, smem, grid, st);
+        else rc = arg ? launch_fwd_kernel<true, false, true>(dev, 10, tq, td, a, smem, grid, st)
+                      : launch_fwd_kernel<false, false, true>(dev, 11, tq, td, a, smem, grid, st);
     } else {
         if (p.int8) rc = arg ? launch_fwd_kernel<true, true, false>(dev, 0, tq, td, a, smem, grid, st)
                              : launch_fwd_kernel<false, true, false>(dev, 1, tq, td, a, smem, grid, st);
@@ -864,7 +867,7 @@ struct TwoStagePlan {
 TwoStagePlan plan_two_stage(int64_t Nq, int64_t Lq, int64_t Nd, int64_t dim, int64_t k1) {
     TwoStagePlan p;
     const FwdPlan p8 = plan_fwd(Nq, Lq, Nd, dim, false, true);
-    const FwdPlan p16 = plan_fwd(Nq, Lq, Nd, dim, true, false);
+    const FwdPlan p16 = plan_fwd(Nq, Lq, Nd, dim, true, false, false);
     if (!p8.ok || !p16.ok || p16.n_chunks > 1) return p;
     p.stage_bytes = std::max(p8.ws_bytes, pairs_ws(p16.ws_bytes, Nq, Nq * k1).bytes);
     size_t off = 0;
@@ -1113,6 +1116,8 @@ maxsim_status maxsim_device_status(void* stream) {
     return static_cast<maxsim_status>(v);
 }
 
+maxsim_status maxsim_last_device_status(void* stream) { return maxsim_device_status(stream); }
+
 size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim) {
     if (Nq < 0 || Lq < 0 || Nd < 0 || Ld < 0 || dim <= 0) return static_cast<size_t>(-1);
     switch (op) {
@@ -1121,7 +1126,7 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
     case MAXSIM_OP_FWD_VARLEN:
         return plan_fwd(Nq, Lq, Nd, dim, true, false).ws_bytes;
     case MAXSIM_OP_SCORE_PAIRS:  // Ld carries the number of pairs
-        return pairs_ws(plan_fwd(Nq, Lq, Nd, dim, true, false).ws_bytes, Nq, Ld).bytes;
+        return pairs_ws(plan_fwd(Nq, Lq, Nd, dim, true, false, false).ws_bytes, Nq, Ld).bytes;
     case MAXSIM_OP_FWD_INT8:
         return plan_fwd(Nq, Lq, Nd, dim, false, true).ws_bytes;
     case MAXSIM_OP_BWD:
@@ -1278,7 +1283,7 @@ maxsim_status maxsim_score_pairs_packed(const void* Q, const int32_t* cu_seqlens
     if ((max_lq > 0 && (!Q || !aligned16(Q))) || (total_d > 0 && (!D || !aligned16(D))))
         return MAXSIM_ERR_INVALID_ARG;
     if (total_d > kI32Max || Nq * pad_lq(max_lq) > kI32Max || num_pairs > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
-    const FwdPlan p = plan_fwd(Nq, max_lq, Nd, dim, true, false);
+    const FwdPlan p = plan_fwd(Nq, max_lq, Nd, dim, true, false, false);
     if (!p.ok || p.n_chunks > 1) return MAXSIM_ERR_UNSUPPORTED;  // one query per unit: up to 4 M-tiles
     const PairsWs pw = pairs_ws(p.ws_bytes, Nq, num_pairs);
     if (workspace_bytes < pw.bytes || !workspace) return MAXSIM_ERR_WORKSPACE;
