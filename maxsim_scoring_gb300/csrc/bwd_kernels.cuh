@@ -287,6 +287,54 @@ __device__ __forceinline__ void store_row(float* __restrict__ out, int lane, int
 // latencies overlap; the accumulation order is unchanged.
 constexpr int kGather = 4;
 
+// This lane's kVec elements of one row kept as raw 16-bit values (two per
+// word) until they are used: a batch of gathers then holds half the
+// registers of decoded floats, so twice as many rows can be in flight.
+template <int kVec>
+struct RawRow {
+    uint32_t w[(kVec + 1) / 2];
+};
+
+template <int kVec>
+__device__ __forceinline__ void load_raw(const uint16_t* __restrict__ row, int lane, int32_t dim, RawRow<kVec>& r) {
+    const int k0 = lane * kVec;
+    if constexpr (kVec == 2 || kVec == 4 || kVec == 8) {
+        if (dim == 32 * kVec) {
+            if constexpr (kVec == 2) {
+                r.w[0] = __ldg(reinterpret_cast<const uint32_t*>(row + k0));
+            } else if constexpr (kVec == 4) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(row + k0));
+                r.w[0] = u.x;
+                r.w[1] = u.y;
+            } else {
+                const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + k0));
+                r.w[0] = u.x;
+                r.w[1] = u.y;
+                r.w[2] = u.z;
+                r.w[3] = u.w;
+            }
+            return;
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < (kVec + 1) / 2; ++h) {
+        const int k = k0 + 2 * h;
+        const uint32_t lo = k < dim ? row[k] : 0u;
+        const uint32_t hi = (2 * h + 1 < kVec && k + 1 < dim) ? row[k + 1] : 0u;
+        r.w[h] = lo | (hi << 16);
+    }
+}
+
+// acc[v] += wgt * element v, in element order (the same FMAs as with decoded rows).
+template <int kVec>
+__device__ __forceinline__ void fma_raw(float wgt, const RawRow<kVec>& r, int32_t is_bf16, float (&acc)[kVec]) {
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+        const uint16_t h = static_cast<uint16_t>((v & 1) ? (r.w[v >> 1] >> 16) : (r.w[v >> 1] & 0xFFFFu));
+        acc[v] = fmaf(wgt, bits_to_f32(h, is_bf16), acc[v]);
+    }
+}
+
 // dD: one warp per destination row (j, t); lanes split the embedding. The
 // row's sources are taken 32 at a time: each lane decodes one (index, weight),
 // then the warp walks them in CSR order.
@@ -352,7 +400,7 @@ __global__ void __launch_bounds__(256) dd_kernel(const BwdArgs b) {
 constexpr int kDdRows = 128;     // destination rows per CTA
 constexpr int kDdWarps = 16;     // warps per CTA
 constexpr int kDdMaxSrc = 16384; // sources of one document the shared-memory sort takes (Nq * Lq)
-constexpr int kDdGather = 8;     // source rows loaded together
+constexpr int kDdGather = 16;    // source rows loaded together
 
 inline size_t dd_fused_smem(int32_t nsrc) {
     // slot byte per source, per-warp histograms, row starts, the sorted sources (u16)
@@ -458,14 +506,14 @@ __global__ void __launch_bounds__(32 * kDdWarps, 2) dd_fused_kernel(const BwdArg
             off = qr * b.dim;
         }
         for (int32_t k = 0; k < cnt; k += kG) {
-            float x[kG][kVec];
+            RawRow<kVec> x[kG];
             float w[kG];
 #pragma unroll
             for (int u = 0; u < kG; ++u) {
                 const int32_t src = min(k + u, cnt - 1);
                 w[u] = __shfl_sync(0xFFFFFFFFu, wl, src);
                 const int64_t o = __shfl_sync(0xFFFFFFFFu, off, src);
-                load_row<kVec>(b.Q + o, lane, b.dim, b.is_bf16, x[u]);
+                load_raw<kVec>(b.Q + o, lane, b.dim, x[u]);
             }
 #pragma unroll
             for (int u = 0; u < kG; ++u) {
@@ -478,8 +526,7 @@ __global__ void __launch_bounds__(32 * kDdWarps, 2) dd_fused_kernel(const BwdArg
                         ++row;
                         row_end = rs[row + 1];
                     }
-#pragma unroll
-                    for (int v = 0; v < kVec; ++v) acc[v] = fmaf(w[u], x[u][v], acc[v]);
+                    fma_raw<kVec>(w[u], x[u], b.is_bf16, acc);
                 }
             }
         }
@@ -491,7 +538,7 @@ __global__ void __launch_bounds__(32 * kDdWarps, 2) dd_fused_kernel(const BwdArg
     }
 }
 
-constexpr int kDqGather = 8;  // D rows loaded together by the dQ gather
+constexpr int kDqGather = 16;  // D rows loaded together by the dQ gather
 
 // dQ: one warp per (query row (i, s), chunk of documents), ascending j. The
 // winners and weights of 32 documents are loaded at once, one per lane. With
@@ -499,7 +546,8 @@ constexpr int kDqGather = 8;  // D rows loaded together by the dQ gather
 // per query row) each chunk writes its partial row to `part` and
 // dq_reduce_kernel adds the chunks in order: a fixed summation order either way.
 template <int kVec>
-__global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b, float* __restrict__ part) {
+__global__ void __launch_bounds__(256, 4) dq_kernel(const BwdArgs b, float* __restrict__ part) {
+    constexpr int kG = kVec <= 4 ? kDqGather : kDqGather / 2;  // wide rows: fewer in flight (registers)
     const int lane = threadIdx.x & 31;
     const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nrows = static_cast<int64_t>(b.nq) * b.lq;
@@ -528,24 +576,21 @@ __global__ void __launch_bounds__(256) dq_kernel(const BwdArgs b, float* __restr
                 off = -1;
             }
         }
-        for (int32_t k = 0; k < cnt; k += kDqGather) {
-            float x[kDqGather][kVec];
-            float w[kDqGather];
-            bool use[kDqGather];
+        for (int32_t k = 0; k < cnt; k += kG) {
+            RawRow<kVec> x[kG];
+            float w[kG];
+            bool use[kG];
 #pragma unroll
-            for (int u = 0; u < kDqGather; ++u) {
+            for (int u = 0; u < kG; ++u) {
                 const int32_t src = min(k + u, cnt - 1);
                 w[u] = __shfl_sync(0xFFFFFFFFu, wl, src);
                 const int64_t o = __shfl_sync(0xFFFFFFFFu, off, src);
                 use[u] = k + u < cnt && o >= 0;
-                load_row<kVec>(b.D + (o >= 0 ? o : 0), lane, b.dim, b.is_bf16, x[u]);
+                load_raw<kVec>(b.D + (o >= 0 ? o : 0), lane, b.dim, x[u]);
             }
 #pragma unroll
-            for (int u = 0; u < kDqGather; ++u) {
-                if (use[u]) {
-#pragma unroll
-                    for (int v = 0; v < kVec; ++v) acc[v] = fmaf(w[u], x[u][v], acc[v]);
-                }
+            for (int u = 0; u < kG; ++u) {
+                if (use[u]) fma_raw<kVec>(w[u], x[u], b.is_bf16, acc);
             }
         }
     }
