@@ -15,6 +15,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 
 namespace maxsim {
 
@@ -325,13 +326,46 @@ __device__ __forceinline__ void load_raw(const uint16_t* __restrict__ row, int l
     }
 }
 
-// acc[v] += wgt * element v, in element order (the same FMAs as with decoded rows).
-template <int kVec>
-__device__ __forceinline__ void fma_raw(float wgt, const RawRow<kVec>& r, int32_t is_bf16, float (&acc)[kVec]) {
+// (a0, a1) = w * (x0, x1) + (a0, a1) with one packed instruction; each lane
+// is rounded as a plain fp32 fma.
+__device__ __forceinline__ void fma2_rn(float& a0, float& a1, float w, float x0, float x1) {
+    asm("{\n\t.reg .b64 d, m, x;\n\t"
+        "mov.b64 d, {%0, %1};\n\t"
+        "mov.b64 m, {%2, %2};\n\t"
+        "mov.b64 x, {%3, %4};\n\t"
+        "fma.rn.f32x2 d, m, x, d;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(w), "f"(x0), "f"(x1));
+}
+
+// Two 16-bit values of one word (element 2h in the low half) as fp32.
+template <bool kBf16>
+__device__ __forceinline__ void decode2(uint32_t wd, float& lo, float& hi) {
+    if constexpr (kBf16) {
+        lo = __uint_as_float(wd << 16);
+        hi = __uint_as_float(wd & 0xFFFF0000u);
+    } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wd));
+        lo = f.x;
+        hi = f.y;
+    }
+}
+
+// acc[v] += wgt * element v, element by element (the same fp32 fmas as with
+// decoded rows), two elements per packed instruction.
+template <int kVec, bool kBf16>
+__device__ __forceinline__ void fma_raw(float wgt, const RawRow<kVec>& r, float (&acc)[kVec]) {
 #pragma unroll
-    for (int v = 0; v < kVec; ++v) {
-        const uint16_t h = static_cast<uint16_t>((v & 1) ? (r.w[v >> 1] >> 16) : (r.w[v >> 1] & 0xFFFFu));
-        acc[v] = fmaf(wgt, bits_to_f32(h, is_bf16), acc[v]);
+    for (int h = 0; h < kVec / 2; ++h) {
+        float lo, hi;
+        decode2<kBf16>(r.w[h], lo, hi);
+        fma2_rn(acc[2 * h], acc[2 * h + 1], wgt, lo, hi);
+    }
+    if constexpr (kVec & 1) {
+        float lo, hi;
+        decode2<kBf16>(r.w[kVec / 2], lo, hi);
+        acc[kVec - 1] = fmaf(wgt, lo, acc[kVec - 1]);
     }
 }
 
@@ -408,7 +442,7 @@ inline size_t dd_fused_smem(int32_t nsrc) {
            16;
 }
 
-template <int kVec>
+template <int kVec, bool kBf16>
 __global__ void __launch_bounds__(32 * kDdWarps, 2) dd_fused_kernel(const BwdArgs b) {
     constexpr int kG = kVec <= 4 ? kDdGather : kDdGather / 2;  // wide rows: fewer in flight (registers)
     extern __shared__ __align__(16) uint8_t dd_smem[];
@@ -495,15 +529,14 @@ __global__ void __launch_bounds__(32 * kDdWarps, 2) dd_fused_kernel(const BwdArg
     const int32_t e_end = rs[r1];
     for (int32_t eb = rs[r0]; eb < e_end; eb += 32) {
         const int32_t cnt = min(32, e_end - eb);
-        int64_t off = 0;
+        int32_t rowl = 0;  // Q row of this lane's source
         float wl = 0.f;
         if (lane < cnt) {
             const int32_t n = list[eb + lane];
             const int32_t i = n / b.lq, sq = n - (n / b.lq) * b.lq;
-            const int64_t qr = static_cast<int64_t>(i) * b.lq + sq;
+            rowl = i * b.lq + sq;
             wl = b.g[static_cast<int64_t>(i) * b.nd + j];
-            if (b.q_mask && !b.q_mask[qr]) wl = 0.f;
-            off = qr * b.dim;
+            if (b.q_mask && !b.q_mask[rowl]) wl = 0.f;
         }
         for (int32_t k = 0; k < cnt; k += kG) {
             RawRow<kVec> x[kG];
@@ -512,8 +545,8 @@ __global__ void __launch_bounds__(32 * kDdWarps, 2) dd_fused_kernel(const BwdArg
             for (int u = 0; u < kG; ++u) {
                 const int32_t src = min(k + u, cnt - 1);
                 w[u] = __shfl_sync(0xFFFFFFFFu, wl, src);
-                const int64_t o = __shfl_sync(0xFFFFFFFFu, off, src);
-                load_raw<kVec>(b.Q + o, lane, b.dim, x[u]);
+                const int32_t r = __shfl_sync(0xFFFFFFFFu, rowl, src);
+                load_raw<kVec>(b.Q + static_cast<int64_t>(r) * b.dim, lane, b.dim, x[u]);
             }
 #pragma unroll
             for (int u = 0; u < kG; ++u) {
@@ -526,7 +559,7 @@ __global__ void __launch_bounds__(32 * kDdWarps, 2) dd_fused_kernel(const BwdArg
                         ++row;
                         row_end = rs[row + 1];
                     }
-                    fma_raw<kVec>(w[u], x[u], b.is_bf16, acc);
+                    fma_raw<kVec, kBf16>(w[u], x[u], acc);
                 }
             }
         }
@@ -545,7 +578,7 @@ constexpr int kDqGather = 16;  // D rows loaded together by the dQ gather
 // one chunk the warp writes dQ; with several (gridDim.y > 1, many documents
 // per query row) each chunk writes its partial row to `part` and
 // dq_reduce_kernel adds the chunks in order: a fixed summation order either way.
-template <int kVec>
+template <int kVec, bool kBf16>
 __global__ void __launch_bounds__(256, 4) dq_kernel(const BwdArgs b, float* __restrict__ part) {
     constexpr int kG = kVec <= 4 ? kDqGather : kDqGather / 2;  // wide rows: fewer in flight (registers)
     const int lane = threadIdx.x & 31;
@@ -564,16 +597,14 @@ __global__ void __launch_bounds__(256, 4) dq_kernel(const BwdArgs b, float* __re
     for (int v = 0; v < kVec; ++v) acc[v] = 0.f;
     for (int32_t jb = j_lo; jb < j_hi; jb += 32) {
         const int32_t cnt = min(32, j_hi - jb);
-        int64_t off = 0;
-        float wl = 0.f;  // 0 for a document without a winner (argmax -1)
+        int32_t rowl = -1;  // D row of this lane's document's winner (-1: none)
+        float wl = 0.f;     // 0 for a document without a winner (argmax -1)
         if (lane < cnt) {
             const int32_t j = jb + lane;
             const int32_t a = b.argmax[(static_cast<int64_t>(i) * b.nd + j) * b.lq + s];
             if (a >= 0 && a < doc_len(b, j)) {
                 wl = b.g[static_cast<int64_t>(i) * b.nd + j];
-                off = (doc_row0(b, j) + a) * b.dim;
-            } else {
-                off = -1;
+                rowl = static_cast<int32_t>(doc_row0(b, j) + a);
             }
         }
         for (int32_t k = 0; k < cnt; k += kG) {
@@ -584,13 +615,13 @@ __global__ void __launch_bounds__(256, 4) dq_kernel(const BwdArgs b, float* __re
             for (int u = 0; u < kG; ++u) {
                 const int32_t src = min(k + u, cnt - 1);
                 w[u] = __shfl_sync(0xFFFFFFFFu, wl, src);
-                const int64_t o = __shfl_sync(0xFFFFFFFFu, off, src);
-                use[u] = k + u < cnt && o >= 0;
-                load_raw<kVec>(b.D + (o >= 0 ? o : 0), lane, b.dim, x[u]);
+                const int32_t r = __shfl_sync(0xFFFFFFFFu, rowl, src);
+                use[u] = k + u < cnt && r >= 0;
+                load_raw<kVec>(b.D + static_cast<int64_t>(r >= 0 ? r : 0) * b.dim, lane, b.dim, x[u]);
             }
 #pragma unroll
             for (int u = 0; u < kG; ++u) {
-                if (use[u]) fma_raw<kVec>(w[u], x[u], b.is_bf16, acc);
+                if (use[u]) fma_raw<kVec, kBf16>(w[u], x[u], acc);
             }
         }
     }

@@ -915,14 +915,25 @@ StreamedPlan plan_streamed(int64_t Nq, int64_t Lq, int64_t blk, int64_t Ld, int6
 
 // Document chunks of the dQ gather: enough warps to fill the GPU when a query
 // row has many documents to visit, at least 64 documents per chunk.
-template <int kVec>
+template <int kVec, bool kBf16>
 maxsim_status launch_dd_fused(dim3 grid, size_t shm, cudaStream_t st, const BwdArgs& b) {
     if (shm > 48 * 1024 &&
-        cudaFuncSetAttribute(dd_fused_kernel<kVec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(dd_fused_kernel<kVec, kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(shm)) != cudaSuccess)
         return MAXSIM_ERR_CUDA;
-    dd_fused_kernel<kVec><<<grid, 32 * kDdWarps, shm, st>>>(b);
+    dd_fused_kernel<kVec, kBf16><<<grid, 32 * kDdWarps, shm, st>>>(b);
     return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
+template <int kVec>
+maxsim_status launch_dd_fused_t(dim3 grid, size_t shm, cudaStream_t st, const BwdArgs& b) {
+    return b.is_bf16 ? launch_dd_fused<kVec, true>(grid, shm, st, b) : launch_dd_fused<kVec, false>(grid, shm, st, b);
+}
+
+template <int kVec>
+void launch_dq(dim3 grid, cudaStream_t st, const BwdArgs& b, float* part) {
+    if (b.is_bf16) dq_kernel<kVec, true><<<grid, 256, 0, st>>>(b, part);
+    else dq_kernel<kVec, false><<<grid, 256, 0, st>>>(b, part);
 }
 
 int32_t dq_chunks(int64_t Nq, int64_t lq, int64_t Nd) {
@@ -1010,14 +1021,14 @@ maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void
         static_assert(kDdMaxSrc * 3 + kDdWarps * kDdRows * 4 + (kDdRows + 1) * 4 + 16 <= 227 * 1024, "fused dD smem");
         maxsim_status frc = MAXSIM_OK;
         switch (vec) {
-        case 1: frc = launch_dd_fused<1>(grid, shm, st, b); break;
-        case 2: frc = launch_dd_fused<2>(grid, shm, st, b); break;
-        case 3: frc = launch_dd_fused<3>(grid, shm, st, b); break;
-        case 4: frc = launch_dd_fused<4>(grid, shm, st, b); break;
-        case 5: frc = launch_dd_fused<5>(grid, shm, st, b); break;
-        case 6: frc = launch_dd_fused<6>(grid, shm, st, b); break;
-        case 7: frc = launch_dd_fused<7>(grid, shm, st, b); break;
-        default: frc = launch_dd_fused<8>(grid, shm, st, b); break;
+        case 1: frc = launch_dd_fused_t<1>(grid, shm, st, b); break;
+        case 2: frc = launch_dd_fused_t<2>(grid, shm, st, b); break;
+        case 3: frc = launch_dd_fused_t<3>(grid, shm, st, b); break;
+        case 4: frc = launch_dd_fused_t<4>(grid, shm, st, b); break;
+        case 5: frc = launch_dd_fused_t<5>(grid, shm, st, b); break;
+        case 6: frc = launch_dd_fused_t<6>(grid, shm, st, b); break;
+        case 7: frc = launch_dd_fused_t<7>(grid, shm, st, b); break;
+        default: frc = launch_dd_fused_t<8>(grid, shm, st, b); break;
         }
         if (frc != MAXSIM_OK) return frc;
     } else if (need_csr) {
@@ -1060,14 +1071,14 @@ maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void
         const dim3 grid(static_cast<unsigned>((rows + 7) / 8), static_cast<unsigned>(n_chunks));
         float* part = n_chunks > 1 ? reinterpret_cast<float*>(ws + off_part) : nullptr;
         switch (vec) {
-        case 1: dq_kernel<1><<<grid, 256, 0, st>>>(b, part); break;
-        case 2: dq_kernel<2><<<grid, 256, 0, st>>>(b, part); break;
-        case 3: dq_kernel<3><<<grid, 256, 0, st>>>(b, part); break;
-        case 4: dq_kernel<4><<<grid, 256, 0, st>>>(b, part); break;
-        case 5: dq_kernel<5><<<grid, 256, 0, st>>>(b, part); break;
-        case 6: dq_kernel<6><<<grid, 256, 0, st>>>(b, part); break;
-        case 7: dq_kernel<7><<<grid, 256, 0, st>>>(b, part); break;
-        default: dq_kernel<8><<<grid, 256, 0, st>>>(b, part); break;
+        case 1: launch_dq<1>(grid, st, b, part); break;
+        case 2: launch_dq<2>(grid, st, b, part); break;
+        case 3: launch_dq<3>(grid, st, b, part); break;
+        case 4: launch_dq<4>(grid, st, b, part); break;
+        case 5: launch_dq<5>(grid, st, b, part); break;
+        case 6: launch_dq<6>(grid, st, b, part); break;
+        case 7: launch_dq<7>(grid, st, b, part); break;
+        default: launch_dq<8>(grid, st, b, part); break;
         }
         if (n_chunks > 1)
             dq_reduce_kernel<<<grid_for(rows * dim, 256, dev->num_sms), 256, 0, st>>>(b, part, n_chunks);
