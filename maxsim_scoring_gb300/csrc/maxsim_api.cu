@@ -133,13 +133,14 @@ size_t fwd_smem_bytes(int32_t mt, int32_t k_atoms, int32_t stages, int32_t k8_at
     return b;
 }
 
-// Resident query M-tiles and ring depths: the most query rows per pass, then
+// Resident query M-tiles and ring depths: the most query rows per pass (up to
+// mt_cap M-tiles), then
 // the deepest document rings that fit (the 16-bit operand ring keeps two
 // stages when it can; wide INT8 rows fall back to one). Returns false when
 // nothing fits; the entry points then reject the shape.
-bool choose_pipeline(FwdPlan& p) {
+bool choose_pipeline(FwdPlan& p, int32_t mt_cap) {
     for (int32_t min_stages = 2; min_stages >= 1; --min_stages) {
-        for (int32_t mt = kMaxMT; mt >= 1; --mt) {
+        for (int32_t mt = std::min(kMaxMT, mt_cap); mt >= 1; --mt) {
             if (!p.int8) {
                 if (min_stages < 2 || fwd_smem_bytes(mt, p.k_atoms, 2, 0, 0, p.pair) > kSmemBudget) continue;
                 int32_t s = kMaxStages;
@@ -162,7 +163,8 @@ bool choose_pipeline(FwdPlan& p) {
     return false;
 }
 
-FwdPlan plan_fwd_mode(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varlen_q, bool int8, bool pair) {
+FwdPlan plan_fwd_mode(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varlen_q, bool int8, bool pair,
+                      bool one_query_units) {
     FwdPlan p;
     p.int8 = int8;
     p.pair = pair;
@@ -170,7 +172,11 @@ FwdPlan plan_fwd_mode(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varl
     p.k_atoms = static_cast<int32_t>((dim + 63) / 64);
     p.k8_atoms = int8 ? static_cast<int32_t>((dim + 127) / 128) : 0;
     p.k_steps = static_cast<int32_t>(dim / 16);
-    p.ok = choose_pipeline(p);
+    // resident query M-tiles: no more than one pass over the call's query rows needs
+    // (the memory left goes to the document ring)
+    const int64_t pass_rows =
+        std::min<int64_t>(std::max<int64_t>(one_query_units ? p.lq_pad : nq * p.lq_pad, 1), kBM * kMaxMT);
+    p.ok = choose_pipeline(p, static_cast<int32_t>((pass_rows + kBM - 1) / kBM));
     if (!p.ok) p.mt_max = 1;  // keeps the sizes below defined; the entry points reject the shape
     const int64_t rb_max = static_cast<int64_t>(kBM) * p.mt_max;
     if (p.lq_pad <= rb_max) {
@@ -212,12 +218,12 @@ FwdPlan plan_fwd_mode(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varl
 // per MMA, so the MMAs run at the tensor rate (the single-CTA kernel is bound
 // by shared-memory operand reads at the short tiles of varlen documents), and
 // for INT8 the staging ring and the 16-bit operand ring fit beside four
-// resident query M-tiles. The pair-list walk (allow_pair = false) runs on
-// single CTAs.
-FwdPlan plan_fwd(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varlen_q, bool int8, bool allow_pair = true) {
-    FwdPlan p = plan_fwd_mode(nq, lq, nd, dim, varlen_q, int8, false);
-    if (allow_pair && p.ok && p.n_rb >= 2) {
-        FwdPlan q = plan_fwd_mode(nq, lq, nd, dim, varlen_q, int8, true);
+// resident query M-tiles. The pair-list walk (pair_list = true) runs on
+// single CTAs, one query per unit.
+FwdPlan plan_fwd(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varlen_q, bool int8, bool pair_list = false) {
+    FwdPlan p = plan_fwd_mode(nq, lq, nd, dim, varlen_q, int8, false, pair_list);
+    if (!pair_list && p.ok && p.n_rb >= 2) {
+        FwdPlan q = plan_fwd_mode(nq, lq, nd, dim, varlen_q, int8, true, false);
         if (q.ok && q.n_rb >= 2) return q;
     }
     return p;
@@ -867,7 +873,7 @@ struct TwoStagePlan {
 TwoStagePlan plan_two_stage(int64_t Nq, int64_t Lq, int64_t Nd, int64_t dim, int64_t k1) {
     TwoStagePlan p;
     const FwdPlan p8 = plan_fwd(Nq, Lq, Nd, dim, false, true);
-    const FwdPlan p16 = plan_fwd(Nq, Lq, Nd, dim, true, false, false);
+    const FwdPlan p16 = plan_fwd(Nq, Lq, Nd, dim, true, false, true);
     if (!p8.ok || !p16.ok || p16.n_chunks > 1) return p;
     p.stage_bytes = std::max(p8.ws_bytes, pairs_ws(p16.ws_bytes, Nq, Nq * k1).bytes);
     size_t off = 0;
@@ -1137,7 +1143,7 @@ size_t maxsim_workspace_size(int op, int64_t Nq, int64_t Lq, int64_t Nd, int64_t
     case MAXSIM_OP_FWD_VARLEN:
         return plan_fwd(Nq, Lq, Nd, dim, true, false).ws_bytes;
     case MAXSIM_OP_SCORE_PAIRS:  // Ld carries the number of pairs
-        return pairs_ws(plan_fwd(Nq, Lq, Nd, dim, true, false, false).ws_bytes, Nq, Ld).bytes;
+        return pairs_ws(plan_fwd(Nq, Lq, Nd, dim, true, false, true).ws_bytes, Nq, Ld).bytes;
     case MAXSIM_OP_FWD_INT8:
         return plan_fwd(Nq, Lq, Nd, dim, false, true).ws_bytes;
     case MAXSIM_OP_BWD:
@@ -1294,7 +1300,7 @@ maxsim_status maxsim_score_pairs_packed(const void* Q, const int32_t* cu_seqlens
     if ((max_lq > 0 && (!Q || !aligned16(Q))) || (total_d > 0 && (!D || !aligned16(D))))
         return MAXSIM_ERR_INVALID_ARG;
     if (total_d > kI32Max || Nq * pad_lq(max_lq) > kI32Max || num_pairs > kI32Max) return MAXSIM_ERR_UNSUPPORTED;
-    const FwdPlan p = plan_fwd(Nq, max_lq, Nd, dim, true, false, false);
+    const FwdPlan p = plan_fwd(Nq, max_lq, Nd, dim, true, false, true);
     if (!p.ok || p.n_chunks > 1) return MAXSIM_ERR_UNSUPPORTED;  // one query per unit: up to 4 M-tiles
     const PairsWs pw = pairs_ws(p.ws_bytes, Nq, num_pairs);
     if (workspace_bytes < pw.bytes || !workspace) return MAXSIM_ERR_WORKSPACE;
