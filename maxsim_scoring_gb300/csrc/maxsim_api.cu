@@ -229,13 +229,28 @@ FwdPlan plan_fwd(int64_t nq, int64_t lq, int64_t nd, int64_t dim, bool varlen_q,
     return p;
 }
 
+// Document ranges per row group. A worker (an SM, or an SM pair) runs units
+// u, u + workers, ...: each unit is one row group over 1/n_dr of the document
+// tokens, so a worker's load is ceil(units / workers) / n_dr. Among 1, 2, 4 or
+// 8 ranges per worker and group ("waves") take the smallest load, and the
+// fewest units on a tie (each unit start reloads the query tile and drains
+// the MMA pipeline).
 int64_t choose_doc_ranges(int64_t n_rb, int64_t total_d, int64_t nd, int num_sms) {
     if (nd == 0) return 1;
-    int64_t waves = (total_d * n_rb >= static_cast<int64_t>(num_sms) * 4 * 2048) ? 4 : 1;
-    int64_t n_dr = (static_cast<int64_t>(num_sms) * waves + n_rb - 1) / n_rb;
-    n_dr = std::min<int64_t>(n_dr, std::max<int64_t>(1, total_d / 256));
-    n_dr = std::min<int64_t>(n_dr, nd);
-    return std::max<int64_t>(1, n_dr);
+    const int64_t workers = std::max(1, num_sms);
+    const int64_t cap = std::min<int64_t>(nd, std::max<int64_t>(1, total_d / 256));
+    int64_t best = 1;
+    double best_load = 0.0;
+    for (int64_t waves = 1; waves <= 8; waves *= 2) {
+        const int64_t n_dr = std::max<int64_t>(1, std::min<int64_t>((workers * waves + n_rb - 1) / n_rb, cap));
+        const int64_t units = n_dr * n_rb;
+        const double load = static_cast<double>((units + workers - 1) / workers) / static_cast<double>(n_dr);
+        if (waves == 1 || load < best_load * (1.0 - 1e-9)) {
+            best = n_dr;
+            best_load = load;
+        }
+    }
+    return best;
 }
 
 // ---------------------------------------------------------------- small kernels
