@@ -1001,9 +1001,13 @@ def run_ours(args, rank, world, local_rank):
     l2_gather = None
     if getattr(case, "gather_bytes", None):
         l2 = l2_read_gbs(device)
+        # the step cannot beat moving its HBM bytes at the HBM peak plus its row
+        # gathers at the L2 figure (a lower bound of L2, so this bound is optimistic)
+        bound_ms = 1e3 * (case.bytes / (peaks["hbm_gbs"] * 1e9) + case.gather_bytes / (l2 * 1e9))
         l2_gather = {"bytes_per_launch": case.gather_bytes,
                      "achieved_gbs": round(case.gather_bytes / (ms / 1e3) / 1e9, 1),
                      "l2_read_gbs": round(l2, 1), "frac": round(case.gather_bytes / (ms / 1e3) / 1e9 / l2, 4),
+                     "hbm_plus_l2_bound_ms": round(bound_ms, 5), "frac_hbm_plus_l2": round(bound_ms / ms, 4),
                      "peak_source": "L2 bandwidth measured in this run: 20 back-to-back copies between two "
                                     "24 MiB L2-resident tensors (read + write bytes), best of 5; a "
                                     "streaming copy, so a lower bound of what L2 serves"}
