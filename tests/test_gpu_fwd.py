@@ -118,6 +118,7 @@ def test_repeatable_bitwise():
     (40, 32, 7, 300, 128),   # 1280 query rows: three row blocks
     (8, 128, 5, 260, 128),   # 1024 rows: one full pair of row blocks
     (20, 48, 4, 97, 64),     # padded queries (48 -> 64 rows), 1280 rows
+    (6, 64, 3, 200, 256),    # dim 256 on the CTA pair: two 256-row blocks, four-step K chains
 ])
 def test_several_row_blocks_integer_exact(dtype, shape):
     # more than one 512-row block of query rows; exact integers make every

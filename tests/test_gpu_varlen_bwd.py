@@ -219,6 +219,27 @@ def test_backward_without_csr_equals_csr_path(shape):
     assert_grad(dD2, ref_dD)
 
 
+@pytest.mark.parametrize("Nq", [128, 129])
+def test_backward_shared_memory_csr_size_limit(Nq):
+    # 128 x 128 = 16,384 sources per document is the largest the shared-memory
+    # CSR takes; 129 queries fall back to the CSR in global memory. Both match
+    # the oracle and the path that returns the CSR, bit for bit.
+    Lq, Nd, Ld, dim = 128, 2, 64, 64
+    seed = 43
+    Q = datagen.gaussian_rows(seed, 1, Nq * Lq, dim, "f16").reshape(Nq, Lq, dim)
+    D = datagen.gaussian_rows(seed, 2, Nd * Ld, dim, "f16").reshape(Nd, Ld, dim)
+    g = datagen.normal_f32(seed, 6, Nq * Nd).reshape(Nq, Nd)
+    Qd, Dd = dev_bits(Q, "f16"), dev_bits(D, "f16")
+    _, a = ops.maxsim_fwd(Qd, Dd, want_argmax=True)
+    dQ, dD, _, _ = ops.maxsim_bwd(Qd, Dd, a, dev(g))
+    dQ_c, dD_c, _, _ = ops.maxsim_bwd(Qd, Dd, a, dev(g), want_csr=True)
+    assert ops.device_status() == 0
+    assert torch.equal(dD, dD_c) and torch.equal(dQ, dQ_c)
+    ref_dQ, ref_dD, _, _ = oracle.bwd(Q, D, "f16", a.cpu().numpy(), g)
+    assert_grad(dQ, ref_dQ)
+    assert_grad(dD, ref_dD)
+
+
 def test_backward_without_csr_hot_token():
     # every query token picks token 0 of its document: one destination row gets all sources
     Nq, Lq, Nd, Ld, dim = 64, 128, 2, 300, 64
