@@ -333,11 +333,12 @@ struct alignas(16) SmemCtl {
     uint64_t q_ready;  // pair mode: both CTAs' query rows have landed
     uint64_t acc_full[kNAcc], acc_empty[kNAcc];
     uint64_t mma_done;
-    uint64_t epi_bar;  // rendezvous of the epilogue warps
+    uint64_t epi_bar;                // rendezvous of all epilogue warps
+    uint64_t epi_bar_g[kEpiGroups];  // rendezvous of one epilogue warpgroup
     uint64_t never;    // never arrived at (the fault-handling test hook waits on it)
     uint32_t tmem_base;
     volatile int32_t abort;
-    float wslot[kMaxMT * 4];   // per-warp partial sums of the document being closed
+    float wslot[2][kMaxMT * 4];  // per-warp partial sums of the document being closed (by parity)
 };
 // INT8 mode only: after the control block, a per-warp copy of the tile's
 // document scales, float[kEpiWarps][kBN].
@@ -386,10 +387,10 @@ __device__ __forceinline__ bool wait_bar_warp(const FwdArgs& a, SmemCtl* ctl, ui
 
 // Bounded rendezvous of the epilogue warps (an mbarrier phase per use),
 // so that a warp that gave up on a wait can never strand the others.
-__device__ __forceinline__ bool epi_sync(const FwdArgs& a, SmemCtl* ctl, uint32_t& phase) {
+__device__ __forceinline__ bool epi_sync(const FwdArgs& a, SmemCtl* ctl, uint64_t* bar, uint32_t& phase) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&ctl->epi_bar));
-    const bool ok = wait_bar(a, ctl, smem_u32(&ctl->epi_bar), phase);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(bar));
+    const bool ok = wait_bar(a, ctl, smem_u32(bar), phase);
     phase ^= 1u;
     return ok;
 }
@@ -406,6 +407,25 @@ __device__ __forceinline__ float chunk_max(const float (&x)[32], float m) {
     return fmax3(b1, b2, b3);
 }
 
+// Lowest e with y[e] == cm, where cm is the largest non-NaN entry of y.
+// set.ge turns each column into 1.0 (equal to the maximum) or 0.0 (below it,
+// or NaN), and the flags are added as t_e * 2^-e: the sum lies in
+// [2^-e0, 2^(1-e0)) for the lowest flagged e0 (rounded toward zero, so the
+// lower flags never carry into the next power of two), and its exponent is
+// -e0. One compare (integer pipe) and one FMA (floating-point pipe) per
+// column, in place of a compare and a select on the integer pipe.
+__device__ __forceinline__ int32_t first_equal32(const float (&y)[32], float cm) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        float t;
+        asm("set.ge.f32.f32 %0, %1, %2;" : "=f"(t) : "f"(y[e]), "f"(cm));
+        acc[e >> 3] = __fmaf_rz(t, __uint_as_float(static_cast<uint32_t>(127 - e) << 23), acc[e >> 3]);
+    }
+    const float s = __fadd_rz(__fadd_rz(acc[0], acc[1]), __fadd_rz(acc[2], acc[3]));
+    return 127 - static_cast<int32_t>(__float_as_uint(s) >> 23);
+}
+
 // Fold one 32-column chunk into (m, am); col0 = index of column 0 relative to
 // the document's first token.
 template <bool kArg>
@@ -417,9 +437,7 @@ __device__ __forceinline__ void fold_chunk(const float (&y)[32], int32_t col0, f
         const float cm = chunk_max(y, kNegInf);
         const bool upd = cm > m;  // false for NaN
         if (__any_sync(0xFFFFFFFFu, upd)) {
-            int32_t idx = 31;
-#pragma unroll
-            for (int e = 30; e >= 0; --e) idx = (y[e] == cm) ? e : idx;
+            const int32_t idx = first_equal32(y, cm);
             if (upd) {
                 am = col0 + idx;
                 m = cm;
@@ -434,9 +452,7 @@ __device__ __forceinline__ void fold_chunk(const float (&y)[32], int32_t col0, f
 __device__ __forceinline__ void fold_chunk_max(const float (&y)[32], float cm, int32_t col0, float& m, int32_t& am) {
     const bool upd = cm > m;  // false for NaN
     if (__any_sync(0xFFFFFFFFu, upd)) {
-        int32_t idx = 31;
-#pragma unroll
-        for (int e = 30; e >= 0; --e) idx = (y[e] == cm) ? e : idx;
+        const int32_t idx = first_equal32(y, cm);
         if (upd) {
             am = col0 + idx;
             m = cm;
@@ -519,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(&ctl->mma_done), kMmaWarps);
         mbar_init(smem_u32(&ctl->epi_bar), kEpiWarps);
+        for (int gg = 0; gg < kEpiGroups; ++gg) mbar_init(smem_u32(&ctl->epi_bar_g[gg]), 4);
         mbar_init(smem_u32(&ctl->never), 1);
         ctl->abort = 0;
         fence_barrier_init();
@@ -772,7 +789,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e = ew & 3;                         // TMEM lane quadrant
         const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..32*kEpiWarps-1
         int64_t buf = 0;                              // global index of the tile's first buffer
-        uint32_t epi_phase = 0;
+        uint32_t epi_phase = 0, grp_phase = 0;
+        uint32_t par = 0;  // parity of the documents closed so far (selects the wslot half)
         bool ok = true;
         if (a.inject_wait_ns != 0)  // fault-handling test hook: this wait can only give up
             ok = wait_bar_slow<false>(a, ctl, smem_u32(&ctl->never), 0u, a.inject_wait_ns);
@@ -949,7 +967,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (a.lq_pad < 32 || (a.lq_pad == 32 && !chunked)) {
                             if (in_rb[q] && (lane & (width - 1)) == 0) a.scores[out_index(a, row_i[q], tw.oj)] = val[q];
                         } else if (lane == 0) {
-                            ctl->wslot[k * 4 + e] = val[q];
+                            ctl->wslot[par][k * 4 + e] = val[q];
                         }
                         m[q] = kNegInf;
                         am[q] = -1;
@@ -957,19 +975,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 buf += w.mt;
                 if (closes && (a.lq_pad > 32 || (a.lq_pad == 32 && chunked))) {
-                    if (!epi_sync(a, ctl, epi_phase)) { ok = false; break; }
-                    if (et < rb.nqb) {
-                        const int32_t wpq = a.lq_pad / 32;  // warps per query (capped by the block)
-                        const int32_t wb = et * wpq;
-                        const int32_t we = min(wb + wpq, (rb.row_end - rb.row0) / 32);
+                    // The warps' partial sums of a query are added in slot order by one
+                    // thread after a rendezvous of the warps that wrote them: only the
+                    // owning warpgroup when every query lies inside one M-tile, else all
+                    // epilogue warps. The slots alternate between two halves by document,
+                    // so one rendezvous per document keeps a half from being rewritten
+                    // before it is read (its next writer has passed the rendezvous that
+                    // its reader reaches only after reading).
+                    const int32_t wpq = a.lq_pad / 32;  // warps per query (capped by the block)
+                    const int32_t rows_w = (rb.row_end - rb.row0) / 32;
+                    const float* ws = ctl->wslot[par];
+                    auto sum_query = [&](int32_t qi) {
+                        const int32_t wb = qi * wpq;
+                        const int32_t we = min(wb + wpq, rows_w);
                         float sum = 0.f;
-                        for (int32_t ww = wb; ww < we; ++ww) sum += ctl->wslot[ww];
-                        const int32_t i = rb.q0 + et;
+                        for (int32_t ww = wb; ww < we; ++ww) sum += ws[ww];
+                        const int32_t i = rb.q0 + qi;
                         if (chunked) a.partial[(static_cast<int64_t>(rb.chunk) * a.nq + i) * a.nd + tw.oj] = sum;
                         else a.scores[out_index(a, i, tw.oj)] = sum;
+                    };
+                    if (kBM % a.lq_pad == 0) {
+                        if (g < w.mt) {
+                            if (!epi_sync(a, ctl, &ctl->epi_bar_g[g], grp_phase)) { ok = false; break; }
+                            const int32_t qpm = kBM / a.lq_pad;  // queries per M-tile
+                            const int32_t tg = e * 32 + lane;
+#pragma unroll
+                            for (int q = 0; q < kKPer; ++q) {
+                                const int32_t qi = (g + kEpiGroups * q) * qpm + tg;
+                                if (tg < qpm && qi < rb.nqb) sum_query(qi);
+                            }
+                        }
+                    } else {
+                        if (!epi_sync(a, ctl, &ctl->epi_bar, epi_phase)) { ok = false; break; }
+                        if (et < rb.nqb) sum_query(et);
                     }
-                    if (!epi_sync(a, ctl, epi_phase)) { ok = false; break; }
                 }
+                if (closes) par ^= 1u;
             }
         }
     }
