@@ -74,8 +74,8 @@ constexpr int kAtomBytes = 128 * 128;  // one 128-row x 128-byte swizzled block
 // producer / MMA / prep warpgroup then hands registers to the two epilogue
 // warpgroups, which hold a whole accumulator buffer row (128 values).
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsCtl = 72;
-constexpr int kRegsEpi = 216;
+constexpr int kRegsCtl = 80;
+constexpr int kRegsEpi = 208;
 static_assert(kRegsCtl * 128 + kRegsEpi * 256 <= kRegsLaunch * (128 + 32 * kEpiWarps), "register split");
 constexpr int kMaxStages = 8;
 
@@ -702,6 +702,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // mode each CTA handles its half of the tile's rows.
         const int pt = threadIdx.x - 64;  // 0 .. 32 * kPrepWarps - 1
         constexpr int kPrepThreads = 32 * kPrepWarps;
+        // INT8 widening: when the chunks of a row (dim / 16) divide the prep
+        // threads, each thread keeps one chunk column for the whole kernel
+        const int32_t prep_chunks = a.dim >> 4;
+        const bool prep_fixed_chunk = prep_chunks > 0 && kPrepThreads % prep_chunks == 0;
+        const int32_t prep_c = prep_fixed_chunk ? pt % prep_chunks : 0;
+        const int32_t prep_r0 = prep_fixed_chunk ? pt / prep_chunks : 0;
+        const int32_t prep_rstep = prep_fixed_chunk ? kPrepThreads / prep_chunks : 1;
         int32_t stage = 0, stage8 = 0;
         uint32_t phase = 0, phase8 = 0, q_phase = 0;
         bool ok = true;
@@ -726,9 +733,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(a, ctl, smem_u32(&ctl->d8_full[stage8]), phase8)) { ok = false; break; }
                     if (!wait_bar(a, ctl, smem_u32(&ctl->d_empty[stage]), phase ^ 1u)) { ok = false; break; }
                     const uint8_t* src = sD8 + stage8 * d8_stage_bytes;
-                    const int32_t chunks = a.dim >> 4;  // 16-byte INT8 chunks per row
-                    for (int32_t x = pt; x < rows * chunks; x += kPrepThreads) {
-                        const int32_t r = x / chunks, c = x - (x / chunks) * chunks;
+                    // one 16-byte INT8 chunk (c) of row r: 16 f16 values = two 16-byte
+                    // chunks of a 64-element swizzled atom
+                    auto widen = [&](int32_t r, int32_t c) {
                         const bool nan_row = tr0 + r >= n || (a.d_mask != nullptr && a.d_mask[row0 + r] == 0);
                         uint4 lo, hi;
                         if (nan_row) {
@@ -742,11 +749,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                             lo = i8x8_to_f16x8(v.x, v.y);
                             hi = i8x8_to_f16x8(v.z, v.w);
                         }
-                        // 16 f16 values = two 16-byte chunks of a 64-element swizzled atom
                         const int32_t atom = c >> 2, c16 = (c & 3) * 2;
                         uint8_t* rowp = dst + atom * kDAtom + r * 128;
                         *reinterpret_cast<uint4*>(rowp + (((c16 + 0) ^ (r & 7)) << 4)) = lo;
                         *reinterpret_cast<uint4*>(rowp + (((c16 + 1) ^ (r & 7)) << 4)) = hi;
+                    };
+                    if (prep_fixed_chunk) {
+                        // every thread keeps one chunk column; rows step by the threads
+                        // per chunk column (no division in the loop)
+#pragma unroll 4
+                        for (int32_t r = prep_r0; r < rows; r += prep_rstep) widen(r, prep_c);
+                    } else {
+                        const int32_t chunks = a.dim >> 4;  // 16-byte INT8 chunks per row
+                        for (int32_t x = pt; x < rows * chunks; x += kPrepThreads) {
+                            const int32_t r = x / chunks;
+                            widen(r, x - r * chunks);
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
