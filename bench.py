@@ -200,6 +200,13 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def wait_first(self, timeout_s: float = 3.0):
+        """Block until the sampler has produced its first reading, so that its
+        start-up (driver initialisation) falls before the timed region."""
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout_s:
+            time.sleep(0.01)
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -903,6 +910,7 @@ def run_ours(args, rank, world, local_rank):
 
     clocks = ClockSampler(local_rank)
     clocks.start()
+    clocks.wait_first()
     barrier()
     torch.cuda.synchronize(device)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]

@@ -954,9 +954,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) release_acc(&ctl->acc_empty[slot]);
+                        if (nchunks == 4) {  // a full tile: no branch between the chunks
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (c < nchunks) fold(v[c], c);
+                            for (int c = 0; c < 4; ++c) fold(v[c], c);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                if (c < nchunks) fold(v[c], c);
+                        }
                     }
                 }
                 if (!ok) break;
