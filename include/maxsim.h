@@ -153,7 +153,10 @@ maxsim_status maxsim_score_pairs_packed(const void *Q, const int32_t *cu_seqlens
  * no atomics (Sec. 4.2.2-4.2.3); dQ is reduced row by row in ascending j.
  * Both are bitwise reproducible. Sources with argmax -1 contribute nothing;
  * an argmax outside [-1, Ld) is skipped and reported as
- * MAXSIM_ERR_DEVICE_INPUT by maxsim_device_status().
+ * MAXSIM_ERR_DEVICE_INPUT by maxsim_device_status(). When both dQ and dD (or
+ * the CSR) are asked for, dQ runs on a stream the library owns beside
+ * `stream`, forked after the work already on `stream` and joined back before
+ * the call returns: work enqueued on `stream` afterwards sees both results.
  */
 maxsim_status maxsim_bwd(const void *Q, const void *D, maxsim_dtype dtype,
                          int64_t Nq, int64_t Lq, int64_t Nd, int64_t Ld, int64_t dim,

@@ -974,6 +974,35 @@ size_t bwd_ws_bytes(int64_t Nq, int64_t lq, int64_t Nd, int64_t d_rows, int64_t 
     return off;
 }
 
+// The backward's dQ gather and its dD reduction read the same inputs and
+// write different outputs, so dQ runs on a library stream of its own beside
+// the caller's: forked after the caller's earlier work, joined before the
+// caller's later work. One stream and two events per device; the enqueue of a
+// whole fork / launch / join sequence holds the lock, so calls from several
+// host threads cannot interleave their events.
+struct BwdSide {
+    bool init = false;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_bwd_mu;
+BwdSide g_bwd_side[kMaxDevices];
+
+maxsim_status bwd_side(BwdSide** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MAXSIM_ERR_CUDA;
+    BwdSide& r = g_bwd_side[dev];
+    if (!r.init) {
+        if (cudaStreamCreateWithFlags(&r.stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&r.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&r.join, cudaEventDisableTiming) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        r.init = true;
+    }
+    *out = &r;
+    return MAXSIM_OK;
+}
+
 // Backward for dense (cu_q = cu_d = NULL, ld = the document length) and
 // packed layouts (cu_d given, ld = the longest document).
 maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void* D, const int32_t* cu_d,
@@ -1036,6 +1065,23 @@ maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void
     // memory next to the reduction (the same sorted sources, the same sums)
     const bool fused_dd = dD && !csr_row_ptr && !csr_col && !cu_d && !cu_q && Ld > 0 && Nd > 0 &&
                           Nq * Lq <= kDdMaxSrc;
+    // dQ beside the CSR and dD work when there is any
+    const bool side_dq = dQ && Nq * Lq > 0 && (fused_dd || need_csr || (dD && d_rows > 0));
+    std::unique_lock<std::mutex> side_lock(g_bwd_mu, std::defer_lock);
+    BwdSide* side = nullptr;
+    if (side_dq) {
+        side_lock.lock();
+        if ((rc = bwd_side(&side)) != MAXSIM_OK) return rc;
+        if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+    }
+    // every return after the fork joins the side stream back first
+    auto join = [&](maxsim_status r) -> maxsim_status {
+        if (side && (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
+                     cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess))
+            return MAXSIM_ERR_CUDA;
+        return r;
+    };
     if (fused_dd) {
         const dim3 grid(static_cast<unsigned>(Nd), static_cast<unsigned>((Ld + kDdRows - 1) / kDdRows));
         const size_t shm = dd_fused_smem(static_cast<int32_t>(Nq * Lq));
@@ -1051,7 +1097,7 @@ maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void
         case 7: frc = launch_dd_fused_t<7>(grid, shm, st, b); break;
         default: frc = launch_dd_fused_t<8>(grid, shm, st, b); break;
         }
-        if (frc != MAXSIM_OK) return frc;
+        if (frc != MAXSIM_OK) return join(frc);
     } else if (need_csr) {
         b.doc_cnt = reinterpret_cast<int32_t*>(ws + off_cnt);
         b.doc_base = reinterpret_cast<int32_t*>(ws + off_base);
@@ -1059,7 +1105,7 @@ maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void
         b.col = csr_col ? csr_col : reinterpret_cast<int32_t*>(ws + off_col);
         // packed: rows no document covers (inconsistent offsets) stay empty
         if (cu_d && cudaMemsetAsync(b.row_ptr, 0, static_cast<size_t>(d_rows + 1) * 4, st) != cudaSuccess)
-            return MAXSIM_ERR_CUDA;
+            return join(MAXSIM_ERR_CUDA);
         if (Nd > 0) {
             csr_count_kernel<<<static_cast<int>(Nd), 256, 0, st>>>(b);
         }
@@ -1072,7 +1118,7 @@ maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void
                                      static_cast<int>(shm));
             csr_build_kernel<<<static_cast<int>(Nd), 256, shm, st>>>(b, nw);
         }
-        if (cudaGetLastError() != cudaSuccess) return MAXSIM_ERR_CUDA;
+        if (cudaGetLastError() != cudaSuccess) return join(MAXSIM_ERR_CUDA);
     }
     if (dD && d_rows > 0 && !fused_dd) {
         const int grid = static_cast<int>((d_rows + 7) / 8);
@@ -1091,20 +1137,21 @@ maxsim_status run_bwd(const void* Q, const int32_t* cu_q, int64_t Lq, const void
         const int64_t rows = Nq * Lq;
         const dim3 grid(static_cast<unsigned>((rows + 7) / 8), static_cast<unsigned>(n_chunks));
         float* part = n_chunks > 1 ? reinterpret_cast<float*>(ws + off_part) : nullptr;
+        const cudaStream_t sq = side ? side->stream : st;
         switch (vec) {
-        case 1: launch_dq<1>(grid, st, b, part); break;
-        case 2: launch_dq<2>(grid, st, b, part); break;
-        case 3: launch_dq<3>(grid, st, b, part); break;
-        case 4: launch_dq<4>(grid, st, b, part); break;
-        case 5: launch_dq<5>(grid, st, b, part); break;
-        case 6: launch_dq<6>(grid, st, b, part); break;
-        case 7: launch_dq<7>(grid, st, b, part); break;
-        default: launch_dq<8>(grid, st, b, part); break;
+        case 1: launch_dq<1>(grid, sq, b, part); break;
+        case 2: launch_dq<2>(grid, sq, b, part); break;
+        case 3: launch_dq<3>(grid, sq, b, part); break;
+        case 4: launch_dq<4>(grid, sq, b, part); break;
+        case 5: launch_dq<5>(grid, sq, b, part); break;
+        case 6: launch_dq<6>(grid, sq, b, part); break;
+        case 7: launch_dq<7>(grid, sq, b, part); break;
+        default: launch_dq<8>(grid, sq, b, part); break;
         }
         if (n_chunks > 1)
-            dq_reduce_kernel<<<grid_for(rows * dim, 256, dev->num_sms), 256, 0, st>>>(b, part, n_chunks);
+            dq_reduce_kernel<<<grid_for(rows * dim, 256, dev->num_sms), 256, 0, sq>>>(b, part, n_chunks);
     }
-    return cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+    return join(cudaGetLastError() == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA);
 }
 
 }  // namespace

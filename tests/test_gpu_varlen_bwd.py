@@ -240,6 +240,37 @@ def test_backward_shared_memory_csr_size_limit(Nq):
     assert_grad(dD, ref_dD)
 
 
+def test_backward_side_stream_ordered_with_callers_stream():
+    # dQ runs on a stream of the library's own beside the caller's: the gradient
+    # written on the caller's stream just before each call, and the outputs read
+    # on it just after, must be ordered with it (the stream is kept busy first,
+    # so a missing fork or join would read or return stale data)
+    Nq, Lq, Nd, Ld, dim = 16, 32, 6, 200, 64
+    seed = 47
+    Q = datagen.gaussian_rows(seed, 1, Nq * Lq, dim, "f16").reshape(Nq, Lq, dim)
+    D = datagen.gaussian_rows(seed, 2, Nd * Ld, dim, "f16").reshape(Nd, Ld, dim)
+    g = datagen.normal_f32(seed, 6, Nq * Nd).reshape(Nq, Nd)
+    Qd, Dd = dev_bits(Q, "f16"), dev_bits(D, "f16")
+    _, a = ops.maxsim_fwd(Qd, Dd, want_argmax=True)
+    g_base = dev(g)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    out = []
+    with torch.cuda.stream(s):
+        for rep in range(3):
+            busy = torch.empty(64 << 20, device="cuda").uniform_()
+            gr = g_base * float(rep + 1) + busy[:1] * 0.0
+            dQ, dD, _, _ = ops.maxsim_bwd(Qd, Dd, a, gr)
+            out.append((dQ.clone(), dD.clone()))
+    torch.cuda.synchronize()
+    assert ops.device_status() == 0
+    am = a.cpu().numpy()
+    for rep, (dQ, dD) in enumerate(out):
+        ref_dQ, ref_dD, _, _ = oracle.bwd(Q, D, "f16", am, g * float(rep + 1))
+        assert_grad(dQ, ref_dQ)
+        assert_grad(dD, ref_dD)
+
+
 def test_backward_without_csr_hot_token():
     # every query token picks token 0 of its document: one destination row gets all sources
     Nq, Lq, Nd, Ld, dim = 64, 128, 2, 300, 64
