@@ -138,10 +138,10 @@ def kernel_source_hash(workload: str) -> str:
 # of a smaller instance (the ncu summary of the forward on this workload);
 # valid only for the kernel sources whose hash is recorded with it.
 MEASURED_TRAFFIC = {
-    # (425,494,784 + 3,868,672) B at Nd = 10,000 (1,657,544 tokens), x 16,644,526 / 1,657,544
-    ("colbert_varlen", "e6c7e585e6ca3d91"): 4311530316,
-    # (270,881,792 + 4,037,632) B at Nd = 2,000 documents of 1,024 tokens, x 10,000 / 2,000
-    ("int8_rerank", "e6c7e585e6ca3d91"): 1374597120,
+    # (425,491,456 + 3,865,088) B at Nd = 10,000 (1,657,544 tokens), x 16,644,526 / 1,657,544
+    ("colbert_varlen", "8c0cc3b61b53f37c"): 4311460908,
+    # (270,877,440 + 4,217,600) B at Nd = 2,000 documents of 1,024 tokens, x 10,000 / 2,000
+    ("int8_rerank", "8c0cc3b61b53f37c"): 1375475200,
 }
 
 

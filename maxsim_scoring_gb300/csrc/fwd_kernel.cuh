@@ -872,30 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             TileWalk tw;
             tw.begin(a, w);
             if (kInt8 && tw.valid()) load_scales(tw);
-            // Queries of at most 32 rows whose scores are written by the warp itself:
-            // a closed document's shuffle-sum and score stores wait until the top
-            // of the next tile, where the warp would otherwise idle until that
-            // tile's first accumulator is ready.
-            const bool direct = a.lq_pad < 32 || (a.lq_pad == 32 && !chunked);
-            const int32_t width = min(a.lq_pad, 32);
-            bool pend = false;
-            int32_t pend_oj = 0;
-            float pend_val[kKPer];
-            auto flush_pending = [&]() {
-                for (int o = width >> 1; o > 0; o >>= 1) {
-#pragma unroll
-                    for (int q = 0; q < kKPer; ++q) pend_val[q] += __shfl_xor_sync(0xFFFFFFFFu, pend_val[q], o);
-                }
-#pragma unroll
-                for (int q = 0; q < kKPer; ++q) {
-                    const int k = g + kEpiGroups * q;
-                    if (k >= w.mt) break;
-                    if (in_rb[q] && (lane & (width - 1)) == 0) a.scores[out_index(a, row_i[q], pend_oj)] = pend_val[q];
-                }
-                pend = false;
-            };
             for (; tw.valid() && ok; tw.advance(a)) {
-                if (pend) flush_pending();
                 const int32_t n = tw.ntok(), N = mma_n(n);
                 const int32_t nfull = N >> 5;
                 const bool half = (N & 31) != 0;
@@ -988,24 +965,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (closes && direct) {
-#pragma unroll
-                    for (int q = 0; q < kKPer; ++q) {
-                        const bool has = m[q] > kNegInf;
-                        if (kArg && in_rb[q] && row_s[q] < a.lq_out)
-                            a.argmax[out_index(a, row_i[q], tw.oj) * a.lq_out + row_s[q]] =
-                                (real[q] && has) ? am[q] : -1;
-                        pend_val[q] = (active[q] && has) ? m[q] * qsc[q] : 0.f;
-                        m[q] = kNegInf;
-                        am[q] = -1;
-                    }
-                    pend_oj = tw.oj;
-                    pend = true;
-                } else if (closes) {
-                    // The document ends in this tile (queries of more than 32 rows, or
-                    // chunked). Its reductions come after both M-tiles' loads (off the
-                    // path that hands the accumulator buffers back to the MMA warps),
-                    // the M-tiles' shuffles interleaved; the warps' sums go to wslot.
+                if (closes) {
+                    // The document ends in this tile. Its reductions come after both
+                    // M-tiles' loads (they are off the path that hands the accumulator
+                    // buffers back to the MMA warps), the M-tiles' shuffles interleaved.
                     float val[kKPer];
 #pragma unroll
                     for (int q = 0; q < kKPer; ++q) {
@@ -1015,6 +978,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 (real[q] && has) ? am[q] : -1;
                         val[q] = (active[q] && has) ? m[q] * qsc[q] : 0.f;
                     }
+                    const int32_t width = min(a.lq_pad, 32);
                     for (int o = width >> 1; o > 0; o >>= 1) {
 #pragma unroll
                         for (int q = 0; q < kKPer; ++q) val[q] += __shfl_xor_sync(0xFFFFFFFFu, val[q], o);
@@ -1023,7 +987,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q = 0; q < kKPer; ++q) {
                         const int k = g + kEpiGroups * q;
                         if (k >= w.mt) break;
-                        if (lane == 0) ctl->wslot[par][k * 4 + e] = val[q];
+                        if (a.lq_pad < 32 || (a.lq_pad == 32 && !chunked)) {
+                            if (in_rb[q] && (lane & (width - 1)) == 0) a.scores[out_index(a, row_i[q], tw.oj)] = val[q];
+                        } else if (lane == 0) {
+                            ctl->wslot[par][k * 4 + e] = val[q];
+                        }
                         m[q] = kNegInf;
                         am[q] = -1;
                     }
@@ -1067,7 +1035,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (closes) par ^= 1u;
             }
-            if (pend && ok) flush_pending();
         }
     }
 
