@@ -307,7 +307,9 @@ maxsim_status maxsim_fwd_streamed(const void *Q, const void *D_host, maxsim_dtyp
  *   csr_col      [Nq * Nd * max_lq] i32 (out, optional): sources p = (i*Nd + j)*max_lq + s
  * Deterministic, no atomics on the gradients. Inconsistent offsets, a document
  * longer than max_ld, or an argmax outside its document or past its query's end
- * are skipped and reported as MAXSIM_ERR_DEVICE_INPUT. Workspace:
+ * are skipped and reported as MAXSIM_ERR_DEVICE_INPUT. As for maxsim_bwd, dQ
+ * runs on a library-owned stream beside `stream` when dD or the CSR is also
+ * asked for, joined back before the call returns. Workspace:
  * maxsim_workspace_size(MAXSIM_OP_BWD_VARLEN, Nq, max_lq, Nd, total_d, dim).
  */
 maxsim_status maxsim_bwd_varlen(const void *Q, const int32_t *cu_seqlens_q, int64_t max_lq, const void *D,
